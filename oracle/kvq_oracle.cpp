@@ -1,0 +1,470 @@
+// Plain CPU oracle for low-bit KV-cache quantization and decode attention.
+//
+// TEST INFRASTRUCTURE ONLY. Nothing in the product library links, loads or
+// calls this file; only the tests, the smoke check and the benchmark's CPU
+// baseline do. It shares no code, header or table with the CUDA path.
+//
+// What it computes (step by step, in the order the method states it):
+//   KV Cache量化技术介绍 (developer.horizon.auto/blog/13163), KVQuant section:
+//     "Per-Channel Key Quantization"  -> keys get one scale/zero per channel
+//                                         over a block of tokens;
+//     "Pre-RoPE Key Quantization"     -> keys are quantized before RoPE, and
+//                                         RoPE is applied after dequantization;
+//     "Per-Vector Dense-and-Sparse Quantization" -> each vector's largest
+//                                         |x| elements are kept apart (sparse)
+//                                         and the rest is quantized (dense).
+//   Same page, Quanto section, steps 1-2: block-wise quantization where each
+//     block keeps a scale and a zero_point used to restore the values.
+//   Readings where the page is silent or its formula image was lost (each one
+//   is listed in the design notes): unsigned codes q in [0, L], L = 2^b - 1;
+//   zero z = the block minimum (fp16, exact); scale s = (max - min) / L in fp32,
+//   stored in fp16 rounded toward +infinity; q = clamp(rint((x - z) / s), 0, L)
+//   with fp32 round-to-nearest arithmetic and round-half-to-even; x_hat =
+//   q * s + z; outlier slots hold (index, fp16 value) ordered by descending
+//   |x| then ascending index; a group with max == min has s = 0 and codes 0; a
+//   group whose every element is an outlier has s = 0, z = 0.
+//
+// Build: g++ -O2 -ffp-contract=off -fPIC -shared (no fast-math, no SIMD
+// intrinsics), so every float operation below is one IEEE-754 binary32 or
+// binary64 operation rounded to nearest.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <numeric>
+#include <thread>
+#include <vector>
+
+namespace {
+
+// ---------------------------------------------------------------- binary16
+// IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+
+double half_to_double(uint16_t h) {
+  const int sign = h >> 15;
+  const int e = (h >> 10) & 0x1F;
+  const int f = h & 0x3FF;
+  double v;
+  if (e == 0) {
+    v = std::ldexp(static_cast<double>(f), -24);           // subnormal
+  } else if (e == 31) {
+    v = f ? NAN : INFINITY;
+  } else {
+    v = std::ldexp(static_cast<double>(f | 0x400), e - 25);  // 1.f * 2^(e-15)
+  }
+  return sign ? -v : v;
+}
+
+// Every binary16 value is exactly a binary32 value.
+float half_to_float(uint16_t h) { return static_cast<float>(half_to_double(h)); }
+
+// Encode a non-negative double that is exactly a binary16 value.
+uint16_t encode_exact_half(double v) {
+  if (v == 0.0) return 0;
+  if (v >= 65536.0) return 0x7C00;
+  if (v < std::ldexp(1.0, -14)) {
+    return static_cast<uint16_t>(std::ldexp(v, 24));        // f * 2^-24
+  }
+  int k;
+  std::frexp(v, &k);                                          // v in [2^(k-1), 2^k)
+  const int e = k - 1;                                        // unbiased exponent
+  const double frac = std::ldexp(v, -e) - 1.0;                // in [0, 1)
+  const int f = static_cast<int>(std::ldexp(frac, 10));
+  return static_cast<uint16_t>(((e + 15) << 10) | f);
+}
+
+// Smallest binary16 value >= x, for finite x >= 0 (round toward +infinity).
+uint16_t float_to_half_up(float x) {
+  const double v = static_cast<double>(x);
+  if (v <= 0.0) return 0;
+  if (v > 65504.0) return 0x7C00;
+  double ulp;
+  if (v < std::ldexp(1.0, -14)) {
+    ulp = std::ldexp(1.0, -24);
+  } else {
+    int k;
+    std::frexp(v, &k);
+    ulp = std::ldexp(1.0, (k - 1) - 10);
+  }
+  const double m = std::ceil(v / ulp);                        // exact: ulp is 2^n
+  return encode_exact_half(m * ulp);
+}
+
+// Round half to even, for the finite binary32 quotient of the code step.
+double rint_half_even(float r) {
+  const double x = static_cast<double>(r);
+  const double fl = std::floor(x);
+  const double fr = x - fl;                                   // exact
+  if (fr > 0.5) return fl + 1.0;
+  if (fr < 0.5) return fl;
+  return (std::fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+}
+
+// ---------------------------------------------------------------- method steps
+
+// Dense-and-sparse split of one vector: the n_out indices with the largest
+// |x|; ties go to the lower index; slots ordered by descending |x| then index.
+void select_outliers(const uint16_t* x, int D, int n_out, uint16_t* idx, uint16_t* val) {
+  std::vector<int> order(D);
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+    return half_to_double(x[a] & 0x7FFF) > half_to_double(x[b] & 0x7FFF);
+  });
+  for (int k = 0; k < n_out; ++k) {
+    idx[k] = static_cast<uint16_t>(order[k]);
+    val[k] = x[order[k]];
+  }
+}
+
+// Scale and zero-point of one block (Quanto steps 1-2), over the elements that
+// are not outliers. Returns binary16 bit patterns.
+void group_params(const std::vector<uint16_t>& elems, int bits, uint16_t* s_out, uint16_t* z_out) {
+  if (elems.empty()) {  // every element of the group is an outlier
+    *s_out = 0;
+    *z_out = 0;
+    return;
+  }
+  double mn = INFINITY, mx = -INFINITY;
+  for (uint16_t e : elems) {
+    const double v = half_to_double(e);
+    mn = std::min(mn, v);
+    mx = std::max(mx, v);
+  }
+  const int L = (1 << bits) - 1;
+  // z is the minimum itself; -0 is stored as +0.
+  uint16_t zb = 0;
+  for (uint16_t e : elems) {
+    if (half_to_double(e) == mn) { zb = e; break; }
+  }
+  if (mn == 0.0) zb = 0;
+  const float range = static_cast<float>(mx) - static_cast<float>(mn);  // binary32, RN
+  const float q = range / static_cast<float>(L);                        // binary32, RN
+  *s_out = float_to_half_up(q);
+  *z_out = zb;
+}
+
+// Integer code of one element: clamp(rint((x - z) / s), 0, L).
+int quantize_one(uint16_t x, uint16_t s, uint16_t z, int bits) {
+  const int L = (1 << bits) - 1;
+  if ((s & 0x7FFF) == 0) return 0;
+  const float d = half_to_float(x) - half_to_float(z);       // binary32, RN
+  const float r = d / half_to_float(s);                      // binary32, RN
+  if (!(r > 0.0f)) return 0;
+  if (r >= static_cast<float>(L)) return L;
+  const double n = rint_half_even(r);
+  return static_cast<int>(std::min<double>(n, L));
+}
+
+// LSB-first bit packing of one row: element d occupies bits [b*d, b*d + b).
+void pack_row(const int* codes, int D, int bits, uint8_t* out) {
+  const int nbytes = D * bits / 8;
+  std::memset(out, 0, nbytes);
+  for (int d = 0; d < D; ++d) {
+    for (int k = 0; k < bits; ++k) {
+      if ((codes[d] >> k) & 1) {
+        const int bit = bits * d + k;
+        out[bit / 8] = static_cast<uint8_t>(out[bit / 8] | (1u << (bit % 8)));
+      }
+    }
+  }
+}
+
+int unpack_one(const uint8_t* row, int d, int bits) {
+  int q = 0;
+  for (int k = 0; k < bits; ++k) {
+    const int bit = bits * d + k;
+    q |= ((row[bit / 8] >> (bit % 8)) & 1) << k;
+  }
+  return q;
+}
+
+struct Shape {
+  int T, D, bits, Bk, Gv, n_out;
+  int row_bytes() const { return D * bits / 8; }
+  int n_full() const { return T / Bk; }
+};
+
+bool is_outlier(const uint16_t* idx, int n_out, int c) {
+  for (int k = 0; k < n_out; ++k)
+    if (idx[k] == c) return true;
+  return false;
+}
+
+// Encode one (batch, kv-head) stream of T tokens.
+void encode_stream(const Shape& sh, const uint16_t* K, const uint16_t* V,
+                   uint8_t* k_codes, uint16_t* k_meta, uint16_t* k_tail, uint16_t* k_outl,
+                   uint8_t* v_codes, uint16_t* v_meta, uint16_t* v_outl) {
+  const int D = sh.D, T = sh.T, n_out = sh.n_out, bits = sh.bits;
+  const int rb = sh.row_bytes();
+  const int ng = D / sh.Gv;
+  std::vector<uint16_t> oi(std::max(n_out, 1)), ov(std::max(n_out, 1));
+  std::vector<int> codes(D);
+
+  // Values: per token, per group of Gv channels.
+  for (int t = 0; t < T; ++t) {
+    const uint16_t* x = V + static_cast<size_t>(t) * D;
+    select_outliers(x, D, n_out, oi.data(), ov.data());
+    for (int k = 0; k < n_out; ++k) {
+      v_outl[(static_cast<size_t>(t) * n_out + k) * 2 + 0] = oi[k];
+      v_outl[(static_cast<size_t>(t) * n_out + k) * 2 + 1] = ov[k];
+    }
+    for (int g = 0; g < ng; ++g) {
+      std::vector<uint16_t> dense;
+      for (int c = g * sh.Gv; c < (g + 1) * sh.Gv; ++c)
+        if (!is_outlier(oi.data(), n_out, c)) dense.push_back(x[c]);
+      uint16_t s, z;
+      group_params(dense, bits, &s, &z);
+      v_meta[(static_cast<size_t>(t) * ng + g) * 2 + 0] = s;
+      v_meta[(static_cast<size_t>(t) * ng + g) * 2 + 1] = z;
+      for (int c = g * sh.Gv; c < (g + 1) * sh.Gv; ++c) codes[c] = quantize_one(x[c], s, z, bits);
+    }
+    pack_row(codes.data(), D, bits, v_codes + static_cast<size_t>(t) * rb);
+  }
+
+  // Keys: per channel over each completed block of Bk tokens.
+  const int nb = sh.n_full();
+  std::vector<uint16_t> blk_idx(static_cast<size_t>(sh.Bk) * std::max(n_out, 1));
+  for (int b = 0; b < nb; ++b) {
+    const int t0 = b * sh.Bk;
+    for (int j = 0; j < sh.Bk; ++j) {
+      const int t = t0 + j;
+      const uint16_t* x = K + static_cast<size_t>(t) * D;
+      select_outliers(x, D, n_out, oi.data(), ov.data());
+      for (int k = 0; k < n_out; ++k) {
+        blk_idx[static_cast<size_t>(j) * n_out + k] = oi[k];
+        k_outl[(static_cast<size_t>(t) * n_out + k) * 2 + 0] = oi[k];
+        k_outl[(static_cast<size_t>(t) * n_out + k) * 2 + 1] = ov[k];
+      }
+    }
+    std::vector<uint16_t> s_c(D), z_c(D);
+    for (int c = 0; c < D; ++c) {
+      std::vector<uint16_t> dense;
+      for (int j = 0; j < sh.Bk; ++j)
+        if (!is_outlier(&blk_idx[static_cast<size_t>(j) * n_out], n_out, c))
+          dense.push_back(K[static_cast<size_t>(t0 + j) * D + c]);
+      group_params(dense, bits, &s_c[c], &z_c[c]);
+      k_meta[(static_cast<size_t>(b) * D + c) * 2 + 0] = s_c[c];
+      k_meta[(static_cast<size_t>(b) * D + c) * 2 + 1] = z_c[c];
+    }
+    for (int j = 0; j < sh.Bk; ++j) {
+      const int t = t0 + j;
+      for (int c = 0; c < D; ++c)
+        codes[c] = quantize_one(K[static_cast<size_t>(t) * D + c], s_c[c], z_c[c], bits);
+      pack_row(codes.data(), D, bits, k_codes + static_cast<size_t>(t) * rb);
+    }
+  }
+  // Tokens of the unfinished block stay as fp16 keys.
+  for (int t = nb * sh.Bk; t < T; ++t)
+    std::memcpy(k_tail + static_cast<size_t>(t - nb * sh.Bk) * D, K + static_cast<size_t>(t) * D,
+                sizeof(uint16_t) * D);
+}
+
+// x_hat = q * s + z (binary64), outlier positions restored, tail keys as fp16.
+void dequant_stream(const Shape& sh, const uint8_t* k_codes, const uint16_t* k_meta,
+                    const uint16_t* k_tail, const uint16_t* k_outl, const uint8_t* v_codes,
+                    const uint16_t* v_meta, const uint16_t* v_outl, double* Kh, double* Vh) {
+  const int D = sh.D, T = sh.T, n_out = sh.n_out, bits = sh.bits;
+  const int rb = sh.row_bytes();
+  const int ng = D / sh.Gv;
+  const int nb = sh.n_full();
+  for (int t = 0; t < T; ++t) {
+    const uint8_t* vr = v_codes + static_cast<size_t>(t) * rb;
+    for (int c = 0; c < D; ++c) {
+      const int g = c / sh.Gv;
+      const double s = half_to_double(v_meta[(static_cast<size_t>(t) * ng + g) * 2 + 0]);
+      const double z = half_to_double(v_meta[(static_cast<size_t>(t) * ng + g) * 2 + 1]);
+      Vh[static_cast<size_t>(t) * D + c] = unpack_one(vr, c, bits) * s + z;
+    }
+    for (int k = 0; k < n_out; ++k) {
+      const uint16_t i = v_outl[(static_cast<size_t>(t) * n_out + k) * 2 + 0];
+      const uint16_t v = v_outl[(static_cast<size_t>(t) * n_out + k) * 2 + 1];
+      Vh[static_cast<size_t>(t) * D + i] = half_to_double(v);
+    }
+    if (t < nb * sh.Bk) {
+      const int b = t / sh.Bk;
+      const uint8_t* kr = k_codes + static_cast<size_t>(t) * rb;
+      for (int c = 0; c < D; ++c) {
+        const double s = half_to_double(k_meta[(static_cast<size_t>(b) * D + c) * 2 + 0]);
+        const double z = half_to_double(k_meta[(static_cast<size_t>(b) * D + c) * 2 + 1]);
+        Kh[static_cast<size_t>(t) * D + c] = unpack_one(kr, c, bits) * s + z;
+      }
+      for (int k = 0; k < n_out; ++k) {
+        const uint16_t i = k_outl[(static_cast<size_t>(t) * n_out + k) * 2 + 0];
+        const uint16_t v = k_outl[(static_cast<size_t>(t) * n_out + k) * 2 + 1];
+        Kh[static_cast<size_t>(t) * D + i] = half_to_double(v);
+      }
+    } else {
+      for (int c = 0; c < D; ++c)
+        Kh[static_cast<size_t>(t) * D + c] =
+            half_to_double(k_tail[static_cast<size_t>(t - nb * sh.Bk) * D + c]);
+    }
+  }
+}
+
+// Rotary embedding, rotate-half pairing (i, i + D/2), angle pos * theta^(-2i/D).
+void rope(const double* x, int D, double pos, double theta, double* y) {
+  const int h = D / 2;
+  for (int i = 0; i < h; ++i) {
+    const double phi = pos * std::pow(theta, -2.0 * i / D);
+    const double c = std::cos(phi), s = std::sin(phi);
+    y[i] = x[i] * c - x[i + h] * s;
+    y[i + h] = x[i + h] * c + x[i] * s;
+  }
+}
+
+// Exact (binary64) softmax attention of G query heads over one stream.
+void attention_stream(int T, int D, int G, const double* Kh, const double* Vh, const uint16_t* q,
+                      double q_pos, double pos_offset, double theta, double sm_scale, double* out) {
+  std::vector<double> qr(D), kr(D), sc(T), qd(D);
+  std::vector<double> Krot(static_cast<size_t>(T) * D);
+  for (int t = 0; t < T; ++t) {
+    if (theta > 0.0)
+      rope(Kh + static_cast<size_t>(t) * D, D, t + pos_offset, theta, &Krot[static_cast<size_t>(t) * D]);
+    else
+      std::memcpy(&Krot[static_cast<size_t>(t) * D], Kh + static_cast<size_t>(t) * D, sizeof(double) * D);
+  }
+  for (int h = 0; h < G; ++h) {
+    for (int d = 0; d < D; ++d) qd[d] = half_to_double(q[static_cast<size_t>(h) * D + d]);
+    if (theta > 0.0)
+      rope(qd.data(), D, q_pos + pos_offset, theta, qr.data());
+    else
+      qr = qd;
+    double mx = -INFINITY;
+    for (int t = 0; t < T; ++t) {
+      double acc = 0.0;
+      for (int d = 0; d < D; ++d) acc += qr[d] * Krot[static_cast<size_t>(t) * D + d];
+      sc[t] = sm_scale * acc;
+      mx = std::max(mx, sc[t]);
+    }
+    double den = 0.0;
+    for (int t = 0; t < T; ++t) {
+      sc[t] = std::exp(sc[t] - mx);
+      den += sc[t];
+    }
+    for (int d = 0; d < D; ++d) {
+      double acc = 0.0;
+      for (int t = 0; t < T; ++t) acc += sc[t] * Vh[static_cast<size_t>(t) * D + d];
+      out[static_cast<size_t>(h) * D + d] = acc / den;
+    }
+  }
+}
+
+template <typename F>
+void parallel_for(int n, int nthreads, F f) {
+  if (nthreads <= 1 || n <= 1) {
+    for (int i = 0; i < n; ++i) f(i);
+    return;
+  }
+  std::vector<std::thread> pool;
+  const int nt = std::min(n, nthreads);
+  for (int w = 0; w < nt; ++w)
+    pool.emplace_back([=, &f]() {
+      for (int i = w; i < n; i += nt) f(i);
+    });
+  for (auto& th : pool) th.join();
+}
+
+bool shape_ok(int T, int D, int bits, int Bk, int Gv, int n_out) {
+  if (T < 0 || D <= 0 || D % 2 || Bk <= 0 || Gv <= 0 || D % Gv) return false;
+  if (bits < 1 || bits > 8 || (D * bits) % 8) return false;
+  if (n_out < 0 || n_out > D) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kvqo_encode(int P, int T, int D, int bits, int Bk, int Gv, int n_out, const uint16_t* K,
+                const uint16_t* V, uint8_t* k_codes, uint16_t* k_meta, uint16_t* k_tail,
+                uint16_t* k_outl, uint8_t* v_codes, uint16_t* v_meta, uint16_t* v_outl,
+                int nthreads) {
+  if (!shape_ok(T, D, bits, Bk, Gv, n_out) || P < 0) return 1;
+  const Shape sh{T, D, bits, Bk, Gv, n_out};
+  const size_t td = static_cast<size_t>(T) * D;
+  const size_t rows = static_cast<size_t>(T) * sh.row_bytes();
+  const size_t km = static_cast<size_t>(sh.n_full()) * D * 2;
+  const size_t kt = static_cast<size_t>(Bk) * D;
+  const size_t ol = static_cast<size_t>(T) * n_out * 2;
+  const size_t vm = static_cast<size_t>(T) * (D / Gv) * 2;
+  parallel_for(P, nthreads, [&](int p) {
+    std::memset(k_codes + p * rows, 0, rows);
+    std::memset(k_outl + p * ol, 0, ol * sizeof(uint16_t));
+    std::memset(k_tail + p * kt, 0, kt * sizeof(uint16_t));
+    encode_stream(sh, K + p * td, V + p * td, k_codes + p * rows, k_meta + p * km, k_tail + p * kt,
+                  k_outl + p * ol, v_codes + p * rows, v_meta + p * vm, v_outl + p * ol);
+  });
+  return 0;
+}
+
+int kvqo_dequant(int P, int T, int D, int bits, int Bk, int Gv, int n_out, const uint8_t* k_codes,
+                 const uint16_t* k_meta, const uint16_t* k_tail, const uint16_t* k_outl,
+                 const uint8_t* v_codes, const uint16_t* v_meta, const uint16_t* v_outl,
+                 double* Kh, double* Vh, int nthreads) {
+  if (!shape_ok(T, D, bits, Bk, Gv, n_out) || P < 0) return 1;
+  const Shape sh{T, D, bits, Bk, Gv, n_out};
+  const size_t td = static_cast<size_t>(T) * D;
+  const size_t rows = static_cast<size_t>(T) * sh.row_bytes();
+  const size_t km = static_cast<size_t>(sh.n_full()) * D * 2;
+  const size_t kt = static_cast<size_t>(Bk) * D;
+  const size_t ol = static_cast<size_t>(T) * n_out * 2;
+  const size_t vm = static_cast<size_t>(T) * (D / Gv) * 2;
+  parallel_for(P, nthreads, [&](int p) {
+    dequant_stream(sh, k_codes + p * rows, k_meta + p * km, k_tail + p * kt, k_outl + p * ol,
+                   v_codes + p * rows, v_meta + p * vm, v_outl + p * ol, Kh + p * td, Vh + p * td);
+  });
+  return 0;
+}
+
+int kvqo_attention(int P, int T, int D, int G, const double* Kh, const double* Vh,
+                   const uint16_t* q, double q_pos, double pos_offset, double theta,
+                   double sm_scale, double* out, int nthreads) {
+  if (P < 0 || T <= 0 || D <= 0 || D % 2 || G <= 0) return 1;
+  const size_t td = static_cast<size_t>(T) * D;
+  const size_t gd = static_cast<size_t>(G) * D;
+  parallel_for(P, nthreads, [&](int p) {
+    attention_stream(T, D, G, Kh + p * td, Vh + p * td, q + p * gd, q_pos, pos_offset, theta,
+                     sm_scale, out + p * gd);
+  });
+  return 0;
+}
+
+// Single-step entry points, used by the pins.
+int kvqo_select_outliers(int D, const uint16_t* x, int n_out, uint16_t* idx, uint16_t* val) {
+  if (D <= 0 || n_out < 0 || n_out > D) return 1;
+  select_outliers(x, D, n_out, idx, val);
+  return 0;
+}
+
+int kvqo_group_params(int n, const uint16_t* x, const uint8_t* excluded, int bits, uint16_t* s,
+                      uint16_t* z) {
+  std::vector<uint16_t> dense;
+  for (int i = 0; i < n; ++i)
+    if (!excluded || !excluded[i]) dense.push_back(x[i]);
+  group_params(dense, bits, s, z);
+  return 0;
+}
+
+int kvqo_quantize(int n, const uint16_t* x, uint16_t s, uint16_t z, int bits, int* codes) {
+  for (int i = 0; i < n; ++i) codes[i] = quantize_one(x[i], s, z, bits);
+  return 0;
+}
+
+uint16_t kvqo_half_up(float x) { return float_to_half_up(x); }
+
+double kvqo_half_to_double(uint16_t h) { return half_to_double(h); }
+
+int kvqo_pack_row(int D, const int* codes, int bits, uint8_t* out) {
+  if ((D * bits) % 8) return 1;
+  pack_row(codes, D, bits, out);
+  return 0;
+}
+
+int kvqo_rope(int D, const double* x, double pos, double theta, double* y) {
+  if (D % 2) return 1;
+  rope(x, D, pos, theta, y);
+  return 0;
+}
+
+}  // extern "C"
