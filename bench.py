@@ -1,0 +1,509 @@
+#!/usr/bin/env python
+"""Benchmark of the low-bit KV-cache decode hot path on GB300.
+
+A step is one decode step of one layer: append one new token for every
+(batch, kv-head) stream (kvq_append), then decode attention for every query
+head over the whole cache (kvq_decode_attn: split-T partial kernel + combine).
+The default workload is the 7B-style MHA cache (B=8, H=32/32, D=128, T=32768,
+INT4, RoPE theta 1e4). Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--mode decode|prefill] [--impl kvq|reference]
+
+--impl reference times the CPU oracle (the plain C++ reference) on the host
+cores, on a bounded sample of the same workload per step, extrapolated to the
+full step. --mode prefill times one kvq_append of the workload's whole
+context (the aggressive-bits prefill run) instead of decode steps.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import platform
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import kvq_inputs as ki  # noqa: E402
+
+L2_BYTES = 129 * 2 ** 20
+DECODE_SOURCES = ["kvq_decode.cuh", "kvq_decode.cu", "kvq_decode_inst.cuh", "kvq_common.cuh"]
+
+
+# ----------------------------------------------------------------------------- helpers
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def n_out_of(w):
+    return 0 if w.outlier_frac == 0 else max(1, int(math.floor(w.outlier_frac * w.D)))
+
+
+def decode_alg_bytes(w, T):
+    """Algorithmic bytes one decode call must read/write: packed K and V codes,
+    fp16 key metadata per block and channel, fp16 value metadata per token and
+    group, outlier pairs, the fp16 tail keys, q and out."""
+    streams = w.B * w.H_kv
+    cb = w.D * w.bits // 8
+    ng = w.D // w.value_group
+    nout = n_out_of(w)
+    nf, tail = divmod(T, w.key_block)
+    per_block = 2 * cb * w.key_block + 4 * w.D + 4 * ng * w.key_block + 2 * 4 * nout * w.key_block
+    per_tail_tok = 2 * w.D + cb + 4 * ng + 4 * nout
+    qo = 2 * w.B * w.H_q * w.D * 2
+    return streams * (nf * per_block + tail * per_tail_tok) + qo
+
+
+def append_alg_bytes(w, n_new):
+    """Prefill append: fp16 K and V read, codes + metadata + outliers written."""
+    streams = w.B * w.H_kv
+    cb = w.D * w.bits // 8
+    ng = w.D // w.value_group
+    nout = n_out_of(w)
+    nb = n_new // w.key_block
+    read = 2 * streams * n_new * w.D * 2
+    write = streams * (2 * n_new * cb + nb * w.D * 4 + n_new * ng * 4 + 2 * n_new * nout * 4)
+    return read + write
+
+
+def source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "bit_quantized_kv_append_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(kernel_file, sha):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", kernel_file)
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if "=" in line and not line.lstrip().startswith("#"):
+            k, v = line.split("=", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("source_sha") != sha or "traffic_bytes_per_launch" not in vals:
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except ValueError:
+        return None
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def physical_gpu(local_index):
+    """nvidia-smi's id of a CUDA device index (honours CUDA_VISIBLE_DEVICES)."""
+    cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "").strip()
+    if cvd:
+        items = [x.strip() for x in cvd.split(",")]
+        if local_index < len(items):
+            return items[local_index]
+    return str(local_index)
+
+
+def host_cpu():
+    model = platform.processor() or platform.machine()
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                model = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    return model
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+def oracle_step_seconds(w, n_streams, n_tok, reps=1):
+    """Wall time of the oracle doing one decode step on n_streams streams of
+    n_tok cached tokens each, all host threads in use: encode the new token,
+    dequantize the cache, float64 attention of the stream's G heads."""
+    from oracle import oracle_cpp as oc
+
+    streams = [(s // w.H_kv % w.B, s % w.H_kv) for s in range(n_streams)]
+    K, V = ki.streams_np(w, streams, n_tok + 1)
+    enc = oc.encode(K[:, :n_tok], V[:, :n_tok], w.bits, w.key_block, w.value_group, n_out_of(w))
+    q = ki.queries_np(w, 0, 0)
+    qs = np.stack([q[b, h * w.G:(h + 1) * w.G] for (b, h) in streams])
+    threads = oc.default_threads()
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oc.encode(K[:, n_tok:], V[:, n_tok:], w.bits, w.key_block, w.value_group, n_out_of(w), threads)
+        Kh, Vh = oc.dequant(enc, n_tok, w.D, w.bits, w.key_block, w.value_group, n_out_of(w), threads)
+        oc.attention(Kh, Vh, qs, n_tok, w.rope_theta, 1.0 / math.sqrt(w.D), 0.0, threads)
+        times.append(time.perf_counter() - t0)
+    return statistics.median(times), threads
+
+
+def cpu_baseline(w, budget_s=15.0):
+    """Oracle on a bounded sample: one stream per host thread, the full T each,
+    extrapolated to all B*H_kv streams."""
+    from oracle import oracle_cpp as oc
+    threads = oc.default_threads()
+    n_streams = min(threads, w.B * w.H_kv)
+    n_tok = w.T
+    t_probe, _ = oracle_step_seconds(w, 1, min(n_tok, 4096))
+    est = t_probe * (n_tok / min(n_tok, 4096)) * math.ceil(n_streams / threads)
+    if est > budget_s:
+        n_tok = max(w.key_block, int(n_tok * budget_s / est) // w.key_block * w.key_block)
+    t, threads = oracle_step_seconds(w, n_streams, n_tok)
+    full = t * (w.T / n_tok) * (w.B * w.H_kv / n_streams)
+    return {
+        "value": w.B / full, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+        "sample": (f"{n_streams} of {w.B * w.H_kv} (b,h_kv) streams x {n_tok} of {w.T} cached tokens, "
+                   f"one decode step (encode new token, dequantize, float64 attention), "
+                   f"{t:.2f} s wall, extrapolated linearly to the full step; host {host_cpu()}"),
+    }
+
+
+# ----------------------------------------------------------------------------- GPU runs
+def build_cache(w, T, T_max, device, layer=0, rope_table=None):
+    import bit_quantized_kv_append_gb300 as kvq
+    cache = kvq.QuantizedKVCache(w.B, w.H_kv, w.D, T_max, w.bits, w.key_block, w.value_group,
+                                 w.outlier_frac, H_q=w.H_q, rope_theta=w.rope_theta, device=device,
+                                 rope_table=rope_table)
+    chunk = max(w.key_block, (1 << 26) // max(1, w.B * w.H_kv * w.D) // w.key_block * w.key_block)
+    t = 0
+    while t < T:
+        n = min(chunk, T - t)
+        K, V = ki.kv_torch(w, layer, t, n, device)
+        cache.append(K, V)
+        t += n
+    return cache
+
+
+def run_decode(args, w, rank, world, device):
+    import torch
+    import torch.distributed as dist
+
+    T = w.T
+    T_max = T + w.key_block
+    n_layers = w.layers
+    cache0 = build_cache(w, T, T_max, device)
+    caches = [cache0] + [build_cache(w, T, T_max, device, layer=l, rope_table=cache0.rope)
+                         for l in range(1, n_layers)]
+    k1, v1 = ki.kv_torch(w, 0, T, 1, device)
+    q = ki.queries_torch(w, 0, 1, device)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream()
+
+    def step(i, ev=None):
+        c = caches[i % n_layers]
+        c.reset(T)
+        c.append(k1, v1)
+        if ev is not None:
+            ev[0].record(stream)
+        c.decode(q, out=out)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = ClockSampler(physical_gpu(torch.cuda.current_device()))
+    clocks.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(i, evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    ms = t_start.elapsed_time(t_end)
+    dec_ms = [a.elapsed_time(b) for a, b in evs]
+
+    # end to end through the public API from pinned host buffers
+    kh, vh, qh = k1.cpu().pin_memory(), v1.cpu().pin_memory(), q.cpu().pin_memory()
+    oh = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    kd, vd, qd = torch.empty_like(k1), torch.empty_like(v1), torch.empty_like(q)
+
+    def e2e_step(i):
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        qd.copy_(qh, non_blocking=True)
+        c = caches[i % n_layers]
+        c.reset(T)
+        c.append(kd, vd)
+        c.decode(qd, out=out)
+        oh.copy_(out, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e_start.elapsed_time(e_end)
+
+    times = torch.tensor([ms, e2e_ms, statistics.mean(dec_ms)], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    ms, e2e_ms, dec_mean = (float(x) for x in times.cpu())
+    bytes_step_in = (k1.numel() + v1.numel() + q.numel()) * 2
+    bytes_step_out = out.numel() * 2
+    alg = decode_alg_bytes(w, T + 1)
+    peak, peak_kind = measured_peaks()
+    achieved = alg / (dec_mean * 1e-3) / 1e9
+    sha = source_sha(DECODE_SOURCES)
+    line = {
+        "metric": "decode-attn tokens/s (one layer; B query tokens per step)",
+        "value": world * w.B * args.steps / (ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": (f"{w.name}: B={w.B} H_q={w.H_q} H_kv={w.H_kv} D={w.D} T={T} INT{w.bits} "
+                         f"key_block={w.key_block} value_group={w.value_group} outliers={w.outlier_frac} "
+                         f"rope_theta={w.rope_theta} layers_resident={n_layers}"),
+            "step": "kvq_append of 1 token per stream + kvq_decode_attn over T+1 tokens",
+            "l2": f"inputs larger than L2 (cache {caches[0].layout.cache_bytes / 1e9:.2f} GB per layer > 129 MB); no flush",
+            "parallelism": f"replicas x{world}",
+            "kv_tokens_per_s": world * w.B * (T + 1) * args.steps / (ms * 1e-3),
+            "model_level_tokens_per_s_32_layers": world * w.B * args.steps / (ms * 1e-3) / 32,
+            "decode_call_ms": dec_mean,
+        },
+        "e2e": {"value": world * w.B * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": bytes_step_in, "d2h_bytes_per_step": bytes_step_out},
+        "gpu_launches": 3 * args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "kernel": "decode_partial_kernel (+ combine, timed together per call)",
+                     "alg_bytes_per_launch": alg,
+                     "traffic": profile_traffic(f"decode_partial_{w.name}.txt", sha),
+                     "source_sha": sha},
+        "clocks": clk,
+    }
+    return line
+
+
+def run_prefill(args, w, rank, world, device):
+    import torch
+    import torch.distributed as dist
+    import bit_quantized_kv_append_gb300 as kvq
+
+    n_new = w.T
+    T_max = n_new
+    cache = kvq.QuantizedKVCache(w.B, w.H_kv, w.D, T_max, w.bits, w.key_block, w.value_group,
+                                 w.outlier_frac, H_q=w.H_q, device=device)
+    K, V = ki.kv_torch(w, 0, 0, n_new, device)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        cache.reset(0)
+        cache.append(K, V)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = ClockSampler(physical_gpu(torch.cuda.current_device()))
+    clocks.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        cache.reset(0)
+        evs[i][0].record(stream)
+        cache.append(K, V)
+        evs[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    call_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    # end to end: fp16 K/V copied from pinned host memory each step
+    Kh, Vh = K.cpu().pin_memory(), V.cpu().pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        K.copy_(Kh, non_blocking=True)
+        V.copy_(Vh, non_blocking=True)
+        cache.reset(0)
+        cache.append(K, V)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    alg = append_alg_bytes(w, n_new)
+    peak, peak_kind = measured_peaks()
+    achieved = alg / (call_ms * 1e-3) / 1e9
+    sha = source_sha(["kvq_append.cu", "kvq_common.cuh"])
+    toks = w.B * w.H_kv * n_new
+    return {
+        "metric": "append (prefill quantize) kv-tokens/s",
+        "value": world * toks * args.steps / (ms * 1e-3), "unit": "kv-tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{w.name} prefill: B={w.B} H_kv={w.H_kv} D={w.D} n_new={n_new} INT{w.bits} "
+                               f"key_block={w.key_block} value_group={w.value_group} outliers={w.outlier_frac}",
+                   "l2": f"inputs larger than L2 ({2 * toks * w.D * 2 / 1e9:.2f} GB fp16 in); no flush",
+                   "parallelism": f"replicas x{world}"},
+        "e2e": {"value": world * toks * args.steps / (e2e_ms * 1e-3), "unit": "kv-tokens/s",
+                "h2d_bytes_per_step": 2 * toks * w.D * 2, "d2h_bytes_per_step": 0},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": peak_kind, "kernel": "append_kernel", "alg_bytes_per_launch": alg,
+                     "traffic": profile_traffic(f"append_{w.name}.txt", sha), "source_sha": sha},
+        "clocks": clk,
+    }
+
+
+def run_reference(args, w):
+    """The CPU oracle as the reference arm: each step a bounded sample of the
+    workload's decode step, extrapolated to the full step."""
+    from oracle import oracle_cpp as oc
+    oc.build()
+    threads = oc.default_threads()
+    n_streams = min(threads, w.B * w.H_kv)
+    budget = max(0.02, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    t_probe, _ = oracle_step_seconds(w, n_streams, min(w.T, 1024))
+    n_tok = min(w.T, max(w.key_block, int(1024 * budget / max(t_probe, 1e-6)) // w.key_block * w.key_block))
+    full = []
+    for i in range(args.warmup + args.steps):
+        t, threads = oracle_step_seconds(w, n_streams, n_tok)
+        if i >= args.warmup:
+            full.append(t * (w.T / n_tok) * (w.B * w.H_kv / n_streams))
+    step_s = statistics.mean(full)
+    value = w.B / step_s
+    sample = (f"per step {n_streams} of {w.B * w.H_kv} (b,h_kv) streams x {n_tok} of {w.T} tokens "
+              f"(encode new token, dequantize, float64 attention), extrapolated; host {host_cpu()}")
+    return {
+        "impl": "reference", "metric": "decode-attn tokens/s (one layer; B query tokens per step)",
+        "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: B={w.B} H_q={w.H_q} H_kv={w.H_kv} D={w.D} T={w.T} INT{w.bits}"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    ap.add_argument("--workload", default="mha7b", choices=list(ki.WORKLOADS))
+    ap.add_argument("--mode", default="decode", choices=["decode", "prefill"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = ki.WORKLOADS[args.workload]
+    rank, local_rank, world = dist_env()
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, w)), flush=True)
+        return
+
+    import torch
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    from bit_quantized_kv_append_gb300 import build as kbuild
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if rank == 0:
+        kbuild.build()
+    if world > 1:
+        dist.barrier()
+    device = torch.device("cuda", local_rank if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(device)
+    line = (run_prefill if args.mode == "prefill" else run_decode)(args, w, rank, world, device)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            if args.mode == "decode":
+                line["cpu_baseline"] = cpu_baseline(w)
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,162 @@
+// C ABI of libkvq: argument checks, buffer layout, and kernel launches.
+// Every check runs on the host before any launch; the library never
+// allocates, frees or synchronizes.
+#include <math.h>
+#include <string.h>
+
+#include "kvq_common.cuh"
+
+namespace kvq {
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int n_outliers(const kvq_config& c) {
+  if (!(c.outlier_frac > 0.0f)) return 0;
+  int n = (int)floor((double)c.outlier_frac * (double)c.D);
+  return n < 1 ? 1 : n;
+}
+
+// Fills `d` from `cfg`; returns a status.
+int make_dims(const kvq_config* cfg, Dims* d) {
+  if (!cfg || !d) return KVQ_ERR_ARG;
+  const kvq_config& c = *cfg;
+  if (c.B < 1 || c.H_kv < 1 || c.T_max < 1) return KVQ_ERR_UNSUPPORTED;
+  if (c.bits < 2 || c.bits > 4) return KVQ_ERR_UNSUPPORTED;
+  if (c.D != 64 && c.D != 128) return KVQ_ERR_UNSUPPORTED;
+  if (c.key_block != 64 && c.key_block != 128) return KVQ_ERR_UNSUPPORTED;
+  if (c.value_group != 32 && c.value_group != 64 && c.value_group != 128) return KVQ_ERR_UNSUPPORTED;
+  if (c.D % c.value_group) return KVQ_ERR_UNSUPPORTED;
+  if (c.T_max % c.key_block || c.T_max >= (1 << 24)) return KVQ_ERR_UNSUPPORTED;
+  if (!(c.outlier_frac >= 0.0f) || c.outlier_frac > 1.0f) return KVQ_ERR_UNSUPPORTED;
+  const int n_out = n_outliers(c);
+  if (n_out > KVQ_MAX_OUTLIERS) return KVQ_ERR_UNSUPPORTED;
+  if ((int64_t)c.B * c.H_kv > 65535) return KVQ_ERR_UNSUPPORTED;  // grid.y
+  d->B = c.B;
+  d->H_kv = c.H_kv;
+  d->D = c.D;
+  d->T_max = c.T_max;
+  d->bits = c.bits;
+  d->Bk = c.key_block;
+  d->Gv = c.value_group;
+  d->n_out = n_out;
+  d->cb = c.D * c.bits / 8;
+  d->ng = c.D / c.value_group;
+  d->n_blk = c.T_max / c.key_block;
+  d->rope_n_hi = rope_n_hi(d->n_blk);
+  return KVQ_OK;
+}
+
+bool cache_ptrs_ok(const Dims& d, const kvq_cache& c) {
+  const void* must[] = {c.k_codes, c.k_meta, c.k_tail, c.v_codes, c.v_meta};
+  for (const void* p : must)
+    if (!p || !aligned16(p)) return false;
+  if (d.n_out > 0) {
+    if (!c.k_outl || !c.v_outl || !aligned16(c.k_outl) || !aligned16(c.v_outl)) return false;
+  }
+  return c.T_cur >= 0 && c.T_cur <= d.T_max;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
+
+}  // namespace
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" {
+
+int kvq_layout(const kvq_config* cfg, int32_t H_q, kvq_layout_t* out) {
+  if (!cfg || !out) return KVQ_ERR_ARG;
+  Dims d;
+  int rc = make_dims(cfg, &d);
+  if (rc) return rc;
+  if (H_q < 1 || H_q % d.H_kv) return KVQ_ERR_UNSUPPORTED;
+  memset(out, 0, sizeof(*out));
+  const size_t streams = (size_t)d.B * d.H_kv;
+  out->stream_bytes[KVQ_K_CODES] = k_codes_stream(d);
+  out->stream_bytes[KVQ_K_META] = k_meta_stream(d) * 4;
+  out->stream_bytes[KVQ_K_TAIL] = k_tail_stream(d) * 2;
+  out->stream_bytes[KVQ_K_OUTL] = outl_stream(d) * 4;
+  out->stream_bytes[KVQ_V_CODES] = k_codes_stream(d);
+  out->stream_bytes[KVQ_V_META] = v_meta_stream(d) * 4;
+  out->stream_bytes[KVQ_V_OUTL] = outl_stream(d) * 4;
+  for (int i = 0; i < KVQ_NBUF; ++i) {
+    out->bytes[i] = out->stream_bytes[i] * streams;
+    out->cache_bytes += out->bytes[i];
+  }
+  out->fp16_equiv_bytes = 2 * streams * (size_t)d.T_max * d.D * 2;
+  out->rope_bytes = rope_entries(d) * sizeof(float2);
+  out->workspace_bytes = (size_t)d.B * H_q * max_splits(d) * (d.D + 2) * sizeof(float);
+  out->n_out = d.n_out;
+  out->code_row_bytes = d.cb;
+  return KVQ_OK;
+}
+
+int kvq_rope_init(const kvq_config* cfg, double rope_theta, void* rope_tab, size_t rope_bytes,
+                  void* stream) {
+  Dims d;
+  int rc = make_dims(cfg, &d);
+  if (rc) return rc;
+  if (!rope_tab || !aligned16(rope_tab) || !(rope_theta > 0.0) || !isfinite(rope_theta))
+    return KVQ_ERR_ARG;
+  if (rope_bytes < rope_entries(d) * sizeof(float2)) return KVQ_ERR_WORKSPACE;
+  return cuda_status(launch_rope_init(d, rope_theta, static_cast<float2*>(rope_tab),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int kvq_append(const kvq_config* cfg, kvq_cache* cache, const void* k_new, const void* v_new,
+               int32_t n_new, void* stream) {
+  Dims d;
+  int rc = make_dims(cfg, &d);
+  if (rc) return rc;
+  if (!cache || n_new < 0 || !cache_ptrs_ok(d, *cache)) return KVQ_ERR_ARG;
+  if (n_new == 0) return KVQ_OK;
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_ARG;
+  if ((int64_t)cache->T_cur + n_new > d.T_max) return KVQ_ERR_CAPACITY;
+  rc = cuda_status(launch_append(d, *cache, static_cast<const __half*>(k_new),
+                                 static_cast<const __half*>(v_new), n_new,
+                                 static_cast<cudaStream_t>(stream)));
+  if (rc == KVQ_OK) cache->T_cur += n_new;
+  return rc;
+}
+
+int kvq_decode_attn(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t H_q,
+                    int32_t q_pos, const void* rope_tab, float sm_scale, void* out,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  Dims d;
+  int rc = make_dims(cfg, &d);
+  if (rc) return rc;
+  if (H_q < 1 || H_q % d.H_kv) return KVQ_ERR_UNSUPPORTED;
+  const int G = H_q / d.H_kv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return KVQ_ERR_UNSUPPORTED;
+  if (!cache || !cache_ptrs_ok(d, *cache) || cache->T_cur < 1) return KVQ_ERR_ARG;
+  if (!q || !out || !workspace || !aligned16(q) || !aligned16(out) || !aligned16(workspace))
+    return KVQ_ERR_ARG;
+  if (q_pos < 0 || q_pos >= d.T_max || !isfinite(sm_scale)) return KVQ_ERR_ARG;
+  if (rope_tab && !aligned16(rope_tab)) return KVQ_ERR_ARG;
+  kvq_layout_t lay;
+  rc = kvq_layout(cfg, H_q, &lay);
+  if (rc) return rc;
+  if (workspace_bytes < lay.workspace_bytes) return KVQ_ERR_WORKSPACE;
+  return cuda_status(launch_decode(d, *cache, static_cast<const __half*>(q), H_q, q_pos,
+                                   static_cast<const float2*>(rope_tab), sm_scale,
+                                   static_cast<__half*>(out), static_cast<float*>(workspace),
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+const char* kvq_status_string(int status) {
+  switch (status) {
+    case KVQ_OK: return "KVQ_OK";
+    case KVQ_ERR_ARG: return "KVQ_ERR_ARG: invalid argument (NULL/misaligned pointer, bad count or position)";
+    case KVQ_ERR_UNSUPPORTED: return "KVQ_ERR_UNSUPPORTED: configuration outside the supported set";
+    case KVQ_ERR_CAPACITY: return "KVQ_ERR_CAPACITY: T_cur + n_new exceeds T_max";
+    case KVQ_ERR_WORKSPACE: return "KVQ_ERR_WORKSPACE: workspace or table smaller than kvq_layout() requires";
+    case KVQ_ERR_CUDA: return "KVQ_ERR_CUDA: CUDA launch error";
+    default: return "KVQ_ERR_UNKNOWN";
+  }
+}
+
+const char* kvq_version(void) { return "kvq 0.1.0 sm_103a"; }
+
+}  // extern "C"

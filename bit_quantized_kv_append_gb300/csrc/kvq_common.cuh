@@ -1,0 +1,64 @@
+// Internal definitions shared by the libkvq translation units (not installed).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+// Shape of one layer's cache as the kernels see it (derived from kvq_config).
+struct Dims {
+  int B, H_kv, D, T_max, bits, Bk, Gv;
+  int n_out;      // outliers per vector
+  int cb;         // code row bytes = D*bits/8
+  int ng;         // value groups per token = D/Gv
+  int n_blk;      // key blocks per stream = T_max/Bk
+  int rope_n_hi;  // rows of the coarse RoPE table
+};
+
+// Strides (elements of the buffer's own unit) of one (b, h_kv) stream.
+__host__ __device__ inline size_t k_codes_stream(const Dims& d) { return (size_t)d.T_max * d.cb; }
+__host__ __device__ inline size_t k_meta_stream(const Dims& d) { return (size_t)d.n_blk * d.D; }     // uint32 {s,z}
+__host__ __device__ inline size_t k_tail_stream(const Dims& d) { return (size_t)d.Bk * d.D; }        // half
+__host__ __device__ inline size_t outl_stream(const Dims& d) { return (size_t)d.T_max * d.n_out; }   // uint32 {idx,val}
+__host__ __device__ inline size_t v_meta_stream(const Dims& d) { return (size_t)d.T_max * d.ng; }    // uint32 {s,z}
+
+// RoPE table: three float2 {cos, sin} tables of rotate-half frequencies
+// w_i = theta^(-2i/D), i < D/2:
+//   fine   [D/2][Bk]     angle j * w_i,          j < Bk         (offset in a block)
+//   coarse [256][D/2]    angle Bk * m * w_i,     m < 256        (block index, low byte)
+//   hi     [n_hi][D/2]   angle 256 * Bk * m * w_i               (block index, high part)
+// A position p = Bk * (256 * m_hi + m_lo) + j is R(p) = R_hi(m_hi) R_lo(m_lo) R_fine(j).
+constexpr int kRopeLo = 256;
+__host__ __device__ inline int rope_n_hi(int n_blk) { return (n_blk - 1) / kRopeLo + 1; }
+__host__ __device__ inline size_t rope_fine_off(const Dims&) { return 0; }
+__host__ __device__ inline size_t rope_lo_off(const Dims& d) { return (size_t)(d.D / 2) * d.Bk; }
+__host__ __device__ inline size_t rope_hi_off(const Dims& d) { return rope_lo_off(d) + (size_t)kRopeLo * (d.D / 2); }
+__host__ __device__ inline size_t rope_entries(const Dims& d) { return rope_hi_off(d) + (size_t)d.rope_n_hi * (d.D / 2); }
+
+// Decode split-T scratch: per (b, h_q, split) the partial output o[D], then m, l.
+constexpr int kMaxSplits = 256;
+__host__ __device__ inline int max_splits(const Dims& d) {
+  return d.n_blk + 1 < kMaxSplits ? d.n_blk + 1 : kMaxSplits;
+}
+
+__device__ __forceinline__ float h2f(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+
+// cos/sin of the composed rotation R(a) R(b) = R(a + b).
+__device__ __forceinline__ float2 rot_compose(float2 a, float2 b) {
+  return make_float2(__fsub_rn(__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y)),
+                     __fadd_rn(__fmul_rn(a.y, b.x), __fmul_rn(a.x, b.y)));
+}
+
+// Launch helpers (defined in the kernel translation units).
+cudaError_t launch_rope_init(const Dims& d, double theta, float2* tab, cudaStream_t st);
+cudaError_t launch_append(const Dims& d, const kvq_cache& c, const __half* k_new,
+                          const __half* v_new, int n_new, cudaStream_t st);
+cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, int H_q, int q_pos,
+                          const float2* rope, float sm_scale, __half* out, float* ws,
+                          cudaStream_t st);
+
+}  // namespace kvq

@@ -1,0 +1,43 @@
+// Launch and occupancy helpers of the decode partial kernel; included by one
+// translation unit per code width so the instantiations compile in parallel.
+#pragma once
+
+#include "kvq_decode.cuh"
+
+namespace kvq {
+
+template <int BITS, int D, int G>
+cudaError_t launch_partial(const DecodeArgs& a, cudaStream_t st) {
+  const dim3 grid(a.n_split, a.d.B * a.d.H_kv);
+  decode_partial_kernel<BITS, D, G><<<grid, kDecThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int BITS, int D, int G>
+int partial_occupancy() {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_partial_kernel<BITS, D, G>,
+                                                    kDecThreads, 0) != cudaSuccess)
+    n = 1;
+  return n < 1 ? 1 : n;
+}
+
+#define KVQ_INSTANTIATE_DECODE(BITS)                                               \
+  template cudaError_t launch_partial<BITS, 64, 1>(const DecodeArgs&, cudaStream_t);  \
+  template cudaError_t launch_partial<BITS, 64, 2>(const DecodeArgs&, cudaStream_t);  \
+  template cudaError_t launch_partial<BITS, 64, 4>(const DecodeArgs&, cudaStream_t);  \
+  template cudaError_t launch_partial<BITS, 64, 8>(const DecodeArgs&, cudaStream_t);  \
+  template cudaError_t launch_partial<BITS, 128, 1>(const DecodeArgs&, cudaStream_t); \
+  template cudaError_t launch_partial<BITS, 128, 2>(const DecodeArgs&, cudaStream_t); \
+  template cudaError_t launch_partial<BITS, 128, 4>(const DecodeArgs&, cudaStream_t); \
+  template cudaError_t launch_partial<BITS, 128, 8>(const DecodeArgs&, cudaStream_t); \
+  template int partial_occupancy<BITS, 64, 1>();                                    \
+  template int partial_occupancy<BITS, 64, 2>();                                    \
+  template int partial_occupancy<BITS, 64, 4>();                                    \
+  template int partial_occupancy<BITS, 64, 8>();                                    \
+  template int partial_occupancy<BITS, 128, 1>();                                   \
+  template int partial_occupancy<BITS, 128, 2>();                                   \
+  template int partial_occupancy<BITS, 128, 4>();                                   \
+  template int partial_occupancy<BITS, 128, 8>();
+
+}  // namespace kvq

@@ -1,0 +1,208 @@
+"""Python binding of libkvq (ctypes): argument marshalling only.
+
+Every step of append and decode runs in the library's CUDA kernels; PyTorch
+only provides device memory and streams. There is no CPU fallback: if the
+library is missing, the calls raise.
+
+Entry points mirror include/kvq.h: ``layout``, ``rope_init``, ``append``,
+``decode_attn``. ``QuantizedKVCache`` owns one layer's buffers.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+
+BUFFERS = ("k_codes", "k_meta", "k_tail", "k_outl", "v_codes", "v_meta", "v_outl")
+STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "KVQ_ERR_CAPACITY",
+          4: "KVQ_ERR_WORKSPACE", 5: "KVQ_ERR_CUDA"}
+EXPORTS = ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_decode_attn",
+           "kvq_status_string", "kvq_version")
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({_status_string(status)})")
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H_kv", ctypes.c_int32), ("D", ctypes.c_int32),
+                ("T_max", ctypes.c_int32), ("bits", ctypes.c_int32),
+                ("key_block", ctypes.c_int32), ("value_group", ctypes.c_int32),
+                ("outlier_frac", ctypes.c_float)]
+
+
+class Layout(ctypes.Structure):
+    _fields_ = [("bytes", ctypes.c_size_t * 7), ("stream_bytes", ctypes.c_size_t * 7),
+                ("cache_bytes", ctypes.c_size_t), ("fp16_equiv_bytes", ctypes.c_size_t),
+                ("rope_bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t),
+                ("n_out", ctypes.c_int32), ("code_row_bytes", ctypes.c_int32)]
+
+
+class CacheRef(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_void_p) for name in BUFFERS] + [("T_cur", ctypes.c_int32)]
+
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvq.so")
+_LIB = None
+
+
+def lib():
+    """The loaded libkvq.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libkvq.so is not built ({LIB_PATH}); run "
+                               "`python -m bit_quantized_kv_append_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32 = ctypes.c_void_p, ctypes.c_int32
+        L.kvq_layout.argtypes = [ctypes.POINTER(Config), i32, ctypes.POINTER(Layout)]
+        L.kvq_rope_init.argtypes = [ctypes.POINTER(Config), ctypes.c_double, vp, ctypes.c_size_t, vp]
+        L.kvq_append.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp, vp, i32, vp]
+        L.kvq_decode_attn.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp, i32, i32,
+                                      vp, ctypes.c_float, vp, vp, ctypes.c_size_t, vp]
+        L.kvq_status_string.argtypes = [ctypes.c_int]
+        L.kvq_status_string.restype = ctypes.c_char_p
+        L.kvq_version.restype = ctypes.c_char_p
+        for fn in ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_decode_attn"):
+            getattr(L, fn).restype = ctypes.c_int
+        _LIB = L
+    return _LIB
+
+
+def _status_string(status: int) -> str:
+    try:
+        return lib().kvq_status_string(status).decode()
+    except Exception:  # noqa: BLE001 - message only
+        return "?"
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise KvqError(rc, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None or t.numel() == 0 else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_config(B, H_kv, D, T_max, bits=4, key_block=64, value_group=64, outlier_frac=0.0) -> Config:
+    return Config(B, H_kv, D, T_max, bits, key_block, value_group, float(outlier_frac))
+
+
+def layout(cfg: Config, H_q: int) -> Layout:
+    out = Layout()
+    _check(lib().kvq_layout(ctypes.byref(cfg), int(H_q), ctypes.byref(out)), "kvq_layout")
+    return out
+
+
+def rope_init(cfg: Config, theta: float, table: torch.Tensor, stream=None):
+    _check(lib().kvq_rope_init(ctypes.byref(cfg), float(theta), _ptr(table), table.numel() * table.element_size(),
+                               _stream(stream)), "kvq_rope_init")
+
+
+def append(cfg: Config, ref: CacheRef, k_new: torch.Tensor, v_new: torch.Tensor, n_new: int, stream=None):
+    _check(lib().kvq_append(ctypes.byref(cfg), ctypes.byref(ref), _ptr(k_new), _ptr(v_new), int(n_new),
+                            _stream(stream)), "kvq_append")
+
+
+def decode_attn(cfg: Config, ref: CacheRef, q: torch.Tensor, H_q: int, q_pos: int,
+                rope: Optional[torch.Tensor], sm_scale: float, out: torch.Tensor,
+                workspace: torch.Tensor, stream=None):
+    _check(lib().kvq_decode_attn(ctypes.byref(cfg), ctypes.byref(ref), _ptr(q), int(H_q), int(q_pos),
+                                 _ptr(rope), float(sm_scale), _ptr(out), _ptr(workspace),
+                                 workspace.numel(), _stream(stream)), "kvq_decode_attn")
+
+
+class QuantizedKVCache:
+    """One layer's low-bit KV cache in device memory (buffers sized by kvq_layout)."""
+
+    def __init__(self, B, H_kv, D, T_max, bits=4, key_block=64, value_group=64, outlier_frac=0.0,
+                 H_q=None, rope_theta=0.0, device="cuda", rope_table: Optional[torch.Tensor] = None):
+        self.cfg = make_config(B, H_kv, D, T_max, bits, key_block, value_group, outlier_frac)
+        self.H_q = H_q or H_kv
+        self.layout = layout(self.cfg, self.H_q)
+        self.device = torch.device(device)
+        self.buffers = {name: torch.empty(self.layout.bytes[i], dtype=torch.uint8, device=self.device)
+                        for i, name in enumerate(BUFFERS)}
+        self.workspace = torch.empty(self.layout.workspace_bytes, dtype=torch.uint8, device=self.device)
+        self.rope_theta = float(rope_theta)
+        self.rope = rope_table
+        if self.rope is None and self.rope_theta > 0:
+            self.rope = torch.empty(self.layout.rope_bytes, dtype=torch.uint8, device=self.device)
+            rope_init(self.cfg, self.rope_theta, self.rope)
+        self.T_cur = 0
+
+    # -- shape helpers
+    @property
+    def n_out(self) -> int:
+        return self.layout.n_out
+
+    def ref(self) -> CacheRef:
+        r = CacheRef()
+        for name in BUFFERS:
+            t = self.buffers[name]
+            setattr(r, name, None if t.numel() == 0 else t.data_ptr())
+        r.T_cur = self.T_cur
+        return r
+
+    def views(self) -> dict:
+        """Typed views of the buffers, shaped as include/kvq.h documents."""
+        c = self.cfg
+        n_out, cb = self.layout.n_out, self.layout.code_row_bytes
+        B, H, T = c.B, c.H_kv, c.T_max
+        bf = self.buffers
+        return {
+            "k_codes": bf["k_codes"].view(B, H, T, cb),
+            "k_meta": bf["k_meta"].view(torch.int16).view(B, H, T // c.key_block, c.D, 2),
+            "k_tail": bf["k_tail"].view(torch.float16).view(B, H, c.key_block, c.D),
+            "k_outl": bf["k_outl"].view(torch.int16).view(B, H, T, n_out, 2),
+            "v_codes": bf["v_codes"].view(B, H, T, cb),
+            "v_meta": bf["v_meta"].view(torch.int16).view(B, H, T, c.D // c.value_group, 2),
+            "v_outl": bf["v_outl"].view(torch.int16).view(B, H, T, n_out, 2),
+        }
+
+    def reset(self, T_cur: int = 0):
+        self.T_cur = int(T_cur)
+
+    # -- the two paths
+    def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
+        """k_new, v_new: fp16 [B, H_kv, n, D] on the cache's device (pre-RoPE keys)."""
+        c = self.cfg
+        for t in (k_new, v_new):
+            if t.dtype != torch.float16 or not t.is_contiguous() or t.device != self.device:
+                raise ValueError("k_new/v_new must be contiguous fp16 tensors on the cache device")
+            if t.dim() != 4 or t.shape[0] != c.B or t.shape[1] != c.H_kv or t.shape[3] != c.D:
+                raise ValueError(f"expected [B={c.B}, H_kv={c.H_kv}, n, D={c.D}], got {tuple(t.shape)}")
+        if k_new.shape != v_new.shape:
+            raise ValueError("k_new and v_new shapes differ")
+        ref = self.ref()
+        append(self.cfg, ref, k_new, v_new, k_new.shape[2], stream)
+        self.T_cur = ref.T_cur
+
+    def decode(self, q: torch.Tensor, q_pos: Optional[int] = None, sm_scale: Optional[float] = None,
+               out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        """q: fp16 [B, H_q, D] pre-RoPE at position q_pos (default T_cur - 1)."""
+        c = self.cfg
+        if q.dtype != torch.float16 or not q.is_contiguous() or q.device != self.device:
+            raise ValueError("q must be a contiguous fp16 tensor on the cache device")
+        if tuple(q.shape) != (c.B, self.H_q, c.D):
+            raise ValueError(f"expected q [B={c.B}, H_q={self.H_q}, D={c.D}], got {tuple(q.shape)}")
+        if out is None:
+            out = torch.empty_like(q)
+        q_pos = self.T_cur - 1 if q_pos is None else q_pos
+        sm_scale = 1.0 / math.sqrt(c.D) if sm_scale is None else sm_scale
+        decode_attn(self.cfg, self.ref(), q, self.H_q, q_pos, self.rope, sm_scale, out,
+                    self.workspace, stream)
+        return out

@@ -1,0 +1,180 @@
+/*
+ * kvq.h -- C ABI of libkvq: low-bit KV-cache append and decode attention,
+ * written for NVIDIA GB300 (sm_103a).
+ *
+ * Method (KV Cache量化技术介绍, developer.horizon.auto/blog/13163):
+ *   KVQuant, "Per-Channel Key Quantization"       keys: one scale/zero per
+ *                                                  channel over a token block;
+ *   KVQuant, "Pre-RoPE Key Quantization"          keys are stored pre-RoPE and
+ *                                                  rotated after dequantization;
+ *   KVQuant, "Per-Vector Dense-and-Sparse ..."    each vector's largest-|x|
+ *                                                  elements kept as fp16 pairs;
+ *   Quanto, "Quanto 的量化原理" steps 1-2          block-wise codes with a
+ *                                                  scale and zero_point each.
+ * Arithmetic of one code (the page's formula image is lost; this is the
+ * reading the library implements and its oracle checks bit for bit):
+ *   z = min over the group's dense elements (fp16, exact; -0 stored as +0)
+ *   s = fp16_round_up(fp32(fp32(max - min) / L)),  L = 2^bits - 1
+ *   q = clamp(rint_half_even(fp32(fp32(x - z) / s)), 0, L)   (q = 0 if s = 0)
+ *   x_hat = q * s + z, except at outlier positions, which hold the fp16 value.
+ *
+ * Conventions for every entry point:
+ *   - Ownership: the caller allocates and frees every device buffer, using the
+ *     sizes kvq_layout() returns. The library allocates nothing, frees
+ *     nothing and never synchronizes the device or the stream.
+ *   - Pointers: device pointers unless marked "host"; each must be 16-byte
+ *     aligned (cudaMalloc and the PyTorch caching allocator return 256-byte
+ *     aligned memory). A buffer whose size is 0 may be NULL.
+ *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *     default stream). Work is enqueued asynchronously; inputs must stay
+ *     valid and unmodified until the stream has executed the call.
+ *   - Errors: every function returns a kvq_status. Arguments are checked on
+ *     the host before anything is launched; on any error nothing is launched
+ *     and no output or cache field changes. KVQ_ERR_CUDA reports a launch
+ *     error (cudaGetLastError after the launch; no synchronization).
+ *   - Devices: calls run on the calling thread's current CUDA device; the
+ *     buffers must belong to that device.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvq_status {
+  KVQ_OK = 0,
+  KVQ_ERR_ARG = 1,          /* NULL or misaligned pointer, negative count, q_pos out of range */
+  KVQ_ERR_UNSUPPORTED = 2,  /* a configuration outside the supported set (see kvq_config) */
+  KVQ_ERR_CAPACITY = 3,     /* T_cur + n_new > T_max */
+  KVQ_ERR_WORKSPACE = 4,    /* workspace or RoPE table smaller than kvq_layout() says */
+  KVQ_ERR_CUDA = 5          /* the CUDA runtime reported an error at launch */
+} kvq_status;
+
+#define KVQ_MAX_OUTLIERS 8  /* largest n_out per vector */
+
+/* One layer's cache shape. Supported: bits in {2, 3, 4}; D in {64, 128};
+ * key_block in {64, 128}; value_group in {32, 64, 128} dividing D;
+ * T_max > 0 a multiple of key_block and < 2^24; B, H_kv >= 1, B*H_kv <= 65535;
+ * outlier_frac = 0 (no outliers) or in (0, 1]: n_out = max(1, floor(frac*D)),
+ * at most KVQ_MAX_OUTLIERS (frac = 0.01 gives n_out = 1 for D = 64 or 128). */
+typedef struct kvq_config {
+  int32_t B;            /* sequences in the batch (all hold T_cur tokens) */
+  int32_t H_kv;         /* key/value heads */
+  int32_t D;            /* head_dim */
+  int32_t T_max;        /* token capacity per sequence */
+  int32_t bits;         /* code width */
+  int32_t key_block;    /* Bk: tokens per key-quantization block */
+  int32_t value_group;  /* Gv: channels per value-quantization group */
+  float outlier_frac;   /* fraction of each K and V vector kept as fp16 outliers */
+} kvq_config;
+
+/* Cache buffers. Every buffer is [B][H_kv][...] with each (b, h_kv) stream
+ * contiguous; "fp16" means IEEE binary16 bits in a uint16.
+ *   K_CODES [B][H_kv][T_max][D*bits/8]   packed key codes; row t is an
+ *            LSB-first bitstream, element d at bits [bits*d, bits*d + bits)
+ *   K_META  [B][H_kv][T_max/Bk][D][2]    fp16 {s, z} per key block and channel
+ *   K_TAIL  [B][H_kv][Bk][D]             fp16 keys of the unfinished block,
+ *            token t at row t % Bk
+ *   K_OUTL  [B][H_kv][T_max][n_out][2]   {uint16 channel, fp16 value} per key
+ *            vector of a finished block, descending |x| then ascending channel
+ *   V_CODES [B][H_kv][T_max][D*bits/8]   packed value codes (same packing)
+ *   V_META  [B][H_kv][T_max][D/Gv][2]    fp16 {s, z} per token and group
+ *   V_OUTL  [B][H_kv][T_max][n_out][2]   {channel, fp16 value} per value vector
+ * Key codes, metadata and outliers exist only for finished blocks (tokens
+ * below Bk * floor(T_cur / Bk)); the last T_cur % Bk keys stay fp16 in K_TAIL.
+ */
+typedef enum kvq_buffer {
+  KVQ_K_CODES = 0, KVQ_K_META, KVQ_K_TAIL, KVQ_K_OUTL,
+  KVQ_V_CODES, KVQ_V_META, KVQ_V_OUTL, KVQ_NBUF
+} kvq_buffer;
+
+typedef struct kvq_layout_t {
+  size_t bytes[KVQ_NBUF];        /* size of each cache buffer, whole batch */
+  size_t stream_bytes[KVQ_NBUF]; /* size of one (b, h_kv) stream of each buffer */
+  size_t cache_bytes;            /* sum of bytes[] */
+  size_t fp16_equiv_bytes;       /* fp16 K and V of the same capacity: 2*B*H_kv*T_max*D*2 */
+  size_t rope_bytes;             /* size of the RoPE table (kvq_rope_init) */
+  size_t workspace_bytes;        /* decode scratch for the given H_q */
+  int32_t n_out;                 /* outliers kept per vector */
+  int32_t code_row_bytes;        /* D*bits/8 */
+} kvq_layout_t;
+
+/* Device pointers to one layer's cache plus its fill level. */
+typedef struct kvq_cache {
+  void* k_codes;
+  void* k_meta;
+  void* k_tail;
+  void* k_outl;   /* may be NULL when n_out = 0 */
+  void* v_codes;
+  void* v_meta;
+  void* v_outl;   /* may be NULL when n_out = 0 */
+  int32_t T_cur;  /* tokens stored per sequence; kvq_append advances it */
+} kvq_cache;
+
+/* Sizes of every buffer for `cfg` and for decode with H_q query heads
+ * (H_q a positive multiple of H_kv). Host-only and pure: touches no device.
+ * Errors: KVQ_ERR_ARG (NULL), KVQ_ERR_UNSUPPORTED (cfg or H_q). */
+KVQ_API int kvq_layout(const kvq_config* cfg, int32_t H_q, kvq_layout_t* out);
+
+/* Fill the RoPE table used by kvq_decode_attn for base `rope_theta` (> 0):
+ * cos/sin of pos * theta^(-2i/D) (rotate-half pairs (i, i + D/2)), built in
+ * binary64 on the device and stored as binary32, for every position the cache
+ * can hold. Its contents are private to the library; build it once per
+ * (cfg, theta) and reuse it for every decode call and layer of that shape.
+ * Errors: KVQ_ERR_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_WORKSPACE (rope_bytes
+ * too small), KVQ_ERR_CUDA. */
+KVQ_API int kvq_rope_init(const kvq_config* cfg, double rope_theta, void* rope_tab, size_t rope_bytes,
+                  void* stream);
+
+/* Append n_new tokens per sequence at positions T_cur .. T_cur + n_new - 1
+ * (KVQuant "Pre-RoPE Key Quantization": keys arrive before RoPE).
+ *   k_new, v_new: fp16 [B][H_kv][n_new][D], contiguous.
+ * Values are quantized per token at once (outliers, then per-group s, z,
+ * codes). Keys are quantized per channel when their block of Bk tokens is
+ * complete (KVQuant "Per-Channel Key Quantization"; keys of the block read so
+ * far come back from K_TAIL); keys of an unfinished block are copied to
+ * K_TAIL. One kernel launch covers every (b, h_kv, block) touched; an append
+ * that completes the tail's block and also leaves a new unfinished block
+ * copies that block's keys to K_TAIL in a second, small launch. On success
+ * cache->T_cur += n_new (host field). n_new = 0 is a no-op.
+ * Errors: KVQ_ERR_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CAPACITY, KVQ_ERR_CUDA. */
+KVQ_API int kvq_append(const kvq_config* cfg, kvq_cache* cache, const void* k_new, const void* v_new,
+               int32_t n_new, void* stream);
+
+/* Decode attention of one query token per sequence over the T_cur cached
+ * tokens (GQA: query head h reads kv head h / G, G = H_q / H_kv in
+ * {1, 2, 4, 8}).
+ *   q:   fp16 [B][H_q][D], pre-RoPE, at position q_pos (0 <= q_pos < T_max);
+ *   out: fp16 [B][H_q][D].
+ * out_h = sum_t softmax_t(sm_scale * <RoPE(q_h, q_pos), RoPE(k_hat_t, t)>) v_hat_t
+ * over t in [0, T_cur); k_hat, v_hat are the dequantized cache with outliers
+ * restored, and tail keys are read as fp16. rope_tab = NULL applies no RoPE;
+ * otherwise it is a table filled by kvq_rope_init for this cfg. The work is
+ * split over T (flash-decode) into partial (max, sum, output) triples in
+ * `workspace`, merged by a second kernel. Requires T_cur >= 1.
+ * Errors: KVQ_ERR_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_WORKSPACE, KVQ_ERR_CUDA. */
+KVQ_API int kvq_decode_attn(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t H_q,
+                    int32_t q_pos, const void* rope_tab, float sm_scale, void* out,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static, human-readable name of a status code. */
+KVQ_API const char* kvq_status_string(int status);
+
+/* Library version, e.g. "kvq 0.1.0 sm_103a". */
+KVQ_API const char* kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -151,6 +151,19 @@ def queries_np(w: Workload, layer: int, step: int) -> np.ndarray:
     return out
 
 
+def streams_np(w: Workload, streams, T: int, layer: int = 0, chunk: int = 1 << 16):
+    """fp16 K, V [P, T, D] of the given (b, h_kv) streams, positions 0 .. T-1."""
+    sigma = channel_sigma(w, layer)
+    K = np.empty((len(streams), T, w.D), np.float16)
+    V = np.empty((len(streams), T, w.D), np.float16)
+    for p, (b, h) in enumerate(streams):
+        for t0 in range(0, T, chunk):
+            n = min(chunk, T - t0)
+            K[p, t0:t0 + n] = keys_np(w, layer, b, h, t0, n, sigma)
+            V[p, t0:t0 + n] = values_np(w, layer, b, h, t0, n)
+    return K, V
+
+
 def kv_torch(w: Workload, layer: int, t0: int, n: int, device, sigma=None, which="kv"):
     """fp16 K and V [B, H_kv, n, D] for positions t0 .. t0+n-1, built on ``device``."""
     import torch

@@ -1,0 +1,165 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+entry point the header declares, sizes its buffers as documented, and rejects
+bad arguments with the documented status before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_quantized_kv_append_gb300 as kvq
+from bit_quantized_kv_append_gb300 import build as kbuild
+import kvq_inputs as ki
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvq.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kvq.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = re.findall(r"KVQ_API\s+[\w\s\*]+?\b(kvq_\w+)\s*\(", open(HEADER).read())
+    assert sorted(names) == sorted(kvq.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.kvq_version().decode().startswith("kvq ")
+
+
+def test_status_strings(lib):
+    for code, name in kvq.kvq.STATUS.items():
+        assert lib.kvq_status_string(code).decode().startswith(name)
+
+
+def _golden(name):
+    vals = {}
+    for line in open(os.path.join(GOLDEN, name)):
+        if line.strip() and not line.startswith("#"):
+            k, v = (p.strip() for p in line.split("="))
+            vals[k] = int(v)
+    return vals
+
+
+def test_fp16_equivalent_size_matches_page_example(lib):
+    g = _golden("kv_memory_example.txt")
+    # one layer: H_kv * D = hidden (32 heads x 128)
+    lay = kvq.layout(kvq.make_config(g["batch"], 32, 128, g["seq"]), 32)
+    total = g["layers"] * lay.fp16_equiv_bytes
+    assert total == g["total_bytes"]
+    assert abs(total / 2 ** 30 - g["approx_gb"]) < 0.01
+
+
+@pytest.mark.parametrize("name", list(ki.WORKLOADS))
+def test_layout_sizes(lib, name):
+    w = ki.WORKLOADS[name]
+    T_max = w.T + w.key_block
+    cfg = kvq.make_config(w.B, w.H_kv, w.D, T_max, w.bits, w.key_block, w.value_group, w.outlier_frac)
+    lay = kvq.layout(cfg, w.H_q)
+    n_out = 0 if w.outlier_frac == 0 else max(1, int(w.outlier_frac * w.D))
+    S = w.B * w.H_kv
+    cb = w.D * w.bits // 8
+    assert lay.n_out == n_out and lay.code_row_bytes == cb
+    want = [T_max * cb, T_max // w.key_block * w.D * 4, w.key_block * w.D * 2, T_max * n_out * 4,
+            T_max * cb, T_max * (w.D // w.value_group) * 4, T_max * n_out * 4]
+    assert list(lay.stream_bytes) == want
+    assert list(lay.bytes) == [x * S for x in want]
+    assert lay.cache_bytes == sum(lay.bytes)
+    assert lay.fp16_equiv_bytes == 2 * S * T_max * w.D * 2
+    for b in lay.stream_bytes:
+        assert b % 16 == 0          # every stream starts 16-byte aligned
+    # packed INT4 + metadata is ~30% of fp16; INT2 well under 25%
+    ratio = lay.cache_bytes / lay.fp16_equiv_bytes
+    if w.T >= 32768:                 # the fp16 tail is a fixed cost on tiny caches
+        assert ratio < {4: 0.32, 3: 0.27, 2: 0.21}[w.bits]
+
+
+def _cfg(**kw):
+    base = dict(B=2, H_kv=2, D=128, T_max=256, bits=4, key_block=64, value_group=64, outlier_frac=0.01)
+    base.update(kw)
+    return kvq.make_config(**base)
+
+
+@pytest.mark.parametrize("kw", [dict(bits=1), dict(bits=5), dict(D=96), dict(key_block=32),
+                                dict(value_group=48), dict(T_max=100), dict(T_max=0), dict(B=0),
+                                dict(outlier_frac=0.2), dict(outlier_frac=-0.1), dict(B=70000),
+                                dict(T_max=1 << 24)])
+def test_layout_rejects_unsupported(lib, kw):
+    out = kvq.Layout()
+    assert lib.kvq_layout(ctypes.byref(_cfg(**kw)), 2, ctypes.byref(out)) == 2
+
+
+def test_layout_rejects_bad_hq_and_null(lib):
+    out = kvq.Layout()
+    assert lib.kvq_layout(ctypes.byref(_cfg()), 3, ctypes.byref(out)) == 2
+    assert lib.kvq_layout(None, 2, ctypes.byref(out)) == 1
+    assert lib.kvq_layout(ctypes.byref(_cfg()), 2, None) == 1
+
+
+FAKE = 0x10000  # never dereferenced: every call below must fail its host checks
+
+
+def _fake_cache(T_cur, n_out=1):
+    r = kvq.CacheRef()
+    for i, n in enumerate(kvq.BUFFERS):
+        setattr(r, n, FAKE * (i + 1) if (n_out or "outl" not in n) else None)
+    r.T_cur = T_cur
+    return r
+
+
+def test_append_host_errors(lib):
+    cfg = _cfg()
+    r = _fake_cache(200)
+    p = ctypes.c_void_p(FAKE)
+    assert lib.kvq_append(ctypes.byref(cfg), ctypes.byref(r), p, p, 57, None) == 3   # capacity
+    assert r.T_cur == 200
+    assert lib.kvq_append(ctypes.byref(cfg), ctypes.byref(r), p, p, -1, None) == 1
+    assert lib.kvq_append(ctypes.byref(cfg), None, p, p, 1, None) == 1
+    assert lib.kvq_append(ctypes.byref(cfg), ctypes.byref(r), None, p, 1, None) == 1
+    assert lib.kvq_append(ctypes.byref(cfg), ctypes.byref(r), ctypes.c_void_p(FAKE + 8), p, 1, None) == 1
+    assert lib.kvq_append(ctypes.byref(cfg), ctypes.byref(r), p, p, 0, None) == 0      # no-op
+    bad = _fake_cache(200)
+    bad.k_meta = FAKE + 4                                                               # misaligned
+    assert lib.kvq_append(ctypes.byref(cfg), ctypes.byref(bad), p, p, 1, None) == 1
+    no_outl = _fake_cache(0, n_out=0)
+    assert lib.kvq_append(ctypes.byref(cfg), ctypes.byref(no_outl), p, p, 1, None) == 1  # n_out=1 needs them
+    assert lib.kvq_append(ctypes.byref(_cfg(bits=7)), ctypes.byref(r), p, p, 1, None) == 2
+    over = _fake_cache(300)
+    assert lib.kvq_append(ctypes.byref(cfg), ctypes.byref(over), p, p, 1, None) == 1   # T_cur > T_max
+
+
+def test_decode_host_errors(lib):
+    cfg = _cfg()
+    lay = kvq.layout(cfg, 8)
+    r = _fake_cache(100)
+    p = ctypes.c_void_p(FAKE)
+    ws = lay.workspace_bytes
+
+    def call(cache=r, q=p, H_q=8, q_pos=99, rope=None, scale=0.1, out=p, w=p, wsb=ws, c=cfg):
+        return lib.kvq_decode_attn(ctypes.byref(c), None if cache is None else ctypes.byref(cache), q, H_q,
+                                   q_pos, rope, scale, out, w, wsb, None)
+
+    assert call(wsb=ws - 1) == 4
+    assert call(H_q=6) == 2                      # G = 3
+    assert call(H_q=3) == 2                      # not a multiple of H_kv
+    assert call(H_q=64) == 2                     # G = 32
+    assert call(q_pos=-1) == 1
+    assert call(q_pos=256) == 1
+    assert call(cache=_fake_cache(0)) == 1       # empty cache
+    assert call(cache=None) == 1
+    assert call(q=None) == 1
+    assert call(out=ctypes.c_void_p(FAKE + 2)) == 1
+    assert call(rope=ctypes.c_void_p(FAKE + 8)) == 1
+    assert call(scale=float("inf")) == 1
+
+
+def test_rope_init_host_errors(lib):
+    cfg = _cfg()
+    lay = kvq.layout(cfg, 2)
+    p = ctypes.c_void_p(FAKE)
+    assert lib.kvq_rope_init(ctypes.byref(cfg), 1e4, p, lay.rope_bytes - 8, None) == 4
+    assert lib.kvq_rope_init(ctypes.byref(cfg), 0.0, p, lay.rope_bytes, None) == 1
+    assert lib.kvq_rope_init(ctypes.byref(cfg), 1e4, None, lay.rope_bytes, None) == 1
