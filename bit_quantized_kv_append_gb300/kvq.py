@@ -134,6 +134,8 @@ class QuantizedKVCache:
         self.H_q = H_q or H_kv
         self.layout = layout(self.cfg, self.H_q)
         self.device = torch.device(device)
+        if self.device.type == "cuda" and self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
         self.buffers = {name: torch.empty(self.layout.bytes[i], dtype=torch.uint8, device=self.device)
                         for i, name in enumerate(BUFFERS)}
         self.workspace = torch.empty(self.layout.workspace_bytes, dtype=torch.uint8, device=self.device)
