@@ -1,6 +1,9 @@
-// Decode dispatch: choose the T split, launch the partial kernel, then merge the
+// Decode dispatch: choose the T split, launch the partial kernel (tensor-core
+// kernel for head_dim 128, CUDA-core kernel for head_dim 64), then merge the
 // splits (log-sum-exp in base 2) into the fp16 output.
-#include "kvq_decode.cuh"
+#include <cuda.h>
+
+#include "kvq_decode_tc.cuh"
 
 namespace kvq {
 namespace {
@@ -39,12 +42,6 @@ void pick_g(int G, LaunchFn* f, OccFn* o) {
   }
 }
 
-template <int BITS>
-void pick_d(int D, int G, LaunchFn* f, OccFn* o) {
-  if (D == 64) pick_g<BITS, 64>(G, f, o);
-  else pick_g<BITS, 128>(G, f, o);
-}
-
 // Occupancy (CTAs per SM) of each kernel variant, per device, computed once.
 int cached_occupancy(int dev, int bits, int D, int G, OccFn fn) {
   static int cache[16][3][2][4];
@@ -73,6 +70,94 @@ int choose_splits(int streams, int units, int slots, int max_split) {
   return best;
 }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 3-D map over a packed code buffer: [stream][token][row byte], box = one key
+// block of rows; INT4 rows (64 B) get the 64 B swizzle, INT2 rows (32 B) 32 B.
+bool encode_codes(CUtensorMap* m, const void* base, const Dims& d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)d.cb, (cuuint64_t)d.T_max, (cuuint64_t)d.B * d.H_kv};
+  const cuuint64_t strides[2] = {(cuuint64_t)d.cb, (cuuint64_t)d.T_max * d.cb};
+  const cuuint32_t box[3] = {(cuuint32_t)d.cb, (cuuint32_t)d.Bk, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const CUtensorMapSwizzle sw = d.bits == 4   ? CU_TENSOR_MAP_SWIZZLE_64B
+                                : d.bits == 2 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                              : CU_TENSOR_MAP_SWIZZLE_NONE;
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+tc::StageLayout stage_layout(const Dims& d) {
+  tc::StageLayout L;
+  L.code_bytes = (uint32_t)(d.Bk * d.cb);
+  L.km_bytes = (uint32_t)(d.D * 4);
+  L.vm_bytes = (uint32_t)(d.Bk * d.ng * 4);
+  L.outl_bytes = (uint32_t)(d.Bk * d.n_out * 4);
+  L.kc = 0;
+  L.vc = align_up(L.code_bytes, 1024);
+  L.km = align_up(L.vc + L.code_bytes, 16);
+  L.vm = L.km + L.km_bytes;
+  L.ko = align_up(L.vm + L.vm_bytes, 16);
+  L.vo = L.ko + L.outl_bytes;
+  L.stage_bytes = align_up(L.vo + L.outl_bytes, 1024);
+  L.tx_bytes = 2 * L.code_bytes + L.km_bytes + L.vm_bytes + 2 * L.outl_bytes;
+  return L;
+}
+
+using TcLaunchFn = cudaError_t (*)(const DecodeArgs&, const tc::StageLayout&, const CUtensorMap&,
+                                   const CUtensorMap&, size_t, cudaStream_t);
+using TcOccFn = int (*)(size_t);
+
+template <int BITS, int SL>
+void pick_tc_g(int G, TcLaunchFn* f, TcOccFn* o) {
+  switch (G) {
+    case 1: *f = launch_tc<BITS, 1, SL>; *o = tc_occupancy<BITS, 1, SL>; break;
+    case 2: *f = launch_tc<BITS, 2, SL>; *o = tc_occupancy<BITS, 2, SL>; break;
+    case 4: *f = launch_tc<BITS, 4, SL>; *o = tc_occupancy<BITS, 4, SL>; break;
+    default: *f = launch_tc<BITS, 8, SL>; *o = tc_occupancy<BITS, 8, SL>; break;
+  }
+}
+
+template <int BITS>
+void pick_tc(int Bk, int G, TcLaunchFn* f, TcOccFn* o) {
+  if (Bk == 64) pick_tc_g<BITS, 1>(G, f, o);
+  else pick_tc_g<BITS, 2>(G, f, o);
+}
+
+int cached_tc_occupancy(int dev, int bits, int Bk, int G, size_t smem, TcOccFn fn) {
+  struct Slot { size_t smem; int occ; };
+  static Slot cache[16][3][2][4];
+  const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+  Slot& s = cache[dev & 15][bits - 2][Bk == 128][gi];
+  if (s.occ == 0 || s.smem != smem) {
+    s.occ = fn(smem);
+    s.smem = smem;
+  }
+  return s.occ;
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, int H_q, int q_pos,
@@ -99,23 +184,41 @@ cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, in
   a.scale_log2 = sm_scale * 1.4426950408889634f;
   const int G = H_q / d.H_kv;
 
-  LaunchFn fn = nullptr;
-  OccFn occ_fn = nullptr;
-  switch (d.bits) {
-    case 2: pick_d<2>(d.D, G, &fn, &occ_fn); break;
-    case 3: pick_d<3>(d.D, G, &fn, &occ_fn); break;
-    default: pick_d<4>(d.D, G, &fn, &occ_fn); break;
-  }
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const int occ = cached_occupancy(dev, d.bits, d.D, G, occ_fn);
   const int units = a.n_full + (a.tail_len > 0 ? 1 : 0);
-  a.n_split = choose_splits(d.B * d.H_kv, units, sms * occ, a.S);
 
-  e = fn(a, st);
+  if (d.D == 128) {
+    CUtensorMap tk, tv;
+    if (!encode_codes(&tk, c.k_codes, d) || !encode_codes(&tv, c.v_codes, d))
+      return cudaErrorInvalidValue;
+    const tc::StageLayout L = stage_layout(d);
+    const size_t smem = (size_t)tc::kStages * L.stage_bytes + 1024;
+    TcLaunchFn fn = nullptr;
+    TcOccFn occ_fn = nullptr;
+    switch (d.bits) {
+      case 2: pick_tc<2>(d.Bk, G, &fn, &occ_fn); break;
+      case 3: pick_tc<3>(d.Bk, G, &fn, &occ_fn); break;
+      default: pick_tc<4>(d.Bk, G, &fn, &occ_fn); break;
+    }
+    const int occ = cached_tc_occupancy(dev, d.bits, d.Bk, G, smem, occ_fn);
+    a.n_split = choose_splits(d.B * d.H_kv, units, sms * occ, a.S);
+    e = fn(a, L, tk, tv, smem, st);
+  } else {
+    LaunchFn fn = nullptr;
+    OccFn occ_fn = nullptr;
+    switch (d.bits) {
+      case 2: pick_g<2, 64>(G, &fn, &occ_fn); break;
+      case 3: pick_g<3, 64>(G, &fn, &occ_fn); break;
+      default: pick_g<4, 64>(G, &fn, &occ_fn); break;
+    }
+    const int occ = cached_occupancy(dev, d.bits, d.D, G, occ_fn);
+    a.n_split = choose_splits(d.B * d.H_kv, units, sms * occ, a.S);
+    e = fn(a, st);
+  }
   if (e != cudaSuccess) return e;
   if (d.D == 64)
     decode_combine_kernel<64><<<d.B * H_q, 64, 0, st>>>(ws, out, a.n_split, a.S);

@@ -27,17 +27,9 @@ int partial_occupancy() {
   template cudaError_t launch_partial<BITS, 64, 2>(const DecodeArgs&, cudaStream_t);  \
   template cudaError_t launch_partial<BITS, 64, 4>(const DecodeArgs&, cudaStream_t);  \
   template cudaError_t launch_partial<BITS, 64, 8>(const DecodeArgs&, cudaStream_t);  \
-  template cudaError_t launch_partial<BITS, 128, 1>(const DecodeArgs&, cudaStream_t); \
-  template cudaError_t launch_partial<BITS, 128, 2>(const DecodeArgs&, cudaStream_t); \
-  template cudaError_t launch_partial<BITS, 128, 4>(const DecodeArgs&, cudaStream_t); \
-  template cudaError_t launch_partial<BITS, 128, 8>(const DecodeArgs&, cudaStream_t); \
   template int partial_occupancy<BITS, 64, 1>();                                    \
   template int partial_occupancy<BITS, 64, 2>();                                    \
   template int partial_occupancy<BITS, 64, 4>();                                    \
-  template int partial_occupancy<BITS, 64, 8>();                                    \
-  template int partial_occupancy<BITS, 128, 1>();                                   \
-  template int partial_occupancy<BITS, 128, 2>();                                   \
-  template int partial_occupancy<BITS, 128, 4>();                                   \
-  template int partial_occupancy<BITS, 128, 8>();
+  template int partial_occupancy<BITS, 64, 8>();
 
 }  // namespace kvq

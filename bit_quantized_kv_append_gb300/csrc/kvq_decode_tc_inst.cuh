@@ -1,0 +1,51 @@
+// Launch and occupancy helpers of the tensor-core decode kernel; included by
+// one translation unit per code width so the instantiations build in parallel.
+#pragma once
+
+#include "kvq_decode_tc.cuh"
+
+namespace kvq {
+
+template <int BITS, int G, int SL>
+cudaError_t launch_tc(const DecodeArgs& a, const tc::StageLayout& L, const CUtensorMap& tk,
+                      const CUtensorMap& tv, size_t smem, cudaStream_t st) {
+  auto kern = tc::decode_tc_kernel<BITS, G, SL>;
+  static size_t smem_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (smem_set[dev & 63] < smem) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    smem_set[dev & 63] = smem;
+  }
+  const dim3 grid(a.n_split, a.d.B * a.d.H_kv);
+  kern<<<grid, tc::kThreads, smem, st>>>(a, L, tk, tv);
+  return cudaGetLastError();
+}
+
+template <int BITS, int G, int SL>
+int tc_occupancy(size_t smem) {
+  auto kern = tc::decode_tc_kernel<BITS, G, SL>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, tc::kThreads, smem) != cudaSuccess) n = 1;
+  return n < 1 ? 1 : n;
+}
+
+#define KVQ_TC_ONE(BITS, G, SL)                                                                  \
+  template cudaError_t launch_tc<BITS, G, SL>(const DecodeArgs&, const tc::StageLayout&,         \
+                                              const CUtensorMap&, const CUtensorMap&, size_t,    \
+                                              cudaStream_t);                                     \
+  template int tc_occupancy<BITS, G, SL>(size_t);
+#define KVQ_INSTANTIATE_TC(BITS) \
+  KVQ_TC_ONE(BITS, 1, 1)         \
+  KVQ_TC_ONE(BITS, 2, 1)         \
+  KVQ_TC_ONE(BITS, 4, 1)         \
+  KVQ_TC_ONE(BITS, 8, 1)         \
+  KVQ_TC_ONE(BITS, 1, 2)         \
+  KVQ_TC_ONE(BITS, 2, 2)         \
+  KVQ_TC_ONE(BITS, 4, 2)         \
+  KVQ_TC_ONE(BITS, 8, 2)
+
+}  // namespace kvq
