@@ -4,6 +4,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "kvq_common.cuh"
 
 namespace kvq {
@@ -58,6 +60,30 @@ bool cache_ptrs_ok(const Dims& d, const kvq_cache& c) {
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
+
+// Scratch of kvq_decode_attn_noalloc: the split partials live in this
+// file-scope device array instead of a caller-provided workspace. Every device
+// that loads the library holds it until the process exits.
+constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+// Device address of g_noalloc_scratch on the current device. In host code
+// the array's name is only a stand-in symbol, so the address is looked up
+// once per device (with that device current) and remembered.
+int noalloc_scratch(float** out) {
+  static std::mutex mu;
+  static float* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return KVQ_ERR_CUDA;
+    addr[dev] = static_cast<float*>(p);
+  }
+  *out = addr[dev];
+  return KVQ_OK;
+}
 
 }  // namespace
 }  // namespace kvq
@@ -143,6 +169,32 @@ int kvq_decode_attn(const kvq_config* cfg, const kvq_cache* cache, const void* q
                                    static_cast<const float2*>(rope_tab), sm_scale,
                                    static_cast<__half*>(out), static_cast<float*>(workspace),
                                    static_cast<cudaStream_t>(stream)));
+}
+
+int kvq_decode_attn_noalloc(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t H_q,
+                            int32_t q_pos, const void* rope_tab, float sm_scale, void* out,
+                            void* stream) {
+  Dims d;
+  int rc = make_dims(cfg, &d);
+  if (rc) return rc;
+  if (H_q < 1 || H_q % d.H_kv) return KVQ_ERR_UNSUPPORTED;
+  const int G = H_q / d.H_kv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return KVQ_ERR_UNSUPPORTED;
+  if (!cache || !cache_ptrs_ok(d, *cache) || cache->T_cur < 1) return KVQ_ERR_ARG;
+  if (!q || !out || !aligned16(q) || !aligned16(out)) return KVQ_ERR_ARG;
+  if (q_pos < 0 || q_pos >= d.T_max || !isfinite(sm_scale)) return KVQ_ERR_ARG;
+  if (rope_tab && !aligned16(rope_tab)) return KVQ_ERR_ARG;
+  // one T split needs (D + 2) floats per (sequence, query head)
+  const size_t split_bytes = (size_t)d.B * H_q * (d.D + 2) * sizeof(float);
+  const size_t fit = kNoAllocScratchBytes / split_bytes;
+  if (fit < 1) return KVQ_ERR_WORKSPACE;
+  float* scratch = nullptr;
+  rc = noalloc_scratch(&scratch);
+  if (rc) return rc;
+  return cuda_status(launch_decode(d, *cache, static_cast<const __half*>(q), H_q, q_pos,
+                                   static_cast<const float2*>(rope_tab), sm_scale,
+                                   static_cast<__half*>(out), scratch,
+                                   static_cast<cudaStream_t>(stream), fit > 256 ? 256 : (int)fit));
 }
 
 const char* kvq_status_string(int status) {

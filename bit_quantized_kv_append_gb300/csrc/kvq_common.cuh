@@ -57,8 +57,9 @@ __device__ __forceinline__ float2 rot_compose(float2 a, float2 b) {
 cudaError_t launch_rope_init(const Dims& d, double theta, float2* tab, cudaStream_t st);
 cudaError_t launch_append(const Dims& d, const kvq_cache& c, const __half* k_new,
                           const __half* v_new, int n_new, cudaStream_t st);
+// split_cap > 0 bounds the T splits (and the workspace stride) below max_splits().
 cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, int H_q, int q_pos,
                           const float2* rope, float sm_scale, __half* out, float* ws,
-                          cudaStream_t st);
+                          cudaStream_t st, int split_cap = 0);
 
 }  // namespace kvq

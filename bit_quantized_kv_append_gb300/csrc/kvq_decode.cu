@@ -162,7 +162,7 @@ int cached_tc_occupancy(int dev, int bits, int Bk, int G, size_t smem, TcOccFn f
 
 cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, int H_q, int q_pos,
                           const float2* rope, float sm_scale, __half* out, float* ws,
-                          cudaStream_t st) {
+                          cudaStream_t st, int split_cap) {
   DecodeArgs a;
   a.d = d;
   a.k_codes = static_cast<const uint8_t*>(c.k_codes);
@@ -180,7 +180,7 @@ cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, in
   a.tail_len = c.T_cur % d.Bk;
   a.H_q = H_q;
   a.q_pos = q_pos;
-  a.S = max_splits(d);
+  a.S = (split_cap > 0 && split_cap < max_splits(d)) ? split_cap : max_splits(d);
   a.scale_log2 = sm_scale * 1.4426950408889634f;
   const int G = H_q / d.H_kv;
 

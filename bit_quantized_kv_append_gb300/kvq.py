@@ -21,7 +21,7 @@ BUFFERS = ("k_codes", "k_meta", "k_tail", "k_outl", "v_codes", "v_meta", "v_outl
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "KVQ_ERR_CAPACITY",
           4: "KVQ_ERR_WORKSPACE", 5: "KVQ_ERR_CUDA"}
 EXPORTS = ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_decode_attn",
-           "kvq_status_string", "kvq_version")
+           "kvq_decode_attn_noalloc", "kvq_status_string", "kvq_version")
 
 
 class KvqError(RuntimeError):
@@ -66,10 +66,13 @@ def lib():
         L.kvq_append.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp, vp, i32, vp]
         L.kvq_decode_attn.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp, i32, i32,
                                       vp, ctypes.c_float, vp, vp, ctypes.c_size_t, vp]
+        L.kvq_decode_attn_noalloc.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp,
+                                              i32, i32, vp, ctypes.c_float, vp, vp]
         L.kvq_status_string.argtypes = [ctypes.c_int]
         L.kvq_status_string.restype = ctypes.c_char_p
         L.kvq_version.restype = ctypes.c_char_p
-        for fn in ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_decode_attn"):
+        for fn in ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_decode_attn",
+                   "kvq_decode_attn_noalloc"):
             getattr(L, fn).restype = ctypes.c_int
         _LIB = L
     return _LIB
@@ -123,6 +126,15 @@ def decode_attn(cfg: Config, ref: CacheRef, q: torch.Tensor, H_q: int, q_pos: in
     _check(lib().kvq_decode_attn(ctypes.byref(cfg), ctypes.byref(ref), _ptr(q), int(H_q), int(q_pos),
                                  _ptr(rope), float(sm_scale), _ptr(out), _ptr(workspace),
                                  workspace.numel(), _stream(stream)), "kvq_decode_attn")
+
+
+def decode_attn_noalloc(cfg: Config, ref: CacheRef, q: torch.Tensor, H_q: int, q_pos: int,
+                        rope: Optional[torch.Tensor], sm_scale: float, out: torch.Tensor, stream=None):
+    """kvq_decode_attn_noalloc: decode attention with the library's own fixed
+    8 MiB device scratch instead of a workspace (see include/kvq.h)."""
+    _check(lib().kvq_decode_attn_noalloc(ctypes.byref(cfg), ctypes.byref(ref), _ptr(q), int(H_q),
+                                         int(q_pos), _ptr(rope), float(sm_scale), _ptr(out),
+                                         _stream(stream)), "kvq_decode_attn_noalloc")
 
 
 class QuantizedKVCache:

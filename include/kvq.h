@@ -167,6 +167,30 @@ KVQ_API int kvq_decode_attn(const kvq_config* cfg, const kvq_cache* cache, const
                     int32_t q_pos, const void* rope_tab, float sm_scale, void* out,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+/* kvq_decode_attn without a workspace argument, for callers that cannot
+ * allocate device memory on the decode path: for example a serving engine
+ * that reserves all device memory at start-up and forbids later cudaMalloc
+ * calls, or a plain-C host that owns no device allocator from which to hand
+ * over scratch. The pages have no counterpart; it is a convenience of this
+ * library. Same arguments, results and errors as kvq_decode_attn.
+ *   - Scratch: the split partials go to one file-scope device array of
+ *     8 MiB that every GPU loading the library keeps until the process
+ *     exits. No allocation or free happens in this call.
+ *   - Limit: one T split needs B * H_q * (D + 2) * 4 bytes. The call uses at
+ *     most 8 MiB / that many splits (at most 256); a shape whose single split
+ *     exceeds 8 MiB is rejected with KVQ_ERR_WORKSPACE. Fewer splits can make
+ *     it slower than kvq_decode_attn on very wide batches.
+ *   - Set-up: the first call on each device looks up the array's device
+ *     address with that device current; make that first call before any
+ *     stream capture on the device.
+ *   - Sharing: every call uses the same array. Each call writes every entry
+ *     it later reads, so nothing has to be cleared between calls, but calls
+ *     whose kernels overlap on the GPU (different streams, or different host
+ *     threads) race on the array and give wrong results. */
+KVQ_API int kvq_decode_attn_noalloc(const kvq_config* cfg, const kvq_cache* cache, const void* q,
+                                    int32_t H_q, int32_t q_pos, const void* rope_tab,
+                                    float sm_scale, void* out, void* stream);
+
 /* Static, human-readable name of a status code. */
 KVQ_API const char* kvq_status_string(int status);
 
