@@ -37,7 +37,17 @@ __host__ __device__ inline int rope_n_hi(int n_blk) { return (n_blk - 1) / kRope
 __host__ __device__ inline size_t rope_fine_off(const Dims&) { return 0; }
 __host__ __device__ inline size_t rope_lo_off(const Dims& d) { return (size_t)(d.D / 2) * d.Bk; }
 __host__ __device__ inline size_t rope_hi_off(const Dims& d) { return rope_lo_off(d) + (size_t)kRopeLo * (d.D / 2); }
-__host__ __device__ inline size_t rope_entries(const Dims& d) { return rope_hi_off(d) + (size_t)d.rope_n_hi * (d.D / 2); }
+// For D = 128 a fourth table follows (16 B aligned): the in-block rotations of
+// the tensor-core kernel in its fragment order, kRopeFragQuads uint4 of fp16
+// {cos, cos, sin, sin} (see kvq_tc_geom.cuh).
+constexpr int kRopeFragQuads = 1024;
+__host__ __device__ inline size_t rope_frag_off(const Dims& d) {
+  return (rope_hi_off(d) + (size_t)d.rope_n_hi * (d.D / 2) + 1) & ~(size_t)1;
+}
+__host__ __device__ inline size_t rope_entries(const Dims& d) {
+  return d.D == 128 ? rope_frag_off(d) + 2 * (size_t)kRopeFragQuads
+                    : rope_hi_off(d) + (size_t)d.rope_n_hi * (d.D / 2);
+}
 
 // Decode split-T scratch: per (b, h_q, split) the partial output o[D], then m, l.
 constexpr int kMaxSplits = 256;

@@ -196,7 +196,7 @@ cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, in
     if (!encode_codes(&tk, c.k_codes, d) || !encode_codes(&tv, c.v_codes, d))
       return cudaErrorInvalidValue;
     const tc::StageLayout L = stage_layout(d);
-    const size_t smem = (size_t)tc::kStages * L.stage_bytes + 1024;
+    const size_t smem = (size_t)tc::ring_stages(d.Bk) * L.stage_bytes + 1024;
     TcLaunchFn fn = nullptr;
     TcOccFn occ_fn = nullptr;
     switch (d.bits) {

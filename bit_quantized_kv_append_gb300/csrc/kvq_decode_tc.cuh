@@ -4,43 +4,49 @@
 // Key Quantization": dequantize, rotate, q . k; Quanto step 3: dequantize at
 // read time), arranged so the issue slots go to what cannot be avoided:
 //
-//  * data: a 3-stage shared-memory ring per CTA fed by TMA. Code tiles arrive
-//    through 3-D tensor maps with a 64 B (INT4) or 32 B (INT2) swizzle, which
-//    makes the row-crossing accesses below bank-conflict free; metadata and
-//    outliers arrive as 1-D bulk copies. One thread issues, every thread
-//    waits on the stage's mbarrier (bounded; on expiry the CTA drains its
-//    copies, writes NaN partials and exits).
-//  * work split: warp w owns 16 tokens of every key block (two slices of 16
-//    for 128-token blocks) and keeps its own running softmax state; warps
-//    meet once per block (stage release) and merge once per split.
-//  * q . k: each lane turns its codes into exact half2 integers (magic-number
-//    trick), dequantizes (s, z halved so the fp16 rotation cannot overflow),
-//    applies the in-block rotation R(j') from registers, and feeds
-//    mma.sync.m16n8k16 (f16 in, f32 accumulate) with the block-rotated
-//    queries as A (rows = the G query heads of this kv head). The score
-//    fragments are already laid out as the A operand of P . V.
-//  * softmax: base 2, running (m, l) per warp and head; key outliers add
-//    (x_out - x_dense) * <q, R(j') e_c> to their token's score.
-//  * P . V, transposed (rows = channels, columns = heads): A = value codes
-//    as exact fp16 subnormals (q * 2^-24, rescaled after the loop), B = p*s
-//    (value scale folded into the probabilities, split into fp16 hi + lo),
-//    the zero points as sum_t p*z per group, value outliers as scattered
-//    corrections. Accumulators move to fp32 shared sums every kFlush blocks.
+//  * data: a shared-memory ring per CTA (3 stages of 64-token blocks, 2 of
+//    128-token blocks) fed by TMA. Code tiles arrive through 3-D tensor maps
+//    with a 64 B (INT4) or 32 B (INT2) swizzle; metadata and outliers as 1-D
+//    bulk copies. One thread issues, every thread waits on the stage's
+//    mbarrier (bounded; on expiry the CTA drains its copies, writes NaN
+//    partials and exits).
+//  * work split: warp w owns 16 tokens of every 64-token slice and keeps its
+//    own running softmax state; warps meet once per block (stage release)
+//    and merge once per split.
+//  * q . k (mma.m16n8k16, f16 in, f32 out): A = the queries rotated back to
+//    the slice start (rows = the G query heads of this kv head); B = the
+//    lane's dequantized, rotated keys. Lane quarter r owns 16 contiguous
+//    channels and their RoPE partners (kvq_tc_geom.cuh), so a lane reads its
+//    codes with two 64-bit loads, turns them into exact half2 integers with
+//    one LOP3 each (magic-number trick), dequantizes with one HFMA2 (s, z
+//    halved so the rotation cannot overflow fp16) and rotates with the
+//    in-block table R(j), j < 64, read through L1 in fragment order.
+//  * softmax: base 2, running (m, l) per warp and head. Key outliers add
+//    (x_out - x_dense) * <q, R(j) e_c> to their token's score.
+//  * P . V, transposed (rows = channels, columns = heads): A = value codes as
+//    exact fp16 subnormals (q * 2^-24, power-of-two rescale at the flush),
+//    B = p*s split into fp16 hi + lo; zero points as sum_t p*z per group.
+//  * accumulation: the tensor-core accumulators move every kFlush blocks into
+//    fp32 shared sums (long accumulations on the tensor core drift low). The
+//    shared sums and the value-outlier corrections p*(x_out - x_dense) live
+//    in a lazily renormalised frame (factor 2^(m - m_frame)), so a new
+//    running max rescales only registers.
 #pragma once
 
 #include <cuda.h>
 
 #include "kvq_decode.cuh"
+#include "kvq_tc_geom.cuh"
 
 namespace kvq {
 namespace tc {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = 32 * kWarps;
-constexpr int kStages = 3;
-constexpr int kD = 128;
-constexpr uint32_t kWaitLimit = 1u << 20;   // mbarrier polls before giving up (~1 s)
-constexpr int kFlush = 8;                     // blocks between P.V accumulator flushes
+constexpr uint32_t kWaitLimit = 1u << 20;  // mbarrier polls before giving up (~1 s)
+constexpr int kFlush = 8;                   // blocks between P.V accumulator flushes
+constexpr float kFrameGap = 64.0f;          // renormalise the shared sums past 2^64
+
+// Ring stages: 3 of 64-token blocks, 2 of 128-token blocks.
+__host__ __device__ constexpr int ring_stages(int Bk) { return Bk == 64 ? 3 : 2; }
 
 // Byte offsets of one ring stage (host-computed; stages 1024 B aligned).
 struct StageLayout {
@@ -91,18 +97,25 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
-// D += A * B with A rows 8..15 zero (only the G <= 8 query heads are real).
-__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint4& a, uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
 }
 // (a & mask) | orv in one LOP3.
 __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t mask, uint32_t orv) {
   uint32_t d;
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(orv));
   return d;
+}
+__device__ __forceinline__ float ex2(float x) {   // 2^x, hardware approximation (2 ulp)
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ void red_add(float* p, float v) {
+  asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(smem_addr(p)), "f"(v) : "memory");
 }
 __device__ __forceinline__ __half2 as_h2(uint32_t u) {
   __half2 h;
@@ -115,37 +128,37 @@ __device__ __forceinline__ uint32_t as_u32(__half2 h) {
   return u;
 }
 __device__ __forceinline__ uint32_t ld_s32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+__device__ __forceinline__ uint2 ld_s64(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
+__device__ __forceinline__ float ld_h(const uint8_t* p) {
+  return __half2float(*reinterpret_cast<const __half*>(p));
+}
 
 constexpr uint32_t kMagic = 0x64006400u;      // half2(1024, 1024)
-constexpr uint32_t kSixteenth = 0x2C002C00u;  // half2(1/16, 1/16)
-constexpr uint32_t kMinus64 = 0xD400D400u;    // half2(-64, -64)
-constexpr uint32_t kHalf = 0x38003800u;       // half2(0.5, 0.5)
+// (1024 + 2^k c) * 2^-k - 1024 * 2^-k = c for k = 2, 4, 6
+constexpr uint32_t kQuarter = 0x34003400u, kMinus256 = 0xDC00DC00u;
+constexpr uint32_t kSixteenth = 0x2C002C00u, kMinus64 = 0xD400D400u;
+constexpr uint32_t kSixtyFourth = 0x24002400u, kMinus16 = 0xCC00CC00u;
 
-// ------------------------------------------------------------------ code layout
-// Channel (offset within a 16-channel k-step of the first half) of lane
-// quarter r, fragment slot s (0: b0.lo, 1: b0.hi, 2: b1.lo, 3: b1.hi). Chosen
-// so each lane extracts its codes from one 32-bit word with a single mask.
-template <int BITS>
-__host__ __device__ constexpr int chan_off(int r, int s) {
-  return BITS == 4   ? 8 * (r >> 1) + 2 * (r & 1) + (s == 0 ? 0 : s == 1 ? 4 : s == 2 ? 1 : 5)
-         : BITS == 2 ? 2 * r + (s == 0 ? 0 : s == 1 ? 8 : s == 2 ? 1 : 9)
-                     : 4 * r + s;
+__device__ __forceinline__ uint32_t fix1(uint32_t h) { return as_u32(__hsub2(as_h2(h), as_h2(kMagic))); }
+__device__ __forceinline__ uint32_t fixk(uint32_t h, uint32_t mul, uint32_t add) {
+  return as_u32(__hfma2(as_h2(h), as_h2(mul), as_h2(add)));
 }
-template <int BITS>
-__device__ __forceinline__ void chan_slot(int o, int& r, int& s) {
-  if (BITS == 4) {
-    r = 2 * (o >> 3) + ((o >> 1) & 1);
-    const int add = o - 8 * (r >> 1) - 2 * (r & 1);
-    s = ((add & 1) << 1) | (add >> 2);
-  } else if (BITS == 2) {
-    r = (o & 7) >> 1;
-    const int add = o - 2 * r;
-    s = ((add & 1) << 1) | (add >> 3);
-  } else {
-    r = o >> 2;
-    s = o & 3;
-  }
-}
+
+// Identity rotation in fragment order (RoPE off).
+#define KVQ_ROT_ID1 {0x3C003C00u, 0x3C003C00u, 0u, 0u}
+#define KVQ_ROT_ID4 KVQ_ROT_ID1, KVQ_ROT_ID1, KVQ_ROT_ID1, KVQ_ROT_ID1
+#define KVQ_ROT_ID16 KVQ_ROT_ID4, KVQ_ROT_ID4, KVQ_ROT_ID4, KVQ_ROT_ID4
+#define KVQ_ROT_ID64 KVQ_ROT_ID16, KVQ_ROT_ID16, KVQ_ROT_ID16, KVQ_ROT_ID16
+#define KVQ_ROT_ID256 KVQ_ROT_ID64, KVQ_ROT_ID64, KVQ_ROT_ID64, KVQ_ROT_ID64
+static __device__ const uint4 g_rot_identity[kRotFragQuads] = {KVQ_ROT_ID256, KVQ_ROT_ID256, KVQ_ROT_ID256,
+                                                               KVQ_ROT_ID256};
+#undef KVQ_ROT_ID1
+#undef KVQ_ROT_ID4
+#undef KVQ_ROT_ID16
+#undef KVQ_ROT_ID64
+#undef KVQ_ROT_ID256
+
+// ------------------------------------------------------------------ code tiles
 // Byte offset of (row, byte) in a code tile as the TMA swizzle lays it out.
 template <int BITS>
 __device__ __forceinline__ uint32_t code_off(int row, int byte) {
@@ -162,13 +175,14 @@ __device__ __forceinline__ uint32_t tile_code(const uint8_t* tile, int row, int 
   return v & ((1u << BITS) - 1u);
 }
 
-// Per-lane byte offsets into the code tiles. For every row a lane reads, the
-// TMA swizzle term depends only on the lane's own bits, so each load below is
-// a lane offset plus a compile-time immediate.
+// Per-lane byte offsets into the code tiles (row 16 w + tperm(g) for keys,
+// 16 w + tperm(2 r) for values; slices and n-tiles add compile-time rows).
+// The swizzle term of every row a lane reads depends only on the lane.
 struct LaneOff {
-  uint32_t k[4];        // key tile (INT4: per 16 B chunk; INT2: per half; INT3: [0])
-  uint32_t v[4];        // value tile (INT4: per 32-channel block; INT2: per pair; INT3: [0])
-  uint32_t ksh, vsh;    // bit shifts of the lane's key / value codes
+  uint32_t kf, kp;      // key: first-half and partner codes
+  uint32_t ksh;         // INT3: bit shift of the lane's 48-bit key window
+  uint32_t v[4];        // value tile (INT4: per 32-channel block; INT2: per 16 B half; INT3: [0])
+  uint32_t vsh;         // INT3: bit shift of the lane's value codes
   uint32_t sel0, sel1;  // byte_perm selectors of the lane's value bytes
 };
 
@@ -176,76 +190,94 @@ template <int BITS>
 __device__ __forceinline__ LaneOff lane_offsets(int w, int g, int r) {
   LaneOff o;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) o.k[c] = o.v[c] = 0u;
+  for (int c = 0; c < 4; ++c) o.v[c] = 0u;
   o.ksh = o.vsh = o.sel0 = o.sel1 = 0u;
+  const int tk = tperm(g), tv = tperm(2 * r);
+  const int krow = 16 * w + tk, vrow = 16 * w + tv;
   if constexpr (BITS == 4) {
-    const int sw = (g >> 1) & 3, bb = 2 * (g & 1);
+    const int ksw = (tk >> 1) & 3, vsw = (tv >> 1) & 3, bb = 2 * (g & 1);
+    o.kf = 64 * krow + (((r >> 1) ^ ksw) << 4) + 8 * (r & 1);
+    o.kp = 64 * krow + (((2 + (r >> 1)) ^ ksw) << 4) + 8 * (r & 1);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      o.k[c] = 1024 * w + 64 * g + ((c ^ sw) << 4) + 4 * (r >> 1);
-      o.v[c] = 64 * (16 * w + 2 * r) + ((c ^ r) << 4) + 4 * (g >> 1);
-    }
-    o.ksh = 8 * (r & 1);
+    for (int c = 0; c < 4; ++c) o.v[c] = 64 * vrow + ((c ^ vsw) << 4) + 4 * (g >> 1);
     o.sel0 = (uint32_t)(bb | ((bb + 4) << 8));
     o.sel1 = (uint32_t)((bb + 1) | ((bb + 5) << 8));
   } else if constexpr (BITS == 2) {
-    const int sw = (g >> 2) & 1, vsw = (r >> 1) & 1, bb = g & 3;
+    const int ksw = (tk >> 2) & 1, vsw = (tv >> 2) & 1, bb = g & 3;
+    o.kf = 32 * krow + (ksw << 4) + 4 * r;
+    o.kp = 32 * krow + ((1 ^ ksw) << 4) + 4 * r;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      o.k[h] = 512 * w + 32 * g + ((h ^ sw) << 4);
-      o.v[h] = 32 * (16 * w + 2 * r) + ((h ^ vsw) << 4) + 4 * (g >> 2);
-    }
-    o.ksh = 4 * r;
+    for (int h = 0; h < 2; ++h) o.v[h] = 32 * vrow + ((h ^ vsw) << 4) + 4 * (g >> 2);
     o.sel0 = (uint32_t)(bb | ((bb + 4) << 8));
   } else {
-    o.k[0] = 48 * (16 * w + g);
-    o.v[0] = 48 * (16 * w + 2 * r) + 4 * ((12 * g) >> 5);
-    o.ksh = 12 * r;
+    o.kf = 48 * krow + 4 * ((6 * r) >> 2);
+    o.kp = o.kf + 24;
+    o.ksh = 16 * (r & 1);
+    o.v[0] = 48 * vrow + 4 * ((12 * g) >> 5);
     o.vsh = (12 * g) & 31;
   }
   return o;
 }
 
-// Exact integer codes of the lane's channels of first-half k-step kq (q[0],
-// q[1]) and of their RoPE partners (q[2], q[3]), key row 64 sl + 16 w + 8 nt + g.
+// The lane's raw key code words of one token row (first half, partner).
+struct KeyWords {
+  uint32_t f[2], p[2];
+};
 template <int BITS>
-__device__ __forceinline__ void key_codes(const uint8_t* kc, const LaneOff& o, int sl, int nt, int kq,
-                                          uint32_t (&q)[4]) {
+__device__ __forceinline__ KeyWords key_words(const uint8_t* kc, const LaneOff& o, int row0) {
+  constexpr int CB = 16 * BITS;   // code row bytes for D = 128
+  KeyWords k;
+  const uint8_t* base = kc + CB * row0;
   if constexpr (BITS == 4) {
-    const int ro = 4096 * sl + 512 * nt + 8 * (kq & 1);
-    const uint32_t W[2] = {ld_s32(kc + o.k[kq >> 1] + ro) >> o.ksh, ld_s32(kc + o.k[(kq >> 1) + 2] + ro) >> o.ksh};
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      q[2 * h] = as_u32(__hsub2(as_h2(and_or(W[h], 0x000F000Fu, kMagic)), as_h2(kMagic)));
-      q[2 * h + 1] = as_u32(__hfma2(as_h2(and_or(W[h], 0x00F000F0u, kMagic)), as_h2(kSixteenth), as_h2(kMinus64)));
-    }
+    const uint2 f = ld_s64(base + o.kf), p = ld_s64(base + o.kp);
+    k.f[0] = f.x;
+    k.f[1] = f.y;
+    k.p[0] = p.x;
+    k.p[1] = p.y;
   } else if constexpr (BITS == 2) {
-    const int ro = 2048 * sl + 256 * nt + 4 * kq;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t W = ld_s32(kc + o.k[h] + ro);
-      q[2 * h] = as_u32(__hsub2(as_h2(and_or(W >> o.ksh, 0x00030003u, kMagic)), as_h2(kMagic)));
-      q[2 * h + 1] = as_u32(__hsub2(as_h2(and_or(W >> (o.ksh + 2), 0x00030003u, kMagic)), as_h2(kMagic)));
+    k.f[0] = ld_s32(base + o.kf);
+    k.p[0] = ld_s32(base + o.kp);
+    k.f[1] = k.p[1] = 0u;
+  } else {
+    k.f[0] = ld_s32(base + o.kf);
+    k.f[1] = ld_s32(base + o.kf + 4);
+    k.p[0] = ld_s32(base + o.kp);
+    k.p[1] = ld_s32(base + o.kp + 4);
+  }
+  return k;
+}
+
+// Exact integer codes (half2) of k-step kq's slots (0, 1) -> x0 and (2, 3)
+// -> x1 from one half's code words, in kchan order.
+template <int BITS>
+__device__ __forceinline__ void key_codes(const uint32_t (&wd)[2], uint32_t ksh, int kq, uint32_t& x0,
+                                          uint32_t& x1) {
+  if constexpr (BITS == 4) {
+    uint32_t W = wd[kq >> 1];
+    if (kq & 1) W >>= 8;
+    x0 = fix1(and_or(W, 0x000F000Fu, kMagic));
+    x1 = fixk(and_or(W, 0x00F000F0u, kMagic), kSixteenth, kMinus64);
+  } else if constexpr (BITS == 2) {
+    uint32_t W = wd[0];
+    if (kq >= 2) W >>= 8;
+    if ((kq & 1) == 0) {
+      x0 = fix1(and_or(W, 0x00030003u, kMagic));
+      x1 = fixk(and_or(W, 0x000C000Cu, kMagic), kQuarter, kMinus256);
+    } else {
+      x0 = fixk(and_or(W, 0x00300030u, kMagic), kSixteenth, kMinus64);
+      x1 = fixk(and_or(W, 0x00C000C0u, kMagic), kSixtyFourth, kMinus16);
     }
   } else {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int bit = 192 * h + 48 * kq;
-      const uint8_t* p = kc + o.k[0] + 3072 * sl + 384 * nt + 4 * (bit >> 5);
-      const uint64_t v = (uint64_t)ld_s32(p) | ((uint64_t)ld_s32(p + 4) << 32);
-      const uint32_t t = (uint32_t)(v >> ((bit & 31) + o.ksh));
-      const uint32_t lo = and_or(t << 13, 0x00070000u, and_or(t, 0x7u, kMagic));    // c0 | c1 << 16
-      const uint32_t t6 = t >> 6;
-      const uint32_t hi = and_or(t6 << 13, 0x00070000u, and_or(t6, 0x7u, kMagic));  // c2 | c3 << 16
-      q[2 * h] = as_u32(__hsub2(as_h2(lo), as_h2(kMagic)));
-      q[2 * h + 1] = as_u32(__hsub2(as_h2(hi), as_h2(kMagic)));
-    }
+    const uint64_t X = (((uint64_t)wd[1] << 32) | wd[0]) >> ksh;
+    const uint32_t t0 = (uint32_t)(X >> (12 * kq)), t1 = (uint32_t)(X >> (12 * kq + 6));
+    x0 = fix1(and_or(t0 << 13, 0x00070000u, and_or(t0, 0x7u, kMagic)));
+    x1 = fix1(and_or(t1 << 13, 0x00070000u, and_or(t1, 0x7u, kMagic)));
   }
 }
 
 // Value codes of the lane's channels 32 c4 + 4 g + {0..3} for the token pair
-// (t, t+1), t = 64 sl + 16 w + 2 r + 8 rp, as fp16 subnormals (code << shift)
-// * 2^-24: b[2 m] is channel 32 c4 + 4 g + 2 m, b[2 m + 1] the next channel.
+// (t, t+1), t = 64 sl + 16 w + tperm(2 r) + 8 rp, as fp16 subnormals
+// (code << shift) * 2^-24: b[2 m] is channel 32 c4 + 4 g + 2 m, b[2 m + 1] the next.
 template <int BITS>
 __device__ __forceinline__ void value_pair(const uint8_t* vc, const LaneOff& o, int sl, int rp, int c4,
                                            uint32_t (&b)[4]) {
@@ -287,42 +319,38 @@ __device__ __forceinline__ float value_scale(int e) {
   else if constexpr (BITS == 2) return 16777216.0f / (float)(1 << (2 * e));    // 2^(24-2e)
   else return (e & 1) ? 2097152.0f : 16777216.0f;                             // 2^21 : 2^24
 }
-__device__ __forceinline__ void mma16816f(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                          uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+
+// Float offset in s_acc[w][mt][g][r'] (a float4 per lane) of channel c, head h.
+template <int RQ>
+__device__ __forceinline__ int acc_index(int w, int c, int h) {
+  const int mt = 2 * (c >> 5) + ((c >> 1) & 1), gg = (c >> 2) & 7;
+  return ((((w * 8 + mt) * 8 + gg) * RQ + (h >> 1)) << 2) + 2 * (c & 1) + (h & 1);
 }
 
 // ------------------------------------------------------------------ kernel
-// Warp w owns tokens [64 s + 16 w, 64 s + 16 w + 16) of every key block, for
-// slices s < SL = BK / 64. Slice s uses the query rotated back by t0 + 64 s,
-// so the in-block rotation it still needs is R(j') with j' < 64 (a shared
-// table built once). Each warp keeps its own running (m, l, o) per head; the
-// warps merge once at the end of the split.
 //   q . k:  D[head][token]   = sum_c A(q)[head][c] B(k)[c][token]
 //   P . V:  D[channel][head] = sum_t A(v)[channel][t] B(p*s)[t][head]
 // so the score fragment of a lane is exactly its B operand for P . V.
 template <int BITS, int G, int SL>
-__global__ void __launch_bounds__(kThreads) decode_tc_kernel(const DecodeArgs a, const StageLayout L,
+__global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const DecodeArgs a, const StageLayout L,
                                                              const __grid_constant__ CUtensorMap tm_k,
                                                              const __grid_constant__ CUtensorMap tm_v) {
   constexpr int HALF = kD / 2;
   constexpr int BK = 64 * SL;
+  constexpr int NST = ring_stages(BK);
+  constexpr int RQ = (G + 1) / 2;     // lane quarters whose columns hold real heads
 
   extern __shared__ uint8_t dsmem[];
-  __shared__ __align__(8) uint64_t s_bar[kStages];
+  __shared__ __align__(8) uint64_t s_bar[NST];
   __shared__ int s_abort;
-  __shared__ float s_qp[G][kD];                          // q at q_pos, times sm_scale*log2(e)
-  __shared__ __align__(16) uint2 s_qf[2][SL][8][8][4];   // [buf][slice][k-step][row][quarter] {a0, a2}
-  __shared__ __align__(16) uint4 s_kp[2][8][4];          // [buf][k-step][quarter] {s01, s23, z01, z23} / 2
-  __shared__ __align__(16) float2 s_vsz[2][BK][4];       // value (s, z) per token and group, fp32
-  __shared__ __align__(16) uint4 s_rot[kWarps][2][4][32];  // R(j') of each lane's pairs {c, c, s, s}
-  __shared__ float4 s_tok[kWarps][16];                   // per-token outlier data of one warp
-  __shared__ float s_corr[kWarps][G][kD];                // fp32 P.V sums and value-outlier corrections
-  __shared__ float s_z[kWarps][G][4];                    // zero-point sums per 32-channel block
-  __shared__ float s_wm[kWarps][G], s_wl[kWarps][G];
+  __shared__ float s_qp[G][kD];                               // q at q_pos, times sm_scale*log2(e)
+  __shared__ __align__(16) uint4 s_qa[2][SL][8][32];          // A quads {a0, 0, a2, 0} of 2 q_block, fp16
+  __shared__ __align__(16) uint4 s_kz[2][4][4][2];            // key {s01, s23, z01, z23} / 2 [k-step][quarter][half]
+  __shared__ __align__(16) float4 s_acc[kWarps][8][8][RQ];    // P.V sums in the frame m_frame, fragment order
+  __shared__ __align__(16) float4 s_tok[kWarps][16];          // key-outlier staging of one warp
+  __shared__ float s_p[kWarps][G][16];                        // p * 2^(m - m_frame) for value outliers
+  __shared__ float s_wm[kWarps][G], s_wl[kWarps][G], s_wf[kWarps][G];
+  __shared__ float s_z[kWarps][G][4];                         // zero-point sums per 32-channel block
 
   const Dims d = a.d;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -333,9 +361,12 @@ __global__ void __launch_bounds__(kThreads) decode_tc_kernel(const DecodeArgs a,
   const int units = a.n_full + (a.tail_len > 0 ? 1 : 0);
   const int u0 = (int)((long long)split * units / a.n_split);
   const int u1 = (int)((long long)(split + 1) * units / a.n_split);
-  const int n_out = d.n_out, ng = d.ng, Gv = d.Gv;
+  const int n_out = d.n_out, ng = d.ng;
+  const int gv_sh = __ffs(d.Gv) - 1, ng_sh = __ffs(ng) - 1;
   float* ws_base = a.ws + (((size_t)b * a.H_q + hkv * G) * a.S + split) * (kD + 2);
   const LaneOff lo = lane_offsets<BITS>(w, g, r);
+  const uint4* rot_tab = a.rope ? reinterpret_cast<const uint4*>(a.rope + rope_frag_off(d)) : g_rot_identity;
+  const uint4* rot = rot_tab + rot_frag_index(w, 0, 0, lane);
 
   uint8_t* ring = dsmem + ((1024u - (smem_addr(dsmem) & 1023u)) & 1023u);
   const uint32_t ring_s = smem_addr(ring);
@@ -356,71 +387,78 @@ __global__ void __launch_bounds__(kThreads) decode_tc_kernel(const DecodeArgs a,
   };
   auto wait_unit = [&](int u) -> bool {
     const int k = u - u0;
-    return mbar_wait(smem_addr(&s_bar[k % kStages]), (uint32_t)((k / kStages) & 1));
-  };
-  // Per-block tables shared by the warps: q rotated back to each slice start
-  // (fp16, fragment order), the key scale/zero pairs (halved, fragment order)
-  // and the value scale/zero per token and group (fp32).
-  auto prep = [&](int u) {
-    const int buf = (u - u0) & 1;
-    const uint8_t* st = ring + ((u - u0) % kStages) * L.stage_bytes;
-    for (int e = tid; e < SL * G * HALF; e += kThreads) {
-      const int sl = e / (G * HALF), gg = (e / HALF) % G, i = e % HALF;
-      float x = s_qp[gg][i], y = s_qp[gg][i + HALF];
-      if (a.rope) {
-        float2 rr = rope_block(a.rope, d, u, i);                             // R(t0)
-        if (sl) rr = rot_compose(rr, rope_fine(a.rope, d, 64 * sl, i));       // R(t0 + 64 sl)
-        const float x2 = fmaf(x, rr.x, y * rr.y), y2 = fmaf(y, rr.x, -x * rr.y);   // apply R(-.)
-        x = x2;
-        y = y2;
-      }
-      int rq, sq;
-      chan_slot<BITS>(i & 15, rq, sq);
-      reinterpret_cast<__half*>(&s_qf[buf][sl][i >> 4][gg][rq])[sq] = __float2half_rn(x);
-      reinterpret_cast<__half*>(&s_qf[buf][sl][4 + (i >> 4)][gg][rq])[sq] = __float2half_rn(y);
-    }
-    if (u != a.n_full) {
-      const uint32_t* km = reinterpret_cast<const uint32_t*>(st + L.km);
-      for (int c = tid; c < kD; c += kThreads) {
-        const uint32_t m = km[c];
-        const int kq = (c < HALF) ? (c >> 4) : 4 + ((c - HALF) >> 4);
-        int rq, sq;
-        chan_slot<BITS>(c & 15, rq, sq);
-        __half* e = reinterpret_cast<__half*>(&s_kp[buf][kq][rq]);
-        e[sq] = __hmul(__ushort_as_half((uint16_t)(m & 0xFFFFu)), __float2half_rn(0.5f));
-        e[4 + sq] = __hmul(__ushort_as_half((uint16_t)(m >> 16)), __float2half_rn(0.5f));
-      }
-    }
-    const uint32_t* vm = reinterpret_cast<const uint32_t*>(st + L.vm);
-    for (int e = tid; e < BK * ng; e += kThreads) {
-      const uint32_t m = vm[e];
-      s_vsz[buf][e / ng][e % ng] = make_float2(h2f((uint16_t)(m & 0xFFFFu)), h2f((uint16_t)(m >> 16)));
-    }
+    return mbar_wait(smem_addr(&s_bar[k % NST]), (uint32_t)((k / NST) & 1));
   };
   auto abort_split = [&](int u) {
     // drain every copy still in flight, then report NaN for this split
-    for (int x = u; x < u1 && x < u + kStages; ++x) wait_unit(x);
+    for (int x = u; x < u1 && x < u + NST; ++x) wait_unit(x);
     for (int e = tid; e < G * (kD + 2); e += kThreads)
       ws_base[(size_t)(e / (kD + 2)) * a.S * (kD + 2) + e % (kD + 2)] = __int_as_float(0x7fffffff);
   };
-  // fp16 block-rotated q of head gg at channel c (k-step order), for outlier weights
-  auto q_at = [&](int buf, int sl, int gg, int c) -> float {
-    int rq, sq;
-    chan_slot<BITS>(c & 15, rq, sq);
-    const int kq = (c < HALF) ? (c >> 4) : 4 + ((c - HALF) >> 4);
-    return __half2float(reinterpret_cast<const __half*>(&s_qf[buf][sl][kq][gg][rq])[sq]);
+
+  // ---- per-thread constants of the block preparation
+  // queries: thread owns rotate-half pair qi and heads tid/64, tid/64 + 2, ...
+  const int qi = tid & (HALF - 1);
+  const bool q_thread = (G > 1) || (tid < HALF);
+  uint32_t q_off;
+  {
+    int rr, kq, s;
+    kslot<BITS>(qi, rr, kq, s);
+    q_off = (uint32_t)((kq * 32 + rr) * 16 + aslot_byte(s));   // head 0, first half; + 64 g, + 2048 partner
+  }
+  // key scale/zero: thread owns channel tid
+  uint32_t kz_off;
+  {
+    int rr, kq, s;
+    kslot<BITS>(tid & (HALF - 1), rr, kq, s);
+    kz_off = (uint32_t)(((kq * 4 + rr) * 2 + (tid >> 6)) * 16 + slot_byte(s));   // s; z at + 8
+  }
+  // rotations of pair qi: block start R(t0) from the coarse tables, slice step R(64)
+  float2 r64 = make_float2(1.0f, 0.0f);
+  if (a.rope && SL > 1 && q_thread) r64 = rope_fine(a.rope, d, 64, qi);
+  auto block_rot = [&](int u) -> float2 {
+    return (a.rope && q_thread) ? rope_block(a.rope, d, u, qi) : make_float2(1.0f, 0.0f);
+  };
+
+  // Per-block tables shared by the warps: the queries rotated back to each
+  // slice start (fp16 A quads, doubled for the halved keys) and the key
+  // scale/zero (halved, fragment order).
+  auto prep = [&](int u, float2 rr) {
+    const int buf = (u - u0) & 1;
+    const uint8_t* st = ring + ((u - u0) % NST) * L.stage_bytes;
+    if (q_thread) {
+#pragma unroll
+      for (int sl = 0; sl < SL; ++sl) {
+        const float2 rs = sl ? rot_compose(rr, r64) : rr;
+        uint8_t* qa = reinterpret_cast<uint8_t*>(&s_qa[buf][sl][0][0]) + q_off;
+#pragma unroll
+        for (int gg = (G > 1 ? (tid >> 6) : 0); gg < G; gg += 2) {
+          const float x = s_qp[gg][qi], y = s_qp[gg][qi + HALF];
+          const float x2 = fmaf(x, rs.x, y * rs.y), y2 = fmaf(y, rs.x, -x * rs.y);   // apply R(-t)
+          *reinterpret_cast<__half*>(qa + 64 * gg) = __float2half_rn(2.0f * x2);
+          *reinterpret_cast<__half*>(qa + 64 * gg + 2048) = __float2half_rn(2.0f * y2);
+        }
+      }
+    }
+    if (u != a.n_full) {
+      const uint32_t m = reinterpret_cast<const uint32_t*>(st + L.km)[tid];
+      const uint32_t mh = as_u32(__hmul2(as_h2(m), __float2half2_rn(0.5f)));
+      uint8_t* kz = reinterpret_cast<uint8_t*>(&s_kz[buf][0][0][0]) + kz_off;
+      *reinterpret_cast<uint16_t*>(kz) = (uint16_t)(mh & 0xFFFFu);
+      *reinterpret_cast<uint16_t*>(kz + 8) = (uint16_t)(mh >> 16);
+    }
   };
 
   // ---- prologue
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(smem_addr(&s_bar[s]), 1);
+    for (int s = 0; s < NST; ++s) mbar_init(smem_addr(&s_bar[s]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     s_abort = 0;
   }
   __syncthreads();
   if (tid == 0)
-    for (int k = 0; k < kStages && u0 + k < u1; ++k) issue(u0 + k, k);
+    for (int k = 0; k < NST && u0 + k < u1; ++k) issue(u0 + k, k);
   for (int e = tid; e < G * HALF; e += kThreads) {
     const int gg = e / HALF, i = e % HALF;
     const __half* qh = a.q + ((size_t)b * a.H_q + hkv * G + gg) * kD;
@@ -435,62 +473,52 @@ __global__ void __launch_bounds__(kThreads) decode_tc_kernel(const DecodeArgs a,
     s_qp[gg][i + HALF] = y * a.scale_log2;
   }
   {
-    uint32_t* z = reinterpret_cast<uint32_t*>(&s_qf[0][0][0][0][0]);
-    for (int e = tid; e < (int)(sizeof(s_qf) / 4); e += kThreads) z[e] = 0u;
-    for (int e = tid; e < kWarps * G * kD; e += kThreads) (&s_corr[0][0][0])[e] = 0.0f;
-  }
-  // in-block rotation R(j'), j' = 16 w + 8 nt + g, of the lane's channel pairs
-  if (a.rope) {
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const int j = 16 * w + 8 * nt + g;
-#pragma unroll
-      for (int kq = 0; kq < 4; ++kq) {
-        uint32_t cs[2], sn[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float2 c0 = rope_fine(a.rope, d, j, 16 * kq + chan_off<BITS>(r, 2 * h));
-          const float2 c1 = rope_fine(a.rope, d, j, 16 * kq + chan_off<BITS>(r, 2 * h + 1));
-          cs[h] = as_u32(__floats2half2_rn(c0.x, c1.x));
-          sn[h] = as_u32(__floats2half2_rn(c0.y, c1.y));
-        }
-        s_rot[w][nt][kq][lane] = make_uint4(cs[0], cs[1], sn[0], sn[1]);
-      }
-    }
+    uint32_t* z = reinterpret_cast<uint32_t*>(&s_qa[0][0][0][0]);
+    for (int e = tid; e < (int)(sizeof(s_qa) / 4); e += kThreads) z[e] = 0u;
+    float* f = reinterpret_cast<float*>(&s_acc[0][0][0][0]);
+    for (int e = tid; e < (int)(sizeof(s_acc) / 4); e += kThreads) f[e] = 0.0f;
   }
   float o[8][4];     // P.V accumulators: 8 m-tiles of 16 channels x heads (2r, 2r+1)
 #pragma unroll
   for (int n = 0; n < 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
   float m_run = -INFINITY, l_run = 0.0f;
-  float zacc[4] = {0.f, 0.f, 0.f, 0.f};   // sum_t p z for head g, per 32-channel block
+  float m_frame = -INFINITY, fac = 1.0f;   // s_acc frame of head g; fac = 2^(m_run - m_frame)
+  float zacc[4] = {0.f, 0.f, 0.f, 0.f};    // sum_t p z for head g, per 32-channel block
+  float2 rr_next = make_float2(1.0f, 0.0f);
   __syncthreads();
   if (u0 < u1) {
+    const float2 rr0 = block_rot(u0);
     const bool ok = wait_unit(u0);
     if (__syncthreads_or(!ok)) {
       abort_split(u0);
       return;
     }
-    prep(u0);
+    prep(u0, rr0);
+    if (u0 + 1 < u1) rr_next = block_rot(u0 + 1);
   }
   __syncthreads();
 
-  const __half* k_tail = a.k_tail + (size_t)bh * BK * kD;
-
-  // flush the P.V accumulators into the fp32 sums of heads 2r, 2r+1
+  // P.V accumulators into the shared sums (frame m_frame), then cleared
   auto flush_o = [&]() {
+    const float fa = __shfl_sync(0xffffffffu, fac, 8 * r), fb = __shfl_sync(0xffffffffu, fac, (8 * r + 4) & 31);
+    if (r < RQ) {
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int head = 2 * r + (e & 1);
-        const int ch = 32 * (mt >> 1) + 4 * g + 2 * (mt & 1) + (e >> 1);
-        if (head < G) s_corr[w][head][ch] = fmaf(o[mt][e], value_scale<BITS>(2 * (mt & 1) + (e >> 1)), s_corr[w][head][ch]);
-        o[mt][e] = 0.0f;
+      for (int mt = 0; mt < 8; ++mt) {
+        const float v0 = value_scale<BITS>(2 * (mt & 1)), v1 = value_scale<BITS>(2 * (mt & 1) + 1);
+        float4 v = s_acc[w][mt][g][r];
+        v.x = fmaf(o[mt][0], v0 * fa, v.x);
+        v.y = fmaf(o[mt][1], v0 * fb, v.y);
+        v.z = fmaf(o[mt][2], v1 * fa, v.z);
+        v.w = fmaf(o[mt][3], v1 * fb, v.w);
+        s_acc[w][mt][g][r] = v;
       }
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
   };
 
   for (int u = u0; u < u1; ++u) {
-    const int k = u - u0, stage = k % kStages, buf = k & 1;
+    const int k = u - u0, stage = k % NST, buf = k & 1;
     const bool is_tail = (u == a.n_full);
     const int ntok = is_tail ? a.tail_len : BK;
     const uint8_t* st = ring + stage * L.stage_bytes;
@@ -498,125 +526,143 @@ __global__ void __launch_bounds__(kThreads) decode_tc_kernel(const DecodeArgs a,
     const uint8_t* vc = st + L.vc;
     const uint32_t* km = reinterpret_cast<const uint32_t*>(st + L.km);
     const uint32_t* ko = reinterpret_cast<const uint32_t*>(st + L.ko);
+    const uint32_t* vm = reinterpret_cast<const uint32_t*>(st + L.vm);
     const uint32_t* vo = reinterpret_cast<const uint32_t*>(st + L.vo);
 
-    // ---- scores of the warp's tokens (rows = heads, 2 n-tiles per slice)
-    float sc[SL][2][2];
-#pragma unroll
+    // ---- scores of the warp's tokens (rows = heads; column n of n-tile nt
+    // is token 64 sl + 16 w + 8 nt + tperm(n))
+#pragma unroll 1
     for (int sl = 0; sl < SL; ++sl) {
-      // two accumulator chains per n-tile (first-half / partner k-steps)
-      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      float sc[2][2];
+      float acc[2][2][4];   // [n-tile][first half / partner]
 #pragma unroll
-      for (int kq = 0; kq < 4; ++kq) {
-        const uint2 qa = s_qf[buf][sl][kq][g][r];
-        const uint2 qb = s_qf[buf][sl][kq + 4][g][r];
-        uint4 kp = make_uint4(0u, 0u, 0u, 0u), kpp = kp;
-        if (!is_tail) {
-          kp = s_kp[buf][kq][r];
-          kpp = s_kp[buf][kq + 4][r];
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) acc[nt][h][0] = acc[nt][h][1] = acc[nt][h][2] = acc[nt][h][3] = 0.0f;
+      if (!is_tail) {
+        KeyWords kw[2];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) kw[nt] = key_words<BITS>(kc, lo, 64 * sl + 8 * nt);
+#pragma unroll
+        for (int kq = 0; kq < 4; ++kq) {
+          const uint4 qf = s_qa[buf][sl][kq][lane], qp = s_qa[buf][sl][kq + 4][lane];
+          const uint4 zf = s_kz[buf][kq][r][0], zp = s_kz[buf][kq][r][1];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            uint32_t f0, f1, p0, p1;
+            key_codes<BITS>(kw[nt].f, lo.ksh, kq, f0, f1);
+            key_codes<BITS>(kw[nt].p, lo.ksh, kq, p0, p1);
+            const __half2 xf0 = __hfma2(as_h2(f0), as_h2(zf.x), as_h2(zf.z));
+            const __half2 xf1 = __hfma2(as_h2(f1), as_h2(zf.y), as_h2(zf.w));
+            const __half2 xp0 = __hfma2(as_h2(p0), as_h2(zp.x), as_h2(zp.z));
+            const __half2 xp1 = __hfma2(as_h2(p1), as_h2(zp.y), as_h2(zp.w));
+            const uint4 rt = __ldg(rot + (nt * 4 + kq) * 32);
+            const __half2 c01 = as_h2(rt.x), c23 = as_h2(rt.y), s01 = as_h2(rt.z), s23 = as_h2(rt.w);
+            const __half2 kf0 = __hfma2(xf0, c01, __hneg2(__hmul2(xp0, s01)));
+            const __half2 kp0 = __hfma2(xp0, c01, __hmul2(xf0, s01));
+            const __half2 kf1 = __hfma2(xf1, c23, __hneg2(__hmul2(xp1, s23)));
+            const __half2 kp1 = __hfma2(xp1, c23, __hmul2(xf1, s23));
+            mma16816(acc[nt][0], qf, as_u32(kf0), as_u32(kf1));
+            mma16816(acc[nt][1], qp, as_u32(kp0), as_u32(kp1));
+          }
         }
+      } else {
+        // unfinished block: fp16 keys from K_TAIL (halved), same rotation
+        const __half* k_tail = a.k_tail + (size_t)bh * k_tail_stream(d);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const int j = 64 * sl + 16 * w + 8 * nt + g;
-          uint32_t kv[4];
-          if (!is_tail) {
-            uint32_t q[4];
-            key_codes<BITS>(kc, lo, sl, nt, kq, q);
-            kv[0] = as_u32(__hfma2(as_h2(q[0]), as_h2(kp.x), as_h2(kp.z)));
-            kv[1] = as_u32(__hfma2(as_h2(q[1]), as_h2(kp.y), as_h2(kp.w)));
-            kv[2] = as_u32(__hfma2(as_h2(q[2]), as_h2(kpp.x), as_h2(kpp.z)));
-            kv[3] = as_u32(__hfma2(as_h2(q[3]), as_h2(kpp.y), as_h2(kpp.w)));
-          } else {
+        for (int kq = 0; kq < 4; ++kq) {
+          const uint4 qf = s_qa[buf][sl][kq][lane], qp = s_qa[buf][sl][kq + 4][lane];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c0 = 16 * kq + chan_off<BITS>(r, 2 * (e & 1)) + HALF * (e >> 1);
-              const int c1 = 16 * kq + chan_off<BITS>(r, 2 * (e & 1) + 1) + HALF * (e >> 1);
-              __half2 v = __floats2half2_rn(0.f, 0.f);
+          for (int nt = 0; nt < 2; ++nt) {
+            const int j = 64 * sl + 16 * w + 8 * nt + tperm(g);
+            __half xs[8];
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+              const int c = kchan<BITS>(r, kq, s);
+              xs[s] = xs[4 + s] = __float2half_rn(0.0f);
               if (j < ntok) {
-                const __half* row = k_tail + (size_t)j * kD;
-                v = __halves2half2(row[c0], row[c1]);
+                xs[s] = __hmul(k_tail[(size_t)j * kD + c], __float2half_rn(0.5f));
+                xs[4 + s] = __hmul(k_tail[(size_t)j * kD + c + HALF], __float2half_rn(0.5f));
               }
-              kv[e] = as_u32(__hmul2(v, as_h2(kHalf)));
             }
+            const __half2 xf0 = __halves2half2(xs[0], xs[1]), xf1 = __halves2half2(xs[2], xs[3]);
+            const __half2 xp0 = __halves2half2(xs[4], xs[5]), xp1 = __halves2half2(xs[6], xs[7]);
+            const uint4 rt = __ldg(rot + (nt * 4 + kq) * 32);
+            const __half2 c01 = as_h2(rt.x), c23 = as_h2(rt.y), s01 = as_h2(rt.z), s23 = as_h2(rt.w);
+            const __half2 kf0 = __hfma2(xf0, c01, __hneg2(__hmul2(xp0, s01)));
+            const __half2 kp0 = __hfma2(xp0, c01, __hmul2(xf0, s01));
+            const __half2 kf1 = __hfma2(xf1, c23, __hneg2(__hmul2(xp1, s23)));
+            const __half2 kp1 = __hfma2(xp1, c23, __hmul2(xf1, s23));
+            mma16816(acc[nt][0], qf, as_u32(kf0), as_u32(kf1));
+            mma16816(acc[nt][1], qp, as_u32(kp0), as_u32(kp1));
           }
-          if (a.rope) {
-            const uint4 rt = s_rot[w][nt][kq][lane];
-            const uint32_t rcs[2] = {rt.x, rt.y}, rsn[2] = {rt.z, rt.w};
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const __half2 x = as_h2(kv[h]), y = as_h2(kv[h + 2]);
-              const __half2 c = as_h2(rcs[h]), s = as_h2(rsn[h]);
-              kv[h] = as_u32(__hfma2(x, c, __hneg2(__hmul2(y, s))));
-              kv[h + 2] = as_u32(__hfma2(y, c, __hmul2(x, s)));
-            }
-          }
-          mma16816(acc[nt], qa.x, qa.y, kv[0], kv[1]);
-          mma16816(acc2[nt], qb.x, qb.y, kv[2], kv[3]);
         }
       }
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        sc[sl][nt][0] = 2.0f * (acc[nt][0] + acc2[nt][0]);
-        sc[sl][nt][1] = 2.0f * (acc[nt][1] + acc2[nt][1]);
+        sc[nt][0] = acc[nt][0][0] + acc[nt][1][0];
+        sc[nt][1] = acc[nt][0][1] + acc[nt][1][1];
       }
-      // dense-and-sparse keys: (x_out - x_dense) * <q, R(j') e_c> per outlier
+      // dense-and-sparse keys: (x_out - x_dense) * <q, R(j) e_c> per outlier
       if (n_out > 0 && !is_tail) {
         for (int oi = 0; oi < n_out; ++oi) {
           if (lane < 16) {
-            const int t = 64 * sl + 16 * w + lane;
-            const uint32_t e = ko[t * n_out + oi];
-            const int c = (int)(e & 0xFFFFu);
+            const int nt_ = lane >> 3, n_ = lane & 7;
+            const int row = 64 * sl + 16 * w + 8 * nt_ + tperm(n_);
+            const uint32_t e = ko[row * n_out + oi];
+            const int c = (int)(e & (kD - 1));
             const uint32_t m = km[c];
-            const float xd = fmaf((float)tile_code<BITS>(kc, t, c), h2f((uint16_t)(m & 0xFFFFu)),
+            const float xd = fmaf((float)tile_code<BITS>(kc, row, c), h2f((uint16_t)(m & 0xFFFFu)),
                                   h2f((uint16_t)(m >> 16)));
-            float2 rot = make_float2(1.f, 0.f);
-            if (a.rope) rot = rope_fine(a.rope, d, 16 * w + lane, c & (HALF - 1));
-            s_tok[w][lane] = make_float4(h2f((uint16_t)(e >> 16)) - xd, __int_as_float(c), rot.x, rot.y);
+            int rr, kq, s;
+            kslot<BITS>(c & (HALF - 1), rr, kq, s);
+            const uint8_t* rp =
+                reinterpret_cast<const uint8_t*>(rot_tab + rot_frag_index(w, nt_, kq, 4 * n_ + rr)) + slot_byte(s);
+            const float cs = __half2float(__ldg(reinterpret_cast<const __half*>(rp)));
+            const float sn = __half2float(__ldg(reinterpret_cast<const __half*>(rp + 8)));
+            const bool first = c < HALF;
+            s_tok[w][lane] = make_float4(0.5f * (h2f((uint16_t)(e >> 16)) - xd), first ? cs : -sn, first ? sn : cs,
+                                         __int_as_float((kq * 32 + rr) * 16 + aslot_byte(s)));
           }
           __syncwarp();
           if (g < G) {
+            const uint8_t* qa = reinterpret_cast<const uint8_t*>(&s_qa[buf][sl][0][0]) + 64 * g;
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
                 const float4 T = s_tok[w][8 * nt + 2 * r + e];
-                const int c = __float_as_int(T.y), i = c & (HALF - 1);
-                const float qx = q_at(buf, sl, g, i), qy = q_at(buf, sl, g, i + HALF);
-                const float wgt = (c < HALF) ? fmaf(qx, T.z, qy * T.w) : fmaf(qy, T.z, -qx * T.w);
-                sc[sl][nt][e] = fmaf(T.x, wgt, sc[sl][nt][e]);
+                const int qa_off = __float_as_int(T.w);
+                const float wgt = fmaf(ld_h(qa + qa_off), T.y, ld_h(qa + qa_off + 2048) * T.z);
+                sc[nt][e] = fmaf(T.x, wgt, sc[nt][e]);
               }
-            }
           }
           __syncwarp();
         }
       }
+      if (is_tail) {
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int e = 0; e < 2; ++e)
-          if (64 * sl + 16 * w + 8 * nt + 2 * r + e >= ntok) sc[sl][nt][e] = -INFINITY;
-    }
+          for (int e = 0; e < 2; ++e)
+            if (64 * sl + 16 * w + 8 * nt + tperm(2 * r + e) >= ntok) sc[nt][e] = -INFINITY;
+      }
 
     // ---- online softmax of this warp's tokens (row g: head g; 4 lanes per row)
     float mb = -INFINITY;
 #pragma unroll
-    for (int sl = 0; sl < SL; ++sl)
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) mb = fmaxf(mb, fmaxf(sc[sl][nt][0], sc[sl][nt][1]));
+      for (int nt = 0; nt < 2; ++nt) mb = fmaxf(mb, fmaxf(sc[nt][0], sc[nt][1]));
     mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
     mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
     const float m_new = fmaxf(m_run, mb);
-    const float alpha = (m_new == -INFINITY) ? 1.0f : exp2f(m_run - m_new);
+    const float alpha = (m_new == -INFINITY) ? 1.0f : ex2(m_run - m_new);
     float psum = 0.0f;
-#pragma unroll
-    for (int sl = 0; sl < SL; ++sl)
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float p = (sc[sl][nt][e] == -INFINITY) ? 0.0f : exp2f(sc[sl][nt][e] - m_new);
-          sc[sl][nt][e] = p;
+          const float p = (sc[nt][e] == -INFINITY) ? 0.0f : ex2(sc[nt][e] - m_new);
+          sc[nt][e] = p;
           psum += p;
         }
     l_run = fmaf(l_run, alpha, psum);
@@ -634,62 +680,75 @@ __global__ void __launch_bounds__(kThreads) decode_tc_kernel(const DecodeArgs a,
       }
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) zacc[c4] *= alpha;
-      if (g < G)
-        for (int c = r; c < kD; c += 4) s_corr[w][g][c] *= alpha;
-      __syncwarp();
+      if (m_frame == -INFINITY) m_frame = m_run;
+      fac = (m_frame == -INFINITY) ? 1.0f : ex2(m_run - m_frame);
+      if (__any_sync(0xffffffffu, m_run - m_frame > kFrameGap)) {
+        // move the shared sums to the current frame
+        const float rf = (m_frame == -INFINITY) ? 1.0f : ex2(m_frame - m_run);
+        const float ra = __shfl_sync(0xffffffffu, rf, 8 * r), rb = __shfl_sync(0xffffffffu, rf, (8 * r + 4) & 31);
+        __syncwarp();
+        if (r < RQ) {
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            float4 v = s_acc[w][mt][g][r];
+            v.x *= ra;
+            v.y *= rb;
+            v.z *= ra;
+            v.w *= rb;
+            s_acc[w][mt][g][r] = v;
+          }
+        }
+        __syncwarp();
+        m_frame = m_run;
+        fac = 1.0f;
+      }
     }
 
-    // ---- value outliers: p * (x_out - x_dense) into the warp's corrections
+    // ---- value outliers: p * (x_out - x_dense) into the shared sums
     if (n_out > 0) {
+      {
+        if (g < G) {
 #pragma unroll
-      for (int sl = 0; sl < SL; ++sl) {
-        for (int oi = 0; oi < n_out; ++oi) {
-          if (lane < 16) {
-            const int t = 64 * sl + 16 * w + lane;
-            float4 T = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (t < ntok) {
-              const uint32_t e = vo[t * n_out + oi];
-              const int c = (int)(e & 0xFFFFu);
-              const float2 sz = s_vsz[buf][t][c / Gv];
-              const float xd = fmaf((float)tile_code<BITS>(vc, t, c), sz.x, sz.y);
-              T = make_float4(h2f((uint16_t)(e >> 16)) - xd, __int_as_float(c), 0.f, 0.f);
-            }
-            s_tok[w][lane] = T;
+          for (int nt = 0; nt < 2; ++nt) {
+            s_p[w][g][8 * nt + 2 * r] = sc[nt][0] * fac;
+            s_p[w][g][8 * nt + 2 * r + 1] = sc[nt][1] * fac;
           }
-          __syncwarp();
-          if (g < G) {
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const float4 T = s_tok[w][8 * nt + 2 * r + e];
-                if (T.x != 0.0f) atomicAdd(&s_corr[w][g][__float_as_int(T.y)], sc[sl][nt][e] * T.x);
-              }
-          }
-          __syncwarp();
         }
+        __syncwarp();
+        if (lane < 16) {
+          const int row = 64 * sl + 16 * w + 8 * (lane >> 3) + tperm(lane & 7);
+          if (row < ntok) {
+            for (int oi = 0; oi < n_out; ++oi) {
+              const uint32_t e = vo[row * n_out + oi];
+              const int c = (int)(e & (kD - 1));
+              const float2 sz = __half22float2(as_h2(vm[(row << ng_sh) + (c >> gv_sh)]));
+              const float delta = h2f((uint16_t)(e >> 16)) - fmaf((float)tile_code<BITS>(vc, row, c), sz.x, sz.y);
+              float* accs = reinterpret_cast<float*>(&s_acc[0][0][0][0]);
+#pragma unroll
+              for (int h = 0; h < G; ++h) red_add(accs + acc_index<RQ>(w, c, h), s_p[w][h][lane] * delta);
+            }
+          }
+        }
+        __syncwarp();
       }
     }
 
     // ---- P . V: A = value codes (16 channels x 16 tokens), B = p * s (fp16 hi + lo)
-#pragma unroll
-    for (int sl = 0; sl < SL; ++sl) {
-      const int t0 = 64 * sl + 16 * w + 2 * r;         // tokens t0, t0+1, t0+8, t0+9
-      const int tt[4] = {t0, t0 + 1, t0 + 8, t0 + 9};
-      const float pp[4] = {sc[sl][0][0], sc[sl][0][1], sc[sl][1][0], sc[sl][1][1]};
+    {
+      const int tb = 64 * sl + 16 * w + tperm(2 * r);
+      const int tt[4] = {tb, tb + 1, tb + 8, tb + 9};
+      const float pp[4] = {sc[0][0], sc[0][1], sc[1][0], sc[1][1]};
       uint32_t bh0 = 0u, bh1 = 0u, bl0 = 0u, bl1 = 0u;
-      int cur_gr = -1;
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
-        const int gr = (32 * c4) / Gv;
-        if (gr != cur_gr) {
-          cur_gr = gr;
+        const int gr = (32 * c4) >> gv_sh;
+        if (c4 == 0 || gr != ((32 * (c4 - 1)) >> gv_sh)) {
           float A[4], zs = 0.0f;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             A[i] = 0.0f;
-            if (tt[i] < ntok) {
-              const float2 sz = s_vsz[buf][tt[i]][gr];
+            if (!is_tail || tt[i] < ntok) {
+              const float2 sz = __half22float2(as_h2(vm[(tt[i] << ng_sh) + gr]));
               A[i] = pp[i] * sz.x;
               zs = fmaf(pp[i], sz.y, zs);
             }
@@ -710,11 +769,14 @@ __global__ void __launch_bounds__(kThreads) decode_tc_kernel(const DecodeArgs a,
         value_pair<BITS>(vc, lo, sl, 1, c4, x1);
 #pragma unroll
         for (int mi = 0; mi < 2; ++mi) {
-          mma16816f(o[2 * c4 + mi], x0[2 * mi], x0[2 * mi + 1], x1[2 * mi], x1[2 * mi + 1], bh0, bh1);
-          mma16816f(o[2 * c4 + mi], x0[2 * mi], x0[2 * mi + 1], x1[2 * mi], x1[2 * mi + 1], bl0, bl1);
+          const uint4 av = make_uint4(x0[2 * mi], x0[2 * mi + 1], x1[2 * mi], x1[2 * mi + 1]);
+          mma16816(o[2 * c4 + mi], av, bh0, bh1);
+          mma16816(o[2 * c4 + mi], av, bl0, bl1);
         }
       }
     }
+
+    }  // slices
 
     // ---- every kFlush blocks move the P.V accumulators into the fp32 sums:
     // the tensor-core accumulation of many small positive products drifts
@@ -727,14 +789,15 @@ __global__ void __launch_bounds__(kThreads) decode_tc_kernel(const DecodeArgs a,
     // ---- next block's tables; release this stage for the refill
     if (u + 1 < u1) {
       if (!wait_unit(u + 1)) s_abort = 1;
-      prep(u + 1);
+      prep(u + 1, rr_next);
+      if (u + 2 < u1) rr_next = block_rot(u + 2);
     }
     __syncthreads();
     if (s_abort) {
       abort_split(u + 1);
       return;
     }
-    if (tid == 0 && u + kStages < u1) issue(u + kStages, stage);
+    if (tid == 0 && u + NST < u1) issue(u + NST, stage);
   }
 
   // ---- merge the warps
@@ -750,10 +813,12 @@ __global__ void __launch_bounds__(kThreads) decode_tc_kernel(const DecodeArgs a,
   if (g < G && r == 0) {
     s_wm[w][g] = m_run;
     s_wl[w][g] = l_run;
+    s_wf[w][g] = (m_frame == -INFINITY) ? 0.0f : ex2(m_frame - m_run);
 #pragma unroll
     for (int c4 = 0; c4 < 4; ++c4) s_z[w][g][c4] = zacc[c4];
   }
   __syncthreads();
+  const float* accs = reinterpret_cast<const float*>(&s_acc[0][0][0][0]);
   for (int e = tid; e < G * kD; e += kThreads) {
     const int gg = e / kD, ch = e % kD;
     float M = -INFINITY;
@@ -762,8 +827,8 @@ __global__ void __launch_bounds__(kThreads) decode_tc_kernel(const DecodeArgs a,
     float sum = 0.0f, lsum = 0.0f;
 #pragma unroll
     for (int ww = 0; ww < kWarps; ++ww) {
-      const float f = (s_wm[ww][gg] == -INFINITY) ? 0.0f : exp2f(s_wm[ww][gg] - M);
-      sum = fmaf(f, s_corr[ww][gg][ch] + s_z[ww][gg][ch >> 5], sum);
+      const float f = (s_wm[ww][gg] == -INFINITY) ? 0.0f : ex2(s_wm[ww][gg] - M);
+      sum = fmaf(f, fmaf(accs[acc_index<RQ>(ww, ch, gg)], s_wf[ww][gg], s_z[ww][gg][ch >> 5]), sum);
       lsum = fmaf(f, s_wl[ww][gg], lsum);
     }
     float* dst = ws_base + (size_t)gg * a.S * (kD + 2);
