@@ -41,6 +41,16 @@
 namespace kvq {
 namespace tc {
 
+#ifndef KVQ_TC_QK_CHAINS
+#define KVQ_TC_QK_CHAINS 1   // accumulator chains per n-tile in q . k (1: first half and partner share one)
+#endif
+#ifndef KVQ_TC_PV_LO
+#define KVQ_TC_PV_LO 0       // 1: B = p*s as fp16 hi + lo (two mma); 0: hi only
+#endif
+#ifndef KVQ_TC_MINB
+#define KVQ_TC_MINB 4        // CTAs per SM the register allocation is held to
+#endif
+
 constexpr uint32_t kWaitLimit = 1u << 20;  // mbarrier polls before giving up (~1 s)
 constexpr int kFlush = 8;                   // blocks between P.V accumulator flushes
 constexpr float kFrameGap = 64.0f;          // renormalise the shared sums past 2^64
@@ -181,7 +191,7 @@ __device__ __forceinline__ uint32_t tile_code(const uint8_t* tile, int row, int 
 struct LaneOff {
   uint32_t kf, kp;      // key: first-half and partner codes
   uint32_t ksh;         // INT3: bit shift of the lane's 48-bit key window
-  uint32_t v[4];        // value tile (INT4: per 32-channel block; INT2: per 16 B half; INT3: [0])
+  uint32_t vb, vx;      // value tile: row base and swizzle (chunk c at vb + ((c << 4) ^ vx))
   uint32_t vsh;         // INT3: bit shift of the lane's value codes
   uint32_t sel0, sel1;  // byte_perm selectors of the lane's value bytes
 };
@@ -189,8 +199,7 @@ struct LaneOff {
 template <int BITS>
 __device__ __forceinline__ LaneOff lane_offsets(int w, int g, int r) {
   LaneOff o;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) o.v[c] = 0u;
+  o.vb = o.vx = 0u;
   o.ksh = o.vsh = o.sel0 = o.sel1 = 0u;
   const int tk = tperm(g), tv = tperm(2 * r);
   const int krow = 16 * w + tk, vrow = 16 * w + tv;
@@ -198,22 +207,22 @@ __device__ __forceinline__ LaneOff lane_offsets(int w, int g, int r) {
     const int ksw = (tk >> 1) & 3, vsw = (tv >> 1) & 3, bb = 2 * (g & 1);
     o.kf = 64 * krow + (((r >> 1) ^ ksw) << 4) + 8 * (r & 1);
     o.kp = 64 * krow + (((2 + (r >> 1)) ^ ksw) << 4) + 8 * (r & 1);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) o.v[c] = 64 * vrow + ((c ^ vsw) << 4) + 4 * (g >> 1);
+    o.vb = 64 * vrow + 4 * (g >> 1);
+    o.vx = vsw << 4;
     o.sel0 = (uint32_t)(bb | ((bb + 4) << 8));
     o.sel1 = (uint32_t)((bb + 1) | ((bb + 5) << 8));
   } else if constexpr (BITS == 2) {
     const int ksw = (tk >> 2) & 1, vsw = (tv >> 2) & 1, bb = g & 3;
     o.kf = 32 * krow + (ksw << 4) + 4 * r;
     o.kp = 32 * krow + ((1 ^ ksw) << 4) + 4 * r;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) o.v[h] = 32 * vrow + ((h ^ vsw) << 4) + 4 * (g >> 2);
+    o.vb = 32 * vrow + 4 * (g >> 2);
+    o.vx = vsw << 4;
     o.sel0 = (uint32_t)(bb | ((bb + 4) << 8));
   } else {
     o.kf = 48 * krow + 4 * ((6 * r) >> 2);
     o.kp = o.kf + 24;
     o.ksh = 16 * (r & 1);
-    o.v[0] = 48 * vrow + 4 * ((12 * g) >> 5);
+    o.vb = 48 * vrow + 4 * ((12 * g) >> 5);
     o.vsh = (12 * g) & 31;
   }
   return o;
@@ -282,7 +291,7 @@ template <int BITS>
 __device__ __forceinline__ void value_pair(const uint8_t* vc, const LaneOff& o, int sl, int rp, int c4,
                                            uint32_t (&b)[4]) {
   if constexpr (BITS == 4) {
-    const uint8_t* p = vc + o.v[c4] + 4096 * sl + 512 * rp;
+    const uint8_t* p = vc + (o.vb + ((c4 << 4) ^ o.vx)) + 4096 * sl + 512 * rp;
     const uint32_t A = ld_s32(p), B = ld_s32(p + 64);
     const uint32_t x0 = __byte_perm(A, B, o.sel0), x1 = __byte_perm(A, B, o.sel1);
     b[0] = x0 & 0x000F000Fu;
@@ -290,14 +299,14 @@ __device__ __forceinline__ void value_pair(const uint8_t* vc, const LaneOff& o, 
     b[2] = x1 & 0x000F000Fu;
     b[3] = x1 & 0x00F000F0u;
   } else if constexpr (BITS == 2) {
-    const uint8_t* p = vc + o.v[c4 >> 1] + 2048 * sl + 256 * rp + 8 * (c4 & 1);
+    const uint8_t* p = vc + (o.vb + (((c4 >> 1) << 4) ^ o.vx)) + 2048 * sl + 256 * rp + 8 * (c4 & 1);
     const uint32_t x = __byte_perm(ld_s32(p), ld_s32(p + 32), o.sel0);
     b[0] = x & 0x00030003u;
     b[1] = x & 0x000C000Cu;
     b[2] = x & 0x00300030u;
     b[3] = x & 0x00C000C0u;
   } else {
-    const uint8_t* p = vc + o.v[0] + 3072 * sl + 384 * rp + 12 * c4;
+    const uint8_t* p = vc + o.vb + 3072 * sl + 384 * rp + 12 * c4;
     const uint32_t a0 = ld_s32(p), b0 = ld_s32(p + 48);
     uint32_t a1 = 0u, b1 = 0u;
     if (o.vsh + 12 > 32) {
@@ -332,7 +341,7 @@ __device__ __forceinline__ int acc_index(int w, int c, int h) {
 //   P . V:  D[channel][head] = sum_t A(v)[channel][t] B(p*s)[t][head]
 // so the score fragment of a lane is exactly its B operand for P . V.
 template <int BITS, int G, int SL>
-__global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const DecodeArgs a, const StageLayout L,
+__global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const DecodeArgs a, const StageLayout L,
                                                              const __grid_constant__ CUtensorMap tm_k,
                                                              const __grid_constant__ CUtensorMap tm_v) {
   constexpr int HALF = kD / 2;
@@ -343,7 +352,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const DecodeArgs
   extern __shared__ uint8_t dsmem[];
   __shared__ __align__(8) uint64_t s_bar[NST];
   __shared__ int s_abort;
-  __shared__ float s_qp[G][kD];                               // q at q_pos, times sm_scale*log2(e)
+  __shared__ float s_qp[G][kD];                               // q at q_pos, times 2*sm_scale*log2(e)
+  __shared__ const void* s_src[4];                            // this stream's k_meta, v_meta, k_outl, v_outl
   __shared__ __align__(16) uint4 s_qa[2][SL][8][32];          // A quads {a0, 0, a2, 0} of 2 q_block, fp16
   __shared__ __align__(16) uint4 s_kz[2][4][4][2];            // key {s01, s23, z01, z23} / 2 [k-step][quarter][half]
   __shared__ __align__(16) float4 s_acc[kWarps][8][8][RQ];    // P.V sums in the frame m_frame, fragment order
@@ -371,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const DecodeArgs
   uint8_t* ring = dsmem + ((1024u - (smem_addr(dsmem) & 1023u)) & 1023u);
   const uint32_t ring_s = smem_addr(ring);
 
+  // (thread 0) copies of unit u into ring stage `stage`
   auto issue = [&](int u, int stage) {
     const uint32_t bar = smem_addr(&s_bar[stage]);
     const uint32_t base = ring_s + stage * L.stage_bytes;
@@ -378,11 +389,11 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const DecodeArgs
     mbar_arrive_expect_tx(bar, L.tx_bytes);
     tma_load_3d(base + L.kc, &tm_k, 0, t0, bh, bar);
     tma_load_3d(base + L.vc, &tm_v, 0, t0, bh, bar);
-    bulk_load(base + L.km, a.k_meta + ((size_t)bh * d.n_blk + u) * kD, L.km_bytes, bar);
-    bulk_load(base + L.vm, a.v_meta + ((size_t)bh * d.T_max + t0) * ng, L.vm_bytes, bar);
+    bulk_load(base + L.km, static_cast<const uint8_t*>(s_src[0]) + (size_t)u * L.km_bytes, L.km_bytes, bar);
+    bulk_load(base + L.vm, static_cast<const uint8_t*>(s_src[1]) + (size_t)u * L.vm_bytes, L.vm_bytes, bar);
     if (n_out > 0) {
-      bulk_load(base + L.ko, a.k_outl + ((size_t)bh * d.T_max + t0) * n_out, L.outl_bytes, bar);
-      bulk_load(base + L.vo, a.v_outl + ((size_t)bh * d.T_max + t0) * n_out, L.outl_bytes, bar);
+      bulk_load(base + L.ko, static_cast<const uint8_t*>(s_src[2]) + (size_t)u * L.outl_bytes, L.outl_bytes, bar);
+      bulk_load(base + L.vo, static_cast<const uint8_t*>(s_src[3]) + (size_t)u * L.outl_bytes, L.outl_bytes, bar);
     }
   };
   auto wait_unit = [&](int u) -> bool {
@@ -416,16 +427,22 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const DecodeArgs
   // rotations of pair qi: block start R(t0) from the coarse tables, slice step R(64)
   float2 r64 = make_float2(1.0f, 0.0f);
   if (a.rope && SL > 1 && q_thread) r64 = rope_fine(a.rope, d, 64, qi);
+  // R(BK u) = R_hi(u / 256) R_lo(u % 256) from the coarse tables (block index u >= 0)
+  constexpr uint32_t kLoOff = HALF * BK, kHiOff = kLoOff + kRopeLo * HALF;
   auto block_rot = [&](int u) -> float2 {
-    return (a.rope && q_thread) ? rope_block(a.rope, d, u, qi) : make_float2(1.0f, 0.0f);
+    if (!a.rope || !q_thread) return make_float2(1.0f, 0.0f);
+    const uint32_t m = (uint32_t)u;
+    const float2 lo = __ldg(a.rope + (kLoOff + ((m & (kRopeLo - 1)) << 6) + qi));
+    const float2 hi = __ldg(a.rope + (kHiOff + ((m / kRopeLo) << 6) + qi));
+    return rot_compose(hi, lo);
   };
 
   // Per-block tables shared by the warps: the queries rotated back to each
   // slice start (fp16 A quads, doubled for the halved keys) and the key
   // scale/zero (halved, fragment order).
-  auto prep = [&](int u, float2 rr) {
+  auto prep = [&](int u, int stage, float2 rr) {
     const int buf = (u - u0) & 1;
-    const uint8_t* st = ring + ((u - u0) % NST) * L.stage_bytes;
+    const uint8_t* st = ring + stage * L.stage_bytes;
     if (q_thread) {
 #pragma unroll
       for (int sl = 0; sl < SL; ++sl) {
@@ -435,8 +452,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const DecodeArgs
         for (int gg = (G > 1 ? (tid >> 6) : 0); gg < G; gg += 2) {
           const float x = s_qp[gg][qi], y = s_qp[gg][qi + HALF];
           const float x2 = fmaf(x, rs.x, y * rs.y), y2 = fmaf(y, rs.x, -x * rs.y);   // apply R(-t)
-          *reinterpret_cast<__half*>(qa + 64 * gg) = __float2half_rn(2.0f * x2);
-          *reinterpret_cast<__half*>(qa + 64 * gg + 2048) = __float2half_rn(2.0f * y2);
+          *reinterpret_cast<__half*>(qa + 64 * gg) = __float2half_rn(x2);
+          *reinterpret_cast<__half*>(qa + 64 * gg + 2048) = __float2half_rn(y2);
         }
       }
     }
@@ -455,6 +472,10 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const DecodeArgs
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     s_abort = 0;
+    s_src[0] = a.k_meta + (size_t)bh * d.n_blk * kD;
+    s_src[1] = a.v_meta + (size_t)bh * d.T_max * ng;
+    s_src[2] = a.k_outl + (size_t)bh * d.T_max * n_out;
+    s_src[3] = a.v_outl + (size_t)bh * d.T_max * n_out;
   }
   __syncthreads();
   if (tid == 0)
@@ -469,8 +490,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const DecodeArgs
       x = x2;
       y = y2;
     }
-    s_qp[gg][i] = x * a.scale_log2;
-    s_qp[gg][i + HALF] = y * a.scale_log2;
+    s_qp[gg][i] = x * (2.0f * a.scale_log2);        // doubled: the keys are halved
+    s_qp[gg][i + HALF] = y * (2.0f * a.scale_log2);
   }
   {
     uint32_t* z = reinterpret_cast<uint32_t*>(&s_qa[0][0][0][0]);
@@ -493,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const DecodeArgs
       abort_split(u0);
       return;
     }
-    prep(u0, rr0);
+    prep(u0, 0, rr0);
     if (u0 + 1 < u1) rr_next = block_rot(u0 + 1);
   }
   __syncthreads();
@@ -517,8 +538,12 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const DecodeArgs
     for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
   };
 
+  int stage = 0;
+  uint32_t phase = 0;   // ring stage of block u and the parity of its next fill
   for (int u = u0; u < u1; ++u) {
-    const int k = u - u0, stage = k % NST, buf = k & 1;
+    const int k = u - u0, buf = k & 1;
+    const int nstage = (stage + 1 == NST) ? 0 : stage + 1;
+    const uint32_t nphase = phase ^ (nstage == 0 ? 1u : 0u);
     const bool is_tail = (u == a.n_full);
     const int ntok = is_tail ? a.tail_len : BK;
     const uint8_t* st = ring + stage * L.stage_bytes;
@@ -534,11 +559,11 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const DecodeArgs
 #pragma unroll 1
     for (int sl = 0; sl < SL; ++sl) {
       float sc[2][2];
-      float acc[2][2][4];   // [n-tile][first half / partner]
+      float acc[2][KVQ_TC_QK_CHAINS][4];   // [n-tile][chain]
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) acc[nt][h][0] = acc[nt][h][1] = acc[nt][h][2] = acc[nt][h][3] = 0.0f;
+        for (int h = 0; h < KVQ_TC_QK_CHAINS; ++h) acc[nt][h][0] = acc[nt][h][1] = acc[nt][h][2] = acc[nt][h][3] = 0.0f;
       if (!is_tail) {
         KeyWords kw[2];
 #pragma unroll
@@ -563,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const DecodeArgs
             const __half2 kf1 = __hfma2(xf1, c23, __hneg2(__hmul2(xp1, s23)));
             const __half2 kp1 = __hfma2(xp1, c23, __hmul2(xf1, s23));
             mma16816(acc[nt][0], qf, as_u32(kf0), as_u32(kf1));
-            mma16816(acc[nt][1], qp, as_u32(kp0), as_u32(kp1));
+            mma16816(acc[nt][KVQ_TC_QK_CHAINS - 1], qp, as_u32(kp0), as_u32(kp1));
           }
         }
       } else {
@@ -594,14 +619,18 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const DecodeArgs
             const __half2 kf1 = __hfma2(xf1, c23, __hneg2(__hmul2(xp1, s23)));
             const __half2 kp1 = __hfma2(xp1, c23, __hmul2(xf1, s23));
             mma16816(acc[nt][0], qf, as_u32(kf0), as_u32(kf1));
-            mma16816(acc[nt][1], qp, as_u32(kp0), as_u32(kp1));
+            mma16816(acc[nt][KVQ_TC_QK_CHAINS - 1], qp, as_u32(kp0), as_u32(kp1));
           }
         }
       }
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        sc[nt][0] = acc[nt][0][0] + acc[nt][1][0];
-        sc[nt][1] = acc[nt][0][1] + acc[nt][1][1];
+        sc[nt][0] = acc[nt][0][0];
+        sc[nt][1] = acc[nt][0][1];
+        if (KVQ_TC_QK_CHAINS > 1) {
+          sc[nt][0] += acc[nt][KVQ_TC_QK_CHAINS - 1][0];
+          sc[nt][1] += acc[nt][KVQ_TC_QK_CHAINS - 1][1];
+        }
       }
       // dense-and-sparse keys: (x_out - x_dense) * <q, R(j) e_c> per outlier
       if (n_out > 0 && !is_tail) {
@@ -754,12 +783,14 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const DecodeArgs
             }
           }
           const __half2 h0 = __floats2half2_rn(A[0], A[1]), h1 = __floats2half2_rn(A[2], A[3]);
-          const __half2 l0 = __floats2half2_rn(A[0] - __low2float(h0), A[1] - __high2float(h0));
-          const __half2 l1 = __floats2half2_rn(A[2] - __low2float(h1), A[3] - __high2float(h1));
           bh0 = (g < G) ? as_u32(h0) : 0u;
           bh1 = (g < G) ? as_u32(h1) : 0u;
-          bl0 = (g < G) ? as_u32(l0) : 0u;
-          bl1 = (g < G) ? as_u32(l1) : 0u;
+          if (KVQ_TC_PV_LO) {
+            const __half2 l0 = __floats2half2_rn(A[0] - __low2float(h0), A[1] - __high2float(h0));
+            const __half2 l1 = __floats2half2_rn(A[2] - __low2float(h1), A[3] - __high2float(h1));
+            bl0 = (g < G) ? as_u32(l0) : 0u;
+            bl1 = (g < G) ? as_u32(l1) : 0u;
+          }
           zacc[c4] += zs;
         } else {
           zacc[c4] = zacc[c4 - 1];   // same value group: the two sums stay equal
@@ -771,7 +802,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const DecodeArgs
         for (int mi = 0; mi < 2; ++mi) {
           const uint4 av = make_uint4(x0[2 * mi], x0[2 * mi + 1], x1[2 * mi], x1[2 * mi + 1]);
           mma16816(o[2 * c4 + mi], av, bh0, bh1);
-          mma16816(o[2 * c4 + mi], av, bl0, bl1);
+          if (KVQ_TC_PV_LO) mma16816(o[2 * c4 + mi], av, bl0, bl1);
         }
       }
     }
@@ -788,8 +819,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const DecodeArgs
 
     // ---- next block's tables; release this stage for the refill
     if (u + 1 < u1) {
-      if (!wait_unit(u + 1)) s_abort = 1;
-      prep(u + 1, rr_next);
+      if (!mbar_wait(smem_addr(&s_bar[nstage]), nphase)) s_abort = 1;
+      prep(u + 1, nstage, rr_next);
       if (u + 2 < u1) rr_next = block_rot(u + 2);
     }
     __syncthreads();
@@ -798,6 +829,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_tc_kernel(const DecodeArgs
       return;
     }
     if (tid == 0 && u + NST < u1) issue(u + NST, stage);
+    stage = nstage;
+    phase = nphase;
   }
 
   // ---- merge the warps
