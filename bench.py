@@ -37,7 +37,14 @@ import numpy as np  # noqa: E402
 import kvq_inputs as ki  # noqa: E402
 
 L2_BYTES = 129 * 2 ** 20
-DECODE_SOURCES = ["kvq_decode.cuh", "kvq_decode.cu", "kvq_decode_inst.cuh", "kvq_common.cuh"]
+# Sources of the decode kernels: a roofline.traffic figure read from profiles/
+# counts only if it was captured on these exact files.
+DECODE_SOURCES = {
+    128: ["kvq_decode_tc.cuh", "kvq_tc_geom.cuh", "kvq_decode_tc_inst.cuh", "kvq_decode_tc_b4.cu",
+          "kvq_decode_tc_b3.cu", "kvq_decode_tc_b2.cu", "kvq_decode.cuh", "kvq_decode.cu", "kvq_common.cuh"],
+    64: ["kvq_decode.cuh", "kvq_decode.cu", "kvq_decode_inst.cuh", "kvq_common.cuh"],
+}
+DECODE_KERNEL = {128: "decode_tc_kernel", 64: "decode_partial_kernel"}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -186,6 +193,23 @@ def host_cpu():
     return model
 
 
+def max_over_ranks(values, device):
+    """Element-wise max of a list of floats over all ranks (identity at world 1).
+    Replicas run independently; the job's time is its slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def replica_throughput(units_per_rank, world, ms):
+    """Whole-job units/s of `world` independent replicas that each processed
+    units_per_rank units in (at most) ms milliseconds."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 # ----------------------------------------------------------------------------- CPU oracle timing
 def oracle_step_seconds(w, n_streams, n_tok, reps=1):
     """Wall time of the oracle doing one decode step on n_streams streams of
@@ -207,6 +231,31 @@ def oracle_step_seconds(w, n_streams, n_tok, reps=1):
         oc.attention(Kh, Vh, qs, n_tok, w.rope_theta, 1.0 / math.sqrt(w.D), 0.0, threads)
         times.append(time.perf_counter() - t0)
     return statistics.median(times), threads
+
+
+def cpu_baseline_prefill(w, budget_s=15.0):
+    """Oracle encode (the quantizer) on a bounded sample of the prefill:
+    one stream per host thread, a slice of the new tokens, extrapolated."""
+    from oracle import oracle_cpp as oc
+    threads = oc.default_threads()
+    n_streams = min(threads, w.B * w.H_kv)
+    streams = [(s // w.H_kv % w.B, s % w.H_kv) for s in range(n_streams)]
+    n_tok = min(w.T, 4096)
+    K, V = ki.streams_np(w, streams, n_tok)
+    t0 = time.perf_counter()
+    oc.encode(K, V, w.bits, w.key_block, w.value_group, n_out_of(w), threads)
+    t = time.perf_counter() - t0
+    if t < budget_s / 4 and n_tok < w.T:
+        n_tok = min(w.T, int(n_tok * budget_s / 2 / max(t, 1e-3)) // w.key_block * w.key_block)
+        K, V = ki.streams_np(w, streams, n_tok)
+        t0 = time.perf_counter()
+        oc.encode(K, V, w.bits, w.key_block, w.value_group, n_out_of(w), threads)
+        t = time.perf_counter() - t0
+    return {
+        "value": n_streams * n_tok / t, "unit": "kv-tokens/s", "cores": threads, "kind": "oracle",
+        "sample": (f"{n_streams} of {w.B * w.H_kv} (b,h_kv) streams x {n_tok} of {w.T} new tokens, "
+                   f"oracle encode (outliers, scales, codes, packing), {t:.2f} s wall; host {host_cpu()}"),
+    }
 
 
 def cpu_baseline(w, budget_s=15.0):
@@ -319,24 +368,22 @@ def run_decode(args, w, rank, world, device):
     torch.cuda.synchronize()
     e2e_ms = e_start.elapsed_time(e_end)
 
-    times = torch.tensor([ms, e2e_ms, statistics.mean(dec_ms)], dtype=torch.float64, device=device)
-    if world > 1:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    ms, e2e_ms, dec_mean = (float(x) for x in times.cpu())
+    ms, e2e_ms, dec_mean = max_over_ranks([ms, e2e_ms, statistics.mean(dec_ms)], device)
     bytes_step_in = (k1.numel() + v1.numel() + q.numel()) * 2
     bytes_step_out = out.numel() * 2
     alg = decode_alg_bytes(w, T + 1)
     peak, peak_kind = measured_peaks()
     achieved = alg / (dec_mean * 1e-3) / 1e9
-    sha = source_sha(DECODE_SOURCES)
+    sha = source_sha(DECODE_SOURCES[w.D])
+    kname = DECODE_KERNEL[w.D]
     line = {
         "metric": "decode-attn tokens/s (one layer; B query tokens per step)",
-        "value": world * w.B * args.steps / (ms * 1e-3),
+        "value": replica_throughput(w.B * args.steps, world, ms),
         "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic",
+        "dtype": f"u{w.bits}/f16/f32", "data": "synthetic",
         "config": {
             "workload": (f"{w.name}: B={w.B} H_q={w.H_q} H_kv={w.H_kv} D={w.D} T={T} INT{w.bits} "
                          f"key_block={w.key_block} value_group={w.value_group} outliers={w.outlier_frac} "
@@ -344,18 +391,18 @@ def run_decode(args, w, rank, world, device):
             "step": "kvq_append of 1 token per stream + kvq_decode_attn over T+1 tokens",
             "l2": f"inputs larger than L2 (cache {caches[0].layout.cache_bytes / 1e9:.2f} GB per layer > 129 MB); no flush",
             "parallelism": f"replicas x{world}",
-            "kv_tokens_per_s": world * w.B * (T + 1) * args.steps / (ms * 1e-3),
-            "model_level_tokens_per_s_32_layers": world * w.B * args.steps / (ms * 1e-3) / 32,
+            "kv_tokens_per_s": replica_throughput(w.B * (T + 1) * args.steps, world, ms),
+            "model_level_tokens_per_s_32_layers": replica_throughput(w.B * args.steps, world, ms) / 32,
             "decode_call_ms": dec_mean,
         },
-        "e2e": {"value": world * w.B * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": replica_throughput(w.B * args.steps, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": bytes_step_in, "d2h_bytes_per_step": bytes_step_out},
         "gpu_launches": 3 * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
-                     "kernel": "decode_partial_kernel (+ combine, timed together per call)",
+                     "kernel": f"{kname} (+ decode_combine_kernel: one kvq_decode_attn call timed per step)",
                      "alg_bytes_per_launch": alg,
-                     "traffic": profile_traffic(f"decode_partial_{w.name}.txt", sha),
+                     "traffic": profile_traffic(f"{kname}_{w.name}.txt", sha),
                      "source_sha": sha},
         "clocks": clk,
     }
@@ -407,6 +454,7 @@ def run_prefill(args, w, rank, world, device):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
+    ms, e2e_ms, call_ms = max_over_ranks([ms, e2e_ms, call_ms], device)
     alg = append_alg_bytes(w, n_new)
     peak, peak_kind = measured_peaks()
     achieved = alg / (call_ms * 1e-3) / 1e9
@@ -414,14 +462,15 @@ def run_prefill(args, w, rank, world, device):
     toks = w.B * w.H_kv * n_new
     return {
         "metric": "append (prefill quantize) kv-tokens/s",
-        "value": world * toks * args.steps / (ms * 1e-3), "unit": "kv-tokens/s",
+        "value": replica_throughput(toks * args.steps, world, ms), "unit": "kv-tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": f"f16/f32->u{w.bits}",
+        "data": "synthetic",
         "config": {"workload": f"{w.name} prefill: B={w.B} H_kv={w.H_kv} D={w.D} n_new={n_new} INT{w.bits} "
                                f"key_block={w.key_block} value_group={w.value_group} outliers={w.outlier_frac}",
                    "l2": f"inputs larger than L2 ({2 * toks * w.D * 2 / 1e9:.2f} GB fp16 in); no flush",
                    "parallelism": f"replicas x{world}"},
-        "e2e": {"value": world * toks * args.steps / (e2e_ms * 1e-3), "unit": "kv-tokens/s",
+        "e2e": {"value": replica_throughput(toks * args.steps, world, e2e_ms), "unit": "kv-tokens/s",
                 "h2d_bytes_per_step": 2 * toks * w.D * 2, "d2h_bytes_per_step": 0},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -500,8 +549,7 @@ def main():
         dist.destroy_process_group()
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            if args.mode == "decode":
-                line["cpu_baseline"] = cpu_baseline(w)
+            line["cpu_baseline"] = cpu_baseline(w) if args.mode == "decode" else cpu_baseline_prefill(w)
         print(json.dumps(line), flush=True)
 
 
