@@ -5,9 +5,23 @@
 //   KVQuant "Per-Channel Key Quantization"             -> step C, keys;
 //   Quanto steps 1-2 (block scale and zero_point)       -> step C, values;
 //   codes and LSB-first packing                         -> step D.
-// One CTA per (key block touched by the append, (b, h_kv) stream). The CTA
-// stages the block's new value rows, and the block's keys when the append
-// completes it, in shared memory, then runs the steps in the method's order.
+// Grid: (key block touched by the append, (b, h_kv) stream, {values, keys}).
+// A value CTA quantizes the block's new value rows; a key CTA quantizes the
+// block's keys when the append completes it (keys read so far come back from
+// K_TAIL) and otherwise copies the new keys into K_TAIL. Rows are staged in
+// shared memory; then, in the method's order:
+//   B. outliers: the n_out largest |x| of every row (two threads per row for
+//      n_out = 1, a warp per row otherwise); their staged copies become NaN,
+//      which the fp16 min/max of step C skip;
+//   C. scale and zero: values per (row, group) by one thread, keys per
+//      channel by four or eight threads over row slices;
+//   D. codes: 32 channels of a row per thread, two at a time in packed fp32
+//      (x - z, times 1/s, rounded by the 1.5 * 2^23 addition), packed and
+//      stored with one or three vector stores. The product with 1/s is within
+//      3e-6 of the binary32 quotient for codes below 16, so a chunk whose
+//      values all sit further than 1e-5 from a rounding tie gets the codes
+//      of the exact division; a chunk with a near tie is recomputed with it.
+//      Outlier positions are recomputed from their stored value.
 // All rounding follows the library's stated arithmetic: binary32 RN subtract
 // and divide, fp16 round-up for the scale, round-half-even codes.
 #include "kvq_common.cuh"
@@ -16,7 +30,9 @@ namespace kvq {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kMaxGroups = 4;  // D / Gv <= 128 / 32
+constexpr int kMaxGroups = 4;       // D / Gv <= 128 / 32
+constexpr float kTieGuard = 1e-5f;  // |t| above 0.5 - guard: recompute the chunk exactly
+constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23: x + kMagic rounds x to an integer (ties even)
 
 struct AppendArgs {
   Dims d;
@@ -59,15 +75,48 @@ __device__ __forceinline__ uint32_t group_params(float mn, float mx, bool any, f
   return (uint32_t)hbits(sh) | ((uint32_t)hbits(zh) << 16);
 }
 
+// Code-carrying bit patterns (float bits of y + kMagic) -> packed LSB-first words.
 template <int BITS>
-__device__ __forceinline__ void pack32(const uint32_t (&q)[32], uint32_t (&w)[BITS]) {
+__device__ __forceinline__ void pack_bits(const uint32_t (&mb)[32], uint32_t (&w)[BITS]) {
+  constexpr uint32_t M = (1u << BITS) - 1u;
+  if constexpr (BITS == 4) {
 #pragma unroll
-  for (int k = 0; k < BITS; ++k) w[k] = 0u;
+    for (int k = 0; k < 4; ++k) {
+      uint32_t byte[4];
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    const int bit = e * BITS;
-    w[bit >> 5] |= q[e] << (bit & 31);
-    if ((bit & 31) + BITS > 32) w[(bit >> 5) + 1] |= q[e] >> (32 - (bit & 31));
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = mb[8 * k + 2 * j], hi = mb[8 * k + 2 * j + 1];
+        byte[j] = (lo & 0xFu) | ((hi & 0xFu) << 4);
+      }
+      w[k] = __byte_perm(__byte_perm(byte[0], byte[1], 0x0040u), __byte_perm(byte[2], byte[3], 0x0040u), 0x5410u);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < BITS; ++k) w[k] = 0u;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int bit = e * BITS;
+      const uint32_t q = mb[e] & M;
+      w[bit >> 5] |= q << (bit & 31);
+      if ((bit & 31) + BITS > 32) w[(bit >> 5) + 1] |= q >> (32 - (bit & 31));
+    }
+  }
+}
+
+// Replace code e of a packed 32-code chunk.
+template <int BITS>
+__device__ __forceinline__ void set_code(uint32_t (&w)[BITS], int e, uint32_t q) {
+  constexpr uint32_t M = (1u << BITS) - 1u;
+  const int bit = e * BITS, wi = bit >> 5, sh = bit & 31;
+#pragma unroll
+  for (int k = 0; k < BITS; ++k) {
+    if (k == wi) {
+      w[k] = (w[k] & ~(M << sh)) | (q << sh);
+      if (sh + BITS > 32 && k + 1 < BITS) {
+        const int hi = sh + BITS - 32;
+        w[k + 1] = (w[k + 1] & ~((1u << hi) - 1u)) | (q >> (32 - sh));
+      }
+    }
   }
 }
 
@@ -76,7 +125,9 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const Dims d = a.d;
   const int D = d.D, Bk = d.Bk, n_out = d.n_out;
+  const int tid = threadIdx.x;
   const int bh = blockIdx.y;
+  const bool isK = blockIdx.z != 0;
   const int blk = a.first_blk + blockIdx.x;
   const int t_blk0 = blk * Bk;
   const int t_end = a.T_cur + a.n_new;
@@ -85,62 +136,98 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   const int nv = t_hi - t_lo;                      // new tokens in this block, >= 1
   const bool complete = t_blk0 + Bk <= t_end;
   const float Lf = (float)((1 << BITS) - 1);
+  const int vpr = D / 8;                           // 16-byte vectors per row
+  __half* tail = a.k_tail + (size_t)bh * Bk * D;
 
-  __half* sV = reinterpret_cast<__half*>(smem);                       // [Bk][D]
-  __half* sK = sV + Bk * D;                                            // [Bk][D]
-  uint16_t* sVo = reinterpret_cast<uint16_t*>(sK + Bk * D);           // [Bk][MAX_OUT]
-  uint16_t* sKo = sVo + Bk * KVQ_MAX_OUTLIERS;                         // [Bk][MAX_OUT]
-  float2* sVsz = reinterpret_cast<float2*>(sKo + Bk * KVQ_MAX_OUTLIERS);  // [Bk][4]
-  float2* sKsz = sVsz + Bk * kMaxGroups;                               // [D]
+  if (isK && !complete) {
+    // unfinished block: keep the new keys as fp16 rows t % Bk of the tail
+    if (a.tail_in_kernel) {
+      for (int i = tid; i < nv * vpr; i += kThreads) {
+        const int r = i / vpr, c = i % vpr;
+        const int t = t_lo + r;
+        reinterpret_cast<uint4*>(tail + (size_t)(t - t_blk0) * D)[c] = __ldg(
+            reinterpret_cast<const uint4*>(a.k_new + ((size_t)bh * a.n_new + (t - a.T_cur)) * D) + c);
+      }
+    }
+    return;
+  }
+  const int rows = isK ? Bk : nv;
+  const int t_row0 = isK ? t_blk0 : t_lo;          // token of staged row 0
+
+  __half* sX = reinterpret_cast<__half*>(smem);                              // [rows][D]
+  uint32_t* sO = reinterpret_cast<uint32_t*>(sX + Bk * D);                   // [rows][KVQ_MAX_OUTLIERS]
+  float4* sP = reinterpret_cast<float4*>(sO + Bk * KVQ_MAX_OUTLIERS);        // values: [rows][4] {-z, 1/s, s}
+                                                                             // keys: [D/2] {-z0, -z1, r0, r1}
+  float* sS = reinterpret_cast<float*>(sP + Bk * kMaxGroups);                // keys: s per channel [D]
+  __half2* sRed = reinterpret_cast<__half2*>(sS + D);                        // keys: [8][D/2] {min, max}
 
   // ---- A. stage rows in shared memory (16-byte vectors)
-  const int vpr = D / 8;
-  const __half* v_src = a.v_new + ((size_t)bh * a.n_new + (t_lo - a.T_cur)) * D;
-  for (int i = threadIdx.x; i < nv * vpr; i += kThreads) {
+  for (int i = tid; i < rows * vpr; i += kThreads) {
     const int r = i / vpr, c = i % vpr;
-    reinterpret_cast<uint4*>(sV + r * D)[c] =
-        __ldg(reinterpret_cast<const uint4*>(v_src + (size_t)r * D) + c);
-  }
-  __half* tail = a.k_tail + (size_t)bh * Bk * D;
-  if (complete) {
-    for (int i = threadIdx.x; i < Bk * vpr; i += kThreads) {
-      const int j = i / vpr, c = i % vpr;
-      const int t = t_blk0 + j;
-      const __half* src = (t < a.T_cur) ? tail + (size_t)j * D
-                                        : a.k_new + ((size_t)bh * a.n_new + (t - a.T_cur)) * D;
-      reinterpret_cast<uint4*>(sK + j * D)[c] = reinterpret_cast<const uint4*>(src)[c];
-    }
-  } else if (a.tail_in_kernel) {
-    // unfinished block: keep the new keys as fp16 rows t % Bk of the tail
-    for (int i = threadIdx.x; i < nv * vpr; i += kThreads) {
-      const int r = i / vpr, c = i % vpr;
-      const int t = t_lo + r;
-      reinterpret_cast<uint4*>(tail + (size_t)(t - t_blk0) * D)[c] = __ldg(
-          reinterpret_cast<const uint4*>(a.k_new + ((size_t)bh * a.n_new + (t - a.T_cur)) * D) + c);
-    }
+    const int t = t_row0 + r;
+    const __half* src = isK ? ((t < a.T_cur) ? tail + (size_t)r * D
+                                             : a.k_new + ((size_t)bh * a.n_new + (t - a.T_cur)) * D)
+                            : a.v_new + ((size_t)bh * a.n_new + (t - a.T_cur)) * D;
+    reinterpret_cast<uint4*>(sX + r * D)[c] = __ldg(reinterpret_cast<const uint4*>(src) + c);
   }
   __syncthreads();
 
-  // ---- B. dense-and-sparse split: per vector, the n_out largest |x|
-  if (n_out > 0) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // ---- B. dense-and-sparse split: per row, the n_out largest |x|
+  uint32_t* gout_base = (isK ? a.k_outl : a.v_outl) + ((size_t)bh * d.T_max + t_row0) * n_out;
+  if (n_out == 1 && D == 128) {
+    // two threads per row, 64 channels each: the largest |x| (fp16 max), then
+    // its lowest channel
+    const int row = tid >> 1, half = tid & 1;
+    const bool active = row < rows;                // both threads of a row agree
+    uint32_t c_best = 0xFFFFu, m = 0u;
+    uint32_t ab[32];
+    if (active) {
+      const uint4* src = reinterpret_cast<const uint4*>(sX + row * D + 64 * half);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint4 v = src[k];
+        ab[4 * k] = v.x & 0x7FFF7FFFu;
+        ab[4 * k + 1] = v.y & 0x7FFF7FFFu;
+        ab[4 * k + 2] = v.z & 0x7FFF7FFFu;
+        ab[4 * k + 3] = v.w & 0x7FFF7FFFu;
+      }
+      __half2 m2 = *reinterpret_cast<__half2*>(&ab[0]);
+#pragma unroll
+      for (int k = 1; k < 32; ++k) m2 = __hmax2(m2, *reinterpret_cast<__half2*>(&ab[k]));
+      const uint32_t mu = *reinterpret_cast<uint32_t*>(&m2);
+      m = max(mu & 0xFFFFu, mu >> 16);
+    }
+    m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    if (active) {
+      const uint32_t mm = m | (m << 16);
+#pragma unroll
+      for (int k = 31; k >= 0; --k) {
+        const uint32_t eq = __vcmpeq2(ab[k], mm);
+        if (eq) c_best = 64 * half + 2 * k + ((eq & 0xFFFFu) ? 0 : 1);
+      }
+    }
+    const uint32_t other = __shfl_xor_sync(0xffffffffu, c_best, 1);
+    if (row < rows && half == 0) {
+      const uint32_t c = (c_best != 0xFFFFu) ? c_best : other;
+      const uint32_t e = c | ((uint32_t)hbits(sX[row * D + c]) << 16);
+      sO[row * KVQ_MAX_OUTLIERS] = e;
+      gout_base[row] = e;
+      sX[row * D + c] = __ushort_as_half((uint16_t)0x7E00u);   // NaN: skipped by step C
+    }
+  } else if (n_out > 0) {
+    // a warp per row: keys |x| bits (15) above (255 - channel); the max is the
+    // largest |x|, lowest channel on ties; keys of distinct channels differ
+    const int warp = tid >> 5, lane = tid & 31;
     const int E = D >> 5;                          // elements per lane (2 or 4)
-    const int nrows = nv + (complete ? Bk : 0);
-    for (int r = warp; r < nrows; r += kThreads / 32) {
-      const bool isV = r < nv;
-      const int row = isV ? r : r - nv;
-      const __half* x = (isV ? sV : sK) + row * D;
-      uint16_t* so = (isV ? sVo : sKo) + row * KVQ_MAX_OUTLIERS;
-      const int t = isV ? t_lo + row : t_blk0 + row;
-      uint32_t* gout = (isV ? a.v_outl : a.k_outl) + ((size_t)bh * d.T_max + t) * n_out;
-      // key = |x| bits (15) above (255 - channel): the max is the largest |x|,
-      // lowest channel on ties; keys of distinct channels never coincide
+    for (int r = warp; r < rows; r += kThreads / 32) {
+      const __half* x = sX + r * D;
       uint32_t key[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int c = lane * E + e;
         key[e] = (e < E) ? (((uint32_t)(hbits(x[c]) & 0x7FFF) << 8) | (uint32_t)(255 - c)) : 0u;
       }
+      uint32_t pick[KVQ_MAX_OUTLIERS];
       for (int k = 0; k < n_out; ++k) {
         uint32_t best = 0;
 #pragma unroll
@@ -148,95 +235,170 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
         best = __reduce_max_sync(0xffffffffu, best);
 #pragma unroll
         for (int e = 0; e < 4; ++e) key[e] = (key[e] == best) ? 0u : key[e];
-        if (lane == 0) {
-          const int c = 255 - (int)(best & 0xFF);
-          so[k] = (uint16_t)c;
-          gout[k] = (uint32_t)c | ((uint32_t)hbits(x[c]) << 16);
-        }
+        pick[k] = 255u - (best & 0xFFu);
       }
+      __syncwarp();
+      if (lane == 0) {
+        for (int k = 0; k < n_out; ++k) {
+          const uint32_t c = pick[k];
+          const uint32_t e = c | ((uint32_t)hbits(x[c]) << 16);
+          sO[r * KVQ_MAX_OUTLIERS + k] = e;
+          gout_base[(size_t)r * n_out + k] = e;
+        }
+        for (int k = 0; k < n_out; ++k) sX[r * D + pick[k]] = __ushort_as_half((uint16_t)0x7E00u);
+      }
+      __syncwarp();
     }
   }
   __syncthreads();
 
-  // ---- C. statistics: values per (token, group), keys per channel over the block
-  {
+  // ---- C. scale and zero (fp16 min/max skip the NaN-marked outliers)
+  if (!isK) {
     const int Gv = d.Gv, ng = d.ng;
-    const int nVi = nv * ng;
-    const int nKi = complete ? D : 0;
-    for (int it = threadIdx.x; it < nVi + nKi; it += kThreads) {
-      float mn = INFINITY, mx = -INFINITY;
-      bool any = false;
-      if (it < nVi) {
-        const int r = it / ng, g = it % ng;
-        const __half* x = sV + r * D + g * Gv;
-        const uint16_t* so = sVo + r * KVQ_MAX_OUTLIERS;
-        for (int k = 0; k < Gv; ++k) {
-          const int cc = (k + threadIdx.x) & (Gv - 1);   // staggered start spreads banks
-          const int c = g * Gv + cc;
-          bool ex = false;
-          for (int o = 0; o < n_out; ++o) ex |= (so[o] == c);
-          if (!ex) {
-            const float v = __half2float(x[cc]);
-            mn = fminf(mn, v);
-            mx = fmaxf(mx, v);
-            any = true;
-          }
-        }
-        float2 sz;
-        const uint32_t packed = group_params(mn, mx, any, Lf, &sz);
-        a.v_meta[((size_t)bh * d.T_max + (t_lo + r)) * ng + g] = packed;
-        sVsz[r * kMaxGroups + g] = sz;
-      } else {
-        const int c = it - nVi;
-        for (int j = 0; j < Bk; ++j) {
-          const uint16_t* so = sKo + j * KVQ_MAX_OUTLIERS;
-          bool ex = false;
-          for (int o = 0; o < n_out; ++o) ex |= (so[o] == c);
-          if (!ex) {
-            const float v = __half2float(sK[j * D + c]);
-            mn = fminf(mn, v);
-            mx = fmaxf(mx, v);
-            any = true;
-          }
-        }
-        float2 sz;
-        const uint32_t packed = group_params(mn, mx, any, Lf, &sz);
-        a.k_meta[((size_t)bh * d.n_blk + blk) * D + c] = packed;
-        sKsz[c] = sz;
+    for (int it = tid; it < rows * ng; it += kThreads) {
+      const int r = it / ng, g = it % ng;
+      const uint4* x = reinterpret_cast<const uint4*>(sX + r * D + g * Gv);
+      __half2 mn2, mx2;
+      {
+        const uint4 v = x[0];
+        mn2 = __hmin2(__hmin2(*reinterpret_cast<const __half2*>(&v.x), *reinterpret_cast<const __half2*>(&v.y)),
+                      __hmin2(*reinterpret_cast<const __half2*>(&v.z), *reinterpret_cast<const __half2*>(&v.w)));
+        mx2 = __hmax2(__hmax2(*reinterpret_cast<const __half2*>(&v.x), *reinterpret_cast<const __half2*>(&v.y)),
+                      __hmax2(*reinterpret_cast<const __half2*>(&v.z), *reinterpret_cast<const __half2*>(&v.w)));
       }
+      for (int k = 1; k < Gv / 8; ++k) {
+        const uint4 v = x[k];
+        mn2 = __hmin2(mn2, __hmin2(__hmin2(*reinterpret_cast<const __half2*>(&v.x), *reinterpret_cast<const __half2*>(&v.y)),
+                                   __hmin2(*reinterpret_cast<const __half2*>(&v.z), *reinterpret_cast<const __half2*>(&v.w))));
+        mx2 = __hmax2(mx2, __hmax2(__hmax2(*reinterpret_cast<const __half2*>(&v.x), *reinterpret_cast<const __half2*>(&v.y)),
+                                   __hmax2(*reinterpret_cast<const __half2*>(&v.z), *reinterpret_cast<const __half2*>(&v.w))));
+      }
+      const float mn = fminf(__low2float(mn2), __high2float(mn2));
+      const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
+      const bool any = !isnan(mn);
+      float2 sz;
+      const uint32_t packed = group_params(mn, mx, any, Lf, &sz);
+      a.v_meta[((size_t)bh * d.T_max + (t_row0 + r)) * ng + g] = packed;
+      sP[r * kMaxGroups + g] = make_float4(-sz.y, sz.x > 0.0f ? __frcp_rn(sz.x) : 0.0f, sz.x, 0.0f);
+    }
+  } else {
+    // channel pairs p < D/2, row slices q < S: partial fp16 min/max, then combined
+    const int P = D / 2, S = kThreads / P;
+    const int p = tid % P, q = tid / P;
+    const __half nanh = __ushort_as_half((uint16_t)0x7E00u);  // NaN: the identity of min/max here
+    __half2 mn2 = __halves2half2(nanh, nanh), mx2 = mn2;
+    for (int j = q; j < Bk; j += S) {
+      const __half2 v = reinterpret_cast<const __half2*>(sX + j * D)[p];
+      mn2 = __hmin2(mn2, v);
+      mx2 = __hmax2(mx2, v);
+    }
+    sRed[(2 * q) * P + p] = mn2;
+    sRed[(2 * q + 1) * P + p] = mx2;
+    __syncthreads();
+    if (tid < D) {
+      const int c = tid, pc = c >> 1, hc = c & 1;
+      float mn = NAN, mx = NAN;
+      for (int qq = 0; qq < S; ++qq) {
+        const __half2 a2 = sRed[(2 * qq) * P + pc], b2 = sRed[(2 * qq + 1) * P + pc];
+        mn = fminf(mn, hc ? __high2float(a2) : __low2float(a2));
+        mx = fmaxf(mx, hc ? __high2float(b2) : __low2float(b2));
+      }
+      const bool any = !isnan(mn);
+      float2 sz;
+      const uint32_t packed = group_params(mn, mx, any, Lf, &sz);
+      a.k_meta[((size_t)bh * d.n_blk + blk) * D + c] = packed;
+      float* pk = reinterpret_cast<float*>(&sP[pc]);
+      pk[hc] = -sz.y;
+      pk[2 + hc] = sz.x > 0.0f ? __frcp_rn(sz.x) : 0.0f;
+      sS[c] = sz.x;
     }
   }
   __syncthreads();
 
-  // ---- D. codes for every element (outlier positions included), packed
+  // ---- D. codes for every element (outlier positions recomputed), packed
   {
     const int nch = D / 32;
-    const int nVc = nv * nch;
-    const int nKc = complete ? Bk * nch : 0;
-    for (int it = threadIdx.x; it < nVc + nKc; it += kThreads) {
-      const bool isV = it < nVc;
-      const int k = isV ? it : it - nVc;
-      const int r = k / nch, ch = k % nch;
-      const __half* x = (isV ? sV : sK) + r * D + ch * 32;
-      uint32_t q[32];
-      if (isV) {
-        const float2 sz = sVsz[r * kMaxGroups + (ch * 32) / d.Gv];
+    uint8_t* base = isK ? a.k_codes : a.v_codes;
+    const float2 magic2 = make_float2(kMagic, kMagic), nmagic2 = make_float2(-kMagic, -kMagic);
+    const float2 neg1 = make_float2(-1.0f, -1.0f);
+    for (int it = tid; it < rows * nch; it += kThreads) {
+      const int r = it / nch, ch = it % nch;
+      const uint4* xs = reinterpret_cast<const uint4*>(sX + r * D + ch * 32);
+      float4 vp = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (!isK) vp = sP[r * kMaxGroups + (ch * 32) / d.Gv];
+      uint32_t mb[32];
+      float tmax = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) q[e] = quant_code(__half2float(x[e]), sz.y, sz.x, Lf);
-      } else {
+      for (int k = 0; k < 4; ++k) {
+        const uint4 v = xs[k];
+        const uint32_t hw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float2 sz = sKsz[ch * 32 + e];
-          q[e] = quant_code(__half2float(x[e]), sz.y, sz.x, Lf);
+        for (int j = 0; j < 4; ++j) {
+          const int e = 8 * k + 2 * j;
+          const float2 x2 = __half22float2(*reinterpret_cast<const __half2*>(&hw[j]));
+          float2 nz2, r2;
+          if (isK) {
+            const float4 kp = sP[(ch * 32 + e) >> 1];
+            nz2 = make_float2(kp.x, kp.y);
+            r2 = make_float2(kp.z, kp.w);
+          } else {
+            nz2 = make_float2(vp.x, vp.x);
+            r2 = make_float2(vp.y, vp.y);
+          }
+          const float2 y2 = __fmul2_rn(__fadd2_rn(x2, nz2), r2);
+          const float2 m2 = __fadd2_rn(y2, magic2);
+          const float2 t2 = __ffma2_rn(__fadd2_rn(m2, nmagic2), neg1, y2);   // y - rint(y)
+          tmax = fmaxf(tmax, fmaxf(fabsf(t2.x), fabsf(t2.y)));
+          mb[e] = __float_as_uint(m2.x);
+          mb[e + 1] = __float_as_uint(m2.y);
         }
       }
       uint32_t w[BITS];
-      pack32<BITS>(q, w);
-      const int t = isV ? t_lo + r : t_blk0 + r;
-      uint8_t* base = isV ? a.v_codes : a.k_codes;
+      pack_bits<BITS>(mb, w);
+      const int t = t_row0 + r;
+      if (tmax > 0.5f - kTieGuard) {
+        // a value close to a rounding tie: the chunk with the exact division
+        const __half* xh = sX + r * D + ch * 32;
+#pragma unroll 1
+        for (int e = 0; e < 32; ++e) {
+          const int c = ch * 32 + e;
+          const float x = __half2float(xh[e]);
+          if (isnan(x)) continue;   // outlier position: recomputed below
+          float z, s;
+          if (isK) {
+            z = -reinterpret_cast<const float*>(&sP[c >> 1])[c & 1];
+            s = sS[c];
+          } else {
+            z = -vp.x;
+            s = vp.z;
+          }
+          set_code<BITS>(w, e, quant_code(x, z, s, Lf));
+        }
+      }
+      for (int o = 0; o < n_out; ++o) {
+        const uint32_t ev = sO[r * KVQ_MAX_OUTLIERS + o];
+        const int c = (int)(ev & 0xFFFFu);
+        if ((c >> 5) == ch) {
+          float z, s;
+          if (isK) {
+            z = -reinterpret_cast<const float*>(&sP[c >> 1])[c & 1];
+            s = sS[c];
+          } else {
+            z = -vp.x;
+            s = vp.z;
+          }
+          set_code<BITS>(w, c & 31, quant_code(__half2float(__ushort_as_half((uint16_t)(ev >> 16))), z, s, Lf));
+        }
+      }
       uint32_t* dst = reinterpret_cast<uint32_t*>(base + ((size_t)bh * d.T_max + t) * d.cb) + ch * BITS;
+      if constexpr (BITS == 4) {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+      } else if constexpr (BITS == 2) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+      } else {
 #pragma unroll
-      for (int b = 0; b < BITS; ++b) dst[b] = w[b];
+        for (int b = 0; b < BITS; ++b) dst[b] = w[b];
+      }
     }
   }
 }
@@ -257,8 +419,9 @@ __global__ void tail_copy_kernel(__half* __restrict__ k_tail, const __half* __re
 }
 
 size_t append_smem(const Dims& d) {
-  return (size_t)2 * d.Bk * d.D * sizeof(__half) + (size_t)2 * d.Bk * KVQ_MAX_OUTLIERS * sizeof(uint16_t) +
-         (size_t)d.Bk * kMaxGroups * sizeof(float2) + (size_t)d.D * sizeof(float2);
+  return (size_t)d.Bk * d.D * sizeof(__half) + (size_t)d.Bk * KVQ_MAX_OUTLIERS * sizeof(uint32_t) +
+         (size_t)d.Bk * kMaxGroups * sizeof(float4) + (size_t)d.D * sizeof(float) +
+         (size_t)16 * (d.D / 2) * sizeof(__half2);
 }
 
 template <int BITS>
@@ -300,7 +463,7 @@ cudaError_t launch_append(const Dims& d, const kvq_cache& c, const __half* k_new
   a.first_blk = first;
   a.tail_in_kernel = defer_tail ? 0 : 1;
 
-  const dim3 grid(last - first + 1, d.B * d.H_kv);
+  const dim3 grid(last - first + 1, d.B * d.H_kv, 2);
   const size_t smem = append_smem(d);
   cudaError_t e;
   switch (d.bits) {
