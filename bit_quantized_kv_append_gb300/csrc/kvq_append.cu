@@ -120,6 +120,86 @@ __device__ __forceinline__ void set_code(uint32_t (&w)[BITS], int e, uint32_t q)
   }
 }
 
+// Staged rows are stored with their 16-byte chunks XOR-swizzled by the row
+// (chunk c of row r at c ^ (r & 7)), so the row-parallel passes below read
+// eight different bank groups per quarter warp.
+__device__ __forceinline__ int sw_off(int r, int D, int col) {
+  return r * D + ((((col >> 3) ^ (r & 7))) << 3) + (col & 7);
+}
+
+// Step D for one 32-channel chunk of row r: codes from the packed fp32 path,
+// exact division where a value sits near a rounding tie, outlier positions
+// from their stored value; returns the packed words.
+template <int BITS, bool KEYS>
+__device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv, const float4* sPk,
+                                           const float* sS, const uint32_t* sO, int D, int Bk, int rows,
+                                           int r, int ch, int grp, int n_out, uint32_t (&w)[BITS]) {
+  const float Lf = (float)((1 << BITS) - 1);
+  const float2 magic2 = make_float2(kMagic, kMagic), nmagic2 = make_float2(-kMagic, -kMagic);
+  const float2 neg1 = make_float2(-1.0f, -1.0f);
+  float4 vp = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (!KEYS) vp = sPv[grp * Bk + r];
+  uint32_t mb[32];
+  float tmax = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint4 v = *reinterpret_cast<const uint4*>(sX + r * D + ((((4 * ch + k) ^ (r & 7))) << 3));
+    const uint32_t hw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = 8 * k + 2 * j;
+      const float2 x2 = __half22float2(*reinterpret_cast<const __half2*>(&hw[j]));
+      float2 nz2, r2;
+      if (KEYS) {
+        const float4 kp = sPk[(ch * 32 + e) >> 1];
+        nz2 = make_float2(kp.x, kp.y);
+        r2 = make_float2(kp.z, kp.w);
+      } else {
+        nz2 = make_float2(vp.x, vp.x);
+        r2 = make_float2(vp.y, vp.y);
+      }
+      const float2 y2 = __fmul2_rn(__fadd2_rn(x2, nz2), r2);
+      const float2 m2 = __fadd2_rn(y2, magic2);
+      const float2 t2 = __ffma2_rn(__fadd2_rn(m2, nmagic2), neg1, y2);   // y - rint(y)
+      tmax = fmaxf(tmax, fmaxf(fabsf(t2.x), fabsf(t2.y)));
+      mb[e] = __float_as_uint(m2.x);
+      mb[e + 1] = __float_as_uint(m2.y);
+    }
+  }
+  pack_bits<BITS>(mb, w);
+  auto zs_of = [&](int c, float& z, float& sc) {
+    if (KEYS) {
+      z = -reinterpret_cast<const float*>(&sPk[c >> 1])[c & 1];
+      sc = sS[c];
+    } else {
+      z = -vp.x;
+      sc = vp.z;
+    }
+  };
+  if (tmax > 0.5f - kTieGuard) {
+    // a value close to a rounding tie: the chunk with the exact division
+#pragma unroll 1
+    for (int e = 0; e < 32; ++e) {
+      const int c = ch * 32 + e;
+      const float x = __half2float(sX[sw_off(r, D, c)]);
+      if (isnan(x)) continue;   // outlier position: recomputed below
+      float z, sc;
+      zs_of(c, z, sc);
+      set_code<BITS>(w, e, quant_code(x, z, sc, Lf));
+    }
+  }
+#pragma unroll 1
+  for (int o = 0; o < n_out; ++o) {
+    const uint32_t ev = sO[o * Bk + r];
+    const int c = (int)(ev & 0xFFFFu);
+    if ((c >> 5) == ch) {
+      float z, sc;
+      zs_of(c, z, sc);
+      set_code<BITS>(w, c & 31, quant_code(__half2float(__ushort_as_half((uint16_t)(ev >> 16))), z, sc, Lf));
+    }
+  }
+}
+
 template <int BITS>
 __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -154,12 +234,12 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   const int rows = isK ? Bk : nv;
   const int t_row0 = isK ? t_blk0 : t_lo;          // token of staged row 0
 
-  __half* sX = reinterpret_cast<__half*>(smem);                              // [rows][D]
-  uint32_t* sO = reinterpret_cast<uint32_t*>(sX + Bk * D);                   // [rows][KVQ_MAX_OUTLIERS]
-  float4* sP = reinterpret_cast<float4*>(sO + Bk * KVQ_MAX_OUTLIERS);        // values: [rows][4] {-z, 1/s, s}
-                                                                             // keys: [D/2] {-z0, -z1, r0, r1}
-  float* sS = reinterpret_cast<float*>(sP + Bk * kMaxGroups);                // keys: s per channel [D]
-  __half2* sRed = reinterpret_cast<__half2*>(sS + D);                        // keys: [8][D/2] {min, max}
+  __half* sX = reinterpret_cast<__half*>(smem);                              // [rows][D], swizzled
+  uint32_t* sO = reinterpret_cast<uint32_t*>(sX + Bk * D);                   // [KVQ_MAX_OUTLIERS][Bk]
+  float4* sPv = reinterpret_cast<float4*>(sO + Bk * KVQ_MAX_OUTLIERS);       // values: [group][Bk] {-z, 1/s, s}
+  float4* sPk = sPv;                                                         // keys: [D/2] {-z0, -z1, 1/s0, 1/s1}
+  float* sS = reinterpret_cast<float*>(sPv + Bk * kMaxGroups);               // keys: s per channel [D]
+  __half2* sRed = reinterpret_cast<__half2*>(sS + D);                        // keys: [16][D/2] {min | max}
 
   // ---- A. stage rows in shared memory (16-byte vectors)
   for (int i = tid; i < rows * vpr; i += kThreads) {
@@ -168,12 +248,13 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
     const __half* src = isK ? ((t < a.T_cur) ? tail + (size_t)r * D
                                              : a.k_new + ((size_t)bh * a.n_new + (t - a.T_cur)) * D)
                             : a.v_new + ((size_t)bh * a.n_new + (t - a.T_cur)) * D;
-    reinterpret_cast<uint4*>(sX + r * D)[c] = __ldg(reinterpret_cast<const uint4*>(src) + c);
+    reinterpret_cast<uint4*>(sX + r * D)[c ^ (r & 7)] = __ldg(reinterpret_cast<const uint4*>(src) + c);
   }
   __syncthreads();
 
   // ---- B. dense-and-sparse split: per row, the n_out largest |x|
   uint32_t* gout_base = (isK ? a.k_outl : a.v_outl) + ((size_t)bh * d.T_max + t_row0) * n_out;
+  const __half nanh = __ushort_as_half((uint16_t)0x7E00u);   // marks outliers for step C
   if (n_out == 1 && D == 128) {
     // two threads per row, 64 channels each: the largest |x| (fp16 max), then
     // its lowest channel
@@ -182,10 +263,9 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
     uint32_t c_best = 0xFFFFu, m = 0u;
     uint32_t ab[32];
     if (active) {
-      const uint4* src = reinterpret_cast<const uint4*>(sX + row * D + 64 * half);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const uint4 v = src[k];
+        const uint4 v = reinterpret_cast<const uint4*>(sX + row * D)[(8 * half + k) ^ (row & 7)];
         ab[4 * k] = v.x & 0x7FFF7FFFu;
         ab[4 * k + 1] = v.y & 0x7FFF7FFFu;
         ab[4 * k + 2] = v.z & 0x7FFF7FFFu;
@@ -203,16 +283,17 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
 #pragma unroll
       for (int k = 31; k >= 0; --k) {
         const uint32_t eq = __vcmpeq2(ab[k], mm);
-        if (eq) c_best = 64 * half + 2 * k + ((eq & 0xFFFFu) ? 0 : 1);
+        c_best = eq ? (uint32_t)(64 * half + 2 * k + ((eq & 0xFFFFu) ? 0 : 1)) : c_best;
       }
     }
     const uint32_t other = __shfl_xor_sync(0xffffffffu, c_best, 1);
-    if (row < rows && half == 0) {
+    if (active && half == 0) {
       const uint32_t c = (c_best != 0xFFFFu) ? c_best : other;
-      const uint32_t e = c | ((uint32_t)hbits(sX[row * D + c]) << 16);
-      sO[row * KVQ_MAX_OUTLIERS] = e;
+      const int off = sw_off(row, D, (int)c);
+      const uint32_t e = c | ((uint32_t)hbits(sX[off]) << 16);
+      sO[row] = e;
       gout_base[row] = e;
-      sX[row * D + c] = __ushort_as_half((uint16_t)0x7E00u);   // NaN: skipped by step C
+      sX[off] = nanh;
     }
   } else if (n_out > 0) {
     // a warp per row: keys |x| bits (15) above (255 - channel); the max is the
@@ -220,12 +301,11 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
     const int warp = tid >> 5, lane = tid & 31;
     const int E = D >> 5;                          // elements per lane (2 or 4)
     for (int r = warp; r < rows; r += kThreads / 32) {
-      const __half* x = sX + r * D;
       uint32_t key[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int c = lane * E + e;
-        key[e] = (e < E) ? (((uint32_t)(hbits(x[c]) & 0x7FFF) << 8) | (uint32_t)(255 - c)) : 0u;
+        key[e] = (e < E) ? (((uint32_t)(hbits(sX[sw_off(r, D, c)]) & 0x7FFF) << 8) | (uint32_t)(255 - c)) : 0u;
       }
       uint32_t pick[KVQ_MAX_OUTLIERS];
       for (int k = 0; k < n_out; ++k) {
@@ -241,11 +321,11 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
       if (lane == 0) {
         for (int k = 0; k < n_out; ++k) {
           const uint32_t c = pick[k];
-          const uint32_t e = c | ((uint32_t)hbits(x[c]) << 16);
-          sO[r * KVQ_MAX_OUTLIERS + k] = e;
+          const uint32_t e = c | ((uint32_t)hbits(sX[sw_off(r, D, (int)c)]) << 16);
+          sO[k * Bk + r] = e;
           gout_base[(size_t)r * n_out + k] = e;
         }
-        for (int k = 0; k < n_out; ++k) sX[r * D + pick[k]] = __ushort_as_half((uint16_t)0x7E00u);
+        for (int k = 0; k < n_out; ++k) sX[sw_off(r, D, (int)pick[k])] = nanh;
       }
       __syncwarp();
     }
@@ -254,41 +334,33 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
 
   // ---- C. scale and zero (fp16 min/max skip the NaN-marked outliers)
   if (!isK) {
-    const int Gv = d.Gv, ng = d.ng;
+    const int Gv = d.Gv, ng = d.ng, cpg = Gv / 8;  // 16-byte chunks per group
     for (int it = tid; it < rows * ng; it += kThreads) {
-      const int r = it / ng, g = it % ng;
-      const uint4* x = reinterpret_cast<const uint4*>(sX + r * D + g * Gv);
-      __half2 mn2, mx2;
-      {
-        const uint4 v = x[0];
-        mn2 = __hmin2(__hmin2(*reinterpret_cast<const __half2*>(&v.x), *reinterpret_cast<const __half2*>(&v.y)),
-                      __hmin2(*reinterpret_cast<const __half2*>(&v.z), *reinterpret_cast<const __half2*>(&v.w)));
-        mx2 = __hmax2(__hmax2(*reinterpret_cast<const __half2*>(&v.x), *reinterpret_cast<const __half2*>(&v.y)),
-                      __hmax2(*reinterpret_cast<const __half2*>(&v.z), *reinterpret_cast<const __half2*>(&v.w)));
-      }
-      for (int k = 1; k < Gv / 8; ++k) {
-        const uint4 v = x[k];
-        mn2 = __hmin2(mn2, __hmin2(__hmin2(*reinterpret_cast<const __half2*>(&v.x), *reinterpret_cast<const __half2*>(&v.y)),
-                                   __hmin2(*reinterpret_cast<const __half2*>(&v.z), *reinterpret_cast<const __half2*>(&v.w))));
-        mx2 = __hmax2(mx2, __hmax2(__hmax2(*reinterpret_cast<const __half2*>(&v.x), *reinterpret_cast<const __half2*>(&v.y)),
-                                   __hmax2(*reinterpret_cast<const __half2*>(&v.z), *reinterpret_cast<const __half2*>(&v.w))));
+      const int g = it / rows, r = it % rows;      // consecutive threads: consecutive rows
+      const uint4* xr = reinterpret_cast<const uint4*>(sX + r * D);
+      __half2 mn2 = __halves2half2(nanh, nanh), mx2 = mn2;
+      for (int k = 0; k < cpg; ++k) {
+        const uint4 v = xr[(g * cpg + k) ^ (r & 7)];
+        const __half2 a0 = *reinterpret_cast<const __half2*>(&v.x), a1 = *reinterpret_cast<const __half2*>(&v.y);
+        const __half2 a2 = *reinterpret_cast<const __half2*>(&v.z), a3 = *reinterpret_cast<const __half2*>(&v.w);
+        mn2 = __hmin2(mn2, __hmin2(__hmin2(a0, a1), __hmin2(a2, a3)));
+        mx2 = __hmax2(mx2, __hmax2(__hmax2(a0, a1), __hmax2(a2, a3)));
       }
       const float mn = fminf(__low2float(mn2), __high2float(mn2));
       const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
-      const bool any = !isnan(mn);
       float2 sz;
-      const uint32_t packed = group_params(mn, mx, any, Lf, &sz);
+      const uint32_t packed = group_params(mn, mx, !isnan(mn), Lf, &sz);
       a.v_meta[((size_t)bh * d.T_max + (t_row0 + r)) * ng + g] = packed;
-      sP[r * kMaxGroups + g] = make_float4(-sz.y, sz.x > 0.0f ? __frcp_rn(sz.x) : 0.0f, sz.x, 0.0f);
+      sPv[g * Bk + r] = make_float4(-sz.y, sz.x > 0.0f ? __frcp_rn(sz.x) : 0.0f, sz.x, 0.0f);
     }
   } else {
     // channel pairs p < D/2, row slices q < S: partial fp16 min/max, then combined
     const int P = D / 2, S = kThreads / P;
     const int p = tid % P, q = tid / P;
-    const __half nanh = __ushort_as_half((uint16_t)0x7E00u);  // NaN: the identity of min/max here
     __half2 mn2 = __halves2half2(nanh, nanh), mx2 = mn2;
+    const int pc = p >> 2, pw = p & 3;             // 16-byte chunk and half2 within it
     for (int j = q; j < Bk; j += S) {
-      const __half2 v = reinterpret_cast<const __half2*>(sX + j * D)[p];
+      const __half2 v = reinterpret_cast<const __half2*>(sX + j * D)[((pc ^ (j & 7)) << 2) + pw];
       mn2 = __hmin2(mn2, v);
       mx2 = __hmax2(mx2, v);
     }
@@ -296,18 +368,17 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
     sRed[(2 * q + 1) * P + p] = mx2;
     __syncthreads();
     if (tid < D) {
-      const int c = tid, pc = c >> 1, hc = c & 1;
+      const int c = tid, cp = c >> 1, hc = c & 1;
       float mn = NAN, mx = NAN;
       for (int qq = 0; qq < S; ++qq) {
-        const __half2 a2 = sRed[(2 * qq) * P + pc], b2 = sRed[(2 * qq + 1) * P + pc];
+        const __half2 a2 = sRed[(2 * qq) * P + cp], b2 = sRed[(2 * qq + 1) * P + cp];
         mn = fminf(mn, hc ? __high2float(a2) : __low2float(a2));
         mx = fmaxf(mx, hc ? __high2float(b2) : __low2float(b2));
       }
-      const bool any = !isnan(mn);
       float2 sz;
-      const uint32_t packed = group_params(mn, mx, any, Lf, &sz);
+      const uint32_t packed = group_params(mn, mx, !isnan(mn), Lf, &sz);
       a.k_meta[((size_t)bh * d.n_blk + blk) * D + c] = packed;
-      float* pk = reinterpret_cast<float*>(&sP[pc]);
+      float* pk = reinterpret_cast<float*>(&sPk[cp]);
       pk[hc] = -sz.y;
       pk[2 + hc] = sz.x > 0.0f ? __frcp_rn(sz.x) : 0.0f;
       sS[c] = sz.x;
@@ -319,78 +390,14 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   {
     const int nch = D / 32;
     uint8_t* base = isK ? a.k_codes : a.v_codes;
-    const float2 magic2 = make_float2(kMagic, kMagic), nmagic2 = make_float2(-kMagic, -kMagic);
-    const float2 neg1 = make_float2(-1.0f, -1.0f);
     for (int it = tid; it < rows * nch; it += kThreads) {
-      const int r = it / nch, ch = it % nch;
-      const uint4* xs = reinterpret_cast<const uint4*>(sX + r * D + ch * 32);
-      float4 vp = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (!isK) vp = sP[r * kMaxGroups + (ch * 32) / d.Gv];
-      uint32_t mb[32];
-      float tmax = 0.0f;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint4 v = xs[k];
-        const uint32_t hw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int e = 8 * k + 2 * j;
-          const float2 x2 = __half22float2(*reinterpret_cast<const __half2*>(&hw[j]));
-          float2 nz2, r2;
-          if (isK) {
-            const float4 kp = sP[(ch * 32 + e) >> 1];
-            nz2 = make_float2(kp.x, kp.y);
-            r2 = make_float2(kp.z, kp.w);
-          } else {
-            nz2 = make_float2(vp.x, vp.x);
-            r2 = make_float2(vp.y, vp.y);
-          }
-          const float2 y2 = __fmul2_rn(__fadd2_rn(x2, nz2), r2);
-          const float2 m2 = __fadd2_rn(y2, magic2);
-          const float2 t2 = __ffma2_rn(__fadd2_rn(m2, nmagic2), neg1, y2);   // y - rint(y)
-          tmax = fmaxf(tmax, fmaxf(fabsf(t2.x), fabsf(t2.y)));
-          mb[e] = __float_as_uint(m2.x);
-          mb[e + 1] = __float_as_uint(m2.y);
-        }
-      }
+      const int ch = it / rows, r = it % rows;     // consecutive threads: consecutive rows
       uint32_t w[BITS];
-      pack_bits<BITS>(mb, w);
-      const int t = t_row0 + r;
-      if (tmax > 0.5f - kTieGuard) {
-        // a value close to a rounding tie: the chunk with the exact division
-        const __half* xh = sX + r * D + ch * 32;
-#pragma unroll 1
-        for (int e = 0; e < 32; ++e) {
-          const int c = ch * 32 + e;
-          const float x = __half2float(xh[e]);
-          if (isnan(x)) continue;   // outlier position: recomputed below
-          float z, s;
-          if (isK) {
-            z = -reinterpret_cast<const float*>(&sP[c >> 1])[c & 1];
-            s = sS[c];
-          } else {
-            z = -vp.x;
-            s = vp.z;
-          }
-          set_code<BITS>(w, e, quant_code(x, z, s, Lf));
-        }
-      }
-      for (int o = 0; o < n_out; ++o) {
-        const uint32_t ev = sO[r * KVQ_MAX_OUTLIERS + o];
-        const int c = (int)(ev & 0xFFFFu);
-        if ((c >> 5) == ch) {
-          float z, s;
-          if (isK) {
-            z = -reinterpret_cast<const float*>(&sP[c >> 1])[c & 1];
-            s = sS[c];
-          } else {
-            z = -vp.x;
-            s = vp.z;
-          }
-          set_code<BITS>(w, c & 31, quant_code(__half2float(__ushort_as_half((uint16_t)(ev >> 16))), z, s, Lf));
-        }
-      }
-      uint32_t* dst = reinterpret_cast<uint32_t*>(base + ((size_t)bh * d.T_max + t) * d.cb) + ch * BITS;
+      if (isK)
+        chunk_codes<BITS, true>(sX, sPv, sPk, sS, sO, D, Bk, rows, r, ch, 0, n_out, w);
+      else
+        chunk_codes<BITS, false>(sX, sPv, sPk, sS, sO, D, Bk, rows, r, ch, (ch * 32) / d.Gv, n_out, w);
+      uint32_t* dst = reinterpret_cast<uint32_t*>(base + ((size_t)bh * d.T_max + (t_row0 + r)) * d.cb) + ch * BITS;
       if constexpr (BITS == 4) {
         *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
       } else if constexpr (BITS == 2) {
