@@ -17,10 +17,11 @@
 //      channel by four or eight threads over row slices;
 //   D. codes: 32 channels of a row per thread, two at a time in packed fp32
 //      (x - z, times 1/s, rounded by the 1.5 * 2^23 addition), packed and
-//      stored with one or three vector stores. The product with 1/s is within
-//      3e-6 of the binary32 quotient for codes below 16, so a chunk whose
-//      values all sit further than 1e-5 from a rounding tie gets the codes
-//      of the exact division; a chunk with a near tie is recomputed with it.
+//      stored with one or three vector stores. The product with 1/s (1 ulp)
+//      is within 4e-6 of the binary32 quotient for codes below 16, so a chunk
+//      whose values all sit further than 1e-5 from a rounding tie gets the
+//      codes of the exact division; a chunk with a near tie is recomputed
+//      with it.
 //      Outlier positions are recomputed from their stored value.
 // All rounding follows the library's stated arithmetic: binary32 RN subtract
 // and divide, fp16 round-up for the scale, round-half-even codes.
@@ -50,6 +51,14 @@ struct AppendArgs {
 };
 
 __device__ __forceinline__ uint16_t hbits(__half h) { return __half_as_ushort(h); }
+
+// 1/s to within 1 ulp (hardware approximation); 0 for s = 0. The code path
+// above bounds |y - (x - z)/s| by 4e-6 for |y| < 16 with it, below the tie guard.
+__device__ __forceinline__ float rcp_or_zero(float s) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+  return s > 0.0f ? r : 0.0f;
+}
 
 // clamp(rint((x - z) / s), 0, L) in binary32 round-to-nearest; 0 when s = 0.
 // Clamping r to [0, L] before rounding gives the same integer as clamping after.
@@ -200,11 +209,11 @@ __device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv,
   }
 }
 
-template <int BITS>
+template <int BITS, int D>
 __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const Dims d = a.d;
-  const int D = d.D, Bk = d.Bk, n_out = d.n_out;
+  const int Bk = d.Bk, n_out = d.n_out;
   const int tid = threadIdx.x;
   const int bh = blockIdx.y;
   const bool isK = blockIdx.z != 0;
@@ -216,7 +225,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   const int nv = t_hi - t_lo;                      // new tokens in this block, >= 1
   const bool complete = t_blk0 + Bk <= t_end;
   const float Lf = (float)((1 << BITS) - 1);
-  const int vpr = D / 8;                           // 16-byte vectors per row
+  constexpr int vpr = D / 8;                       // 16-byte vectors per row
   __half* tail = a.k_tail + (size_t)bh * Bk * D;
 
   if (isK && !complete) {
@@ -335,8 +344,10 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   // ---- C. scale and zero (fp16 min/max skip the NaN-marked outliers)
   if (!isK) {
     const int Gv = d.Gv, ng = d.ng, cpg = Gv / 8;  // 16-byte chunks per group
-    for (int it = tid; it < rows * ng; it += kThreads) {
-      const int g = it / rows, r = it % rows;      // consecutive threads: consecutive rows
+    const int bk_sh = __ffs(Bk) - 1;
+    for (int it = tid; it < (ng << bk_sh); it += kThreads) {
+      const int g = it >> bk_sh, r = it & (Bk - 1);   // consecutive threads: consecutive rows
+      if (r >= rows) continue;
       const uint4* xr = reinterpret_cast<const uint4*>(sX + r * D);
       __half2 mn2 = __halves2half2(nanh, nanh), mx2 = mn2;
       for (int k = 0; k < cpg; ++k) {
@@ -351,7 +362,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
       float2 sz;
       const uint32_t packed = group_params(mn, mx, !isnan(mn), Lf, &sz);
       a.v_meta[((size_t)bh * d.T_max + (t_row0 + r)) * ng + g] = packed;
-      sPv[g * Bk + r] = make_float4(-sz.y, sz.x > 0.0f ? __frcp_rn(sz.x) : 0.0f, sz.x, 0.0f);
+      sPv[g * Bk + r] = make_float4(-sz.y, rcp_or_zero(sz.x), sz.x, 0.0f);
     }
   } else {
     // channel pairs p < D/2, row slices q < S: partial fp16 min/max, then combined
@@ -380,7 +391,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
       a.k_meta[((size_t)bh * d.n_blk + blk) * D + c] = packed;
       float* pk = reinterpret_cast<float*>(&sPk[cp]);
       pk[hc] = -sz.y;
-      pk[2 + hc] = sz.x > 0.0f ? __frcp_rn(sz.x) : 0.0f;
+      pk[2 + hc] = rcp_or_zero(sz.x);
       sS[c] = sz.x;
     }
   }
@@ -388,15 +399,18 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
 
   // ---- D. codes for every element (outlier positions recomputed), packed
   {
-    const int nch = D / 32;
+    constexpr int nch = D / 32;
+    const int gv_sh = __ffs(d.Gv) - 1;
     uint8_t* base = isK ? a.k_codes : a.v_codes;
-    for (int it = tid; it < rows * nch; it += kThreads) {
-      const int ch = it / rows, r = it % rows;     // consecutive threads: consecutive rows
+    const int bk_sh = __ffs(Bk) - 1;
+    for (int it = tid; it < (nch << bk_sh); it += kThreads) {
+      const int ch = it >> bk_sh, r = it & (Bk - 1);  // consecutive threads: consecutive rows
+      if (r >= rows) continue;
       uint32_t w[BITS];
       if (isK)
         chunk_codes<BITS, true>(sX, sPv, sPk, sS, sO, D, Bk, rows, r, ch, 0, n_out, w);
       else
-        chunk_codes<BITS, false>(sX, sPv, sPk, sS, sO, D, Bk, rows, r, ch, (ch * 32) / d.Gv, n_out, w);
+        chunk_codes<BITS, false>(sX, sPv, sPk, sS, sO, D, Bk, rows, r, ch, (ch * 32) >> gv_sh, n_out, w);
       uint32_t* dst = reinterpret_cast<uint32_t*>(base + ((size_t)bh * d.T_max + (t_row0 + r)) * d.cb) + ch * BITS;
       if constexpr (BITS == 4) {
         *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -431,17 +445,21 @@ size_t append_smem(const Dims& d) {
          (size_t)16 * (d.D / 2) * sizeof(__half2);
 }
 
-template <int BITS>
-cudaError_t launch_bits(const AppendArgs& a, dim3 grid, size_t smem, cudaStream_t st) {
+template <int BITS, int D>
+cudaError_t launch_bd(const AppendArgs& a, dim3 grid, size_t smem, cudaStream_t st) {
   static bool attr_set = false;  // per device the attribute is idempotent
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(append_kernel<BITS>,
+    cudaError_t e = cudaFuncSetAttribute(append_kernel<BITS, D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  append_kernel<BITS><<<grid, kThreads, smem, st>>>(a);
+  append_kernel<BITS, D><<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();
+}
+template <int BITS>
+cudaError_t launch_bits(const AppendArgs& a, dim3 grid, size_t smem, cudaStream_t st) {
+  return a.d.D == 64 ? launch_bd<BITS, 64>(a, grid, smem, st) : launch_bd<BITS, 128>(a, grid, smem, st);
 }
 
 }  // namespace
