@@ -52,21 +52,43 @@ struct AppendArgs {
 
 __device__ __forceinline__ uint16_t hbits(__half h) { return __half_as_ushort(h); }
 
-// 1/s to within 1 ulp (hardware approximation); 0 for s = 0. The code path
-// above bounds |y - (x - z)/s| by 4e-6 for |y| < 16 with it, below the tie guard.
+// 1/s to within 1 ulp (hardware approximation); 0 for s = 0. With it the
+// products below are within 4e-6 of the quotients for |y| < 16, inside the
+// tie guard.
 __device__ __forceinline__ float rcp_or_zero(float s) {
   float r;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
   return s > 0.0f ? r : 0.0f;
 }
 
-// clamp(rint((x - z) / s), 0, L) in binary32 round-to-nearest; 0 when s = 0.
-// Clamping r to [0, L] before rounding gives the same integer as clamping after.
-__device__ __forceinline__ uint32_t quant_code(float x, float z, float s, float Lf) {
-  if (s == 0.0f) return 0u;
-  float r = __fdiv_rn(__fsub_rn(x, z), s);
-  r = fminf(fmaxf(r, 0.0f), Lf);
-  return (uint32_t)__float2int_rn(r);
+// clamp(rint(fl((x - z) / s)), 0, L) in binary32 round-to-nearest (0 when
+// s = 0), computed without a division: y = (x - z) * r with r within 1 ulp of
+// 1/s is within 4e-6 of the binary32 quotient Q = fl((x - z) / s) when
+// |y| < 16. Away from the half-integers the rounding of y is that of Q. Near
+// a half-integer h the exact residual rho = (x - z) - h*s (one fma, exact) and
+// half an ulp of h, times s (exact), tell whether Q rounds to h (then ties go
+// to the even integer) or to a neighbour. Beyond [-0.75, L + 0.75] the clamp
+// decides.
+__device__ __forceinline__ uint32_t exact_code(float x, float z, float s, float r, int L) {
+  if (!(s > 0.0f)) return 0u;
+  const float d = __fsub_rn(x, z);
+  const float y = __fmul_rn(d, r);
+  if (y > (float)L + 0.75f) return (uint32_t)L;
+  if (!(y > -0.75f)) return 0u;
+  const float fl = floorf(y), h = fl + 0.5f;
+  float q;
+  if (fabsf(y - h) > 1e-5f) {
+    q = rintf(y);
+  } else {
+    const float rho = __fmaf_rn(-h, s, d);
+    const int e = ilogbf(h);                                     // ulp(h) = 2^(e - 23)
+    const float hs = s * __int_as_float((e - 24 + 127) << 23);   // half an ulp of h, times s
+    if (rho > hs) q = fl + 1.0f;
+    else if (rho < -hs) q = fl;
+    else q = (((int)fl) & 1) ? fl + 1.0f : fl;                  // Q == h: ties to even
+  }
+  q = fminf(fmaxf(q, 0.0f), (float)L);
+  return (uint32_t)q;
 }
 
 // Scale and zero of one group from the min/max of its dense elements.
@@ -143,7 +165,6 @@ template <int BITS, bool KEYS>
 __device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv, const float4* sPk,
                                            const float* sS, const uint32_t* sO, int D, int Bk, int rows,
                                            int r, int ch, int grp, int n_out, uint32_t (&w)[BITS]) {
-  const float Lf = (float)((1 << BITS) - 1);
   const float2 magic2 = make_float2(kMagic, kMagic), nmagic2 = make_float2(-kMagic, -kMagic);
   const float2 neg1 = make_float2(-1.0f, -1.0f);
   float4 vp = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -176,25 +197,30 @@ __device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv,
     }
   }
   pack_bits<BITS>(mb, w);
-  auto zs_of = [&](int c, float& z, float& sc) {
+  auto zsr_of = [&](int c, float& z, float& sc, float& rc) {
     if (KEYS) {
       z = -reinterpret_cast<const float*>(&sPk[c >> 1])[c & 1];
+      rc = reinterpret_cast<const float*>(&sPk[c >> 1])[2 + (c & 1)];
       sc = sS[c];
     } else {
       z = -vp.x;
+      rc = vp.y;
       sc = vp.z;
     }
   };
+  constexpr int L = (1 << BITS) - 1;
   if (tmax > 0.5f - kTieGuard) {
-    // a value close to a rounding tie: the chunk with the exact division
+    // some value sits close to a rounding tie: those get the exact rule
 #pragma unroll 1
     for (int e = 0; e < 32; ++e) {
       const int c = ch * 32 + e;
       const float x = __half2float(sX[sw_off(r, D, c)]);
-      if (isnan(x)) continue;   // outlier position: recomputed below
-      float z, sc;
-      zs_of(c, z, sc);
-      set_code<BITS>(w, e, quant_code(x, z, sc, Lf));
+      float z, sc, rc;
+      zsr_of(c, z, sc, rc);
+      const float y = __fmul_rn(__fsub_rn(x, z), rc);
+      const float t = y - rintf(y);
+      if (!(fabsf(t) > 0.5f - kTieGuard)) continue;   // NaN (outlier position) included: recomputed below
+      set_code<BITS>(w, e, exact_code(x, z, sc, rc, L));
     }
   }
 #pragma unroll 1
@@ -202,9 +228,9 @@ __device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv,
     const uint32_t ev = sO[o * Bk + r];
     const int c = (int)(ev & 0xFFFFu);
     if ((c >> 5) == ch) {
-      float z, sc;
-      zs_of(c, z, sc);
-      set_code<BITS>(w, c & 31, quant_code(__half2float(__ushort_as_half((uint16_t)(ev >> 16))), z, sc, Lf));
+      float z, sc, rc;
+      zsr_of(c, z, sc, rc);
+      set_code<BITS>(w, c & 31, exact_code(__half2float(__ushort_as_half((uint16_t)(ev >> 16))), z, sc, rc, L));
     }
   }
 }
@@ -250,14 +276,27 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   float* sS = reinterpret_cast<float*>(sPv + Bk * kMaxGroups);               // keys: s per channel [D]
   __half2* sRed = reinterpret_cast<__half2*>(sS + D);                        // keys: [16][D/2] {min | max}
 
-  // ---- A. stage rows in shared memory (16-byte vectors)
-  for (int i = tid; i < rows * vpr; i += kThreads) {
-    const int r = i / vpr, c = i % vpr;
-    const int t = t_row0 + r;
-    const __half* src = isK ? ((t < a.T_cur) ? tail + (size_t)r * D
-                                             : a.k_new + ((size_t)bh * a.n_new + (t - a.T_cur)) * D)
-                            : a.v_new + ((size_t)bh * a.n_new + (t - a.T_cur)) * D;
-    reinterpret_cast<uint4*>(sX + r * D)[c ^ (r & 7)] = __ldg(reinterpret_cast<const uint4*>(src) + c);
+  // ---- A. stage rows in shared memory (16-byte vectors, all loads in flight
+  // before the first store)
+  {
+    constexpr int kMaxVec = 128 * vpr / kThreads;  // rows <= 128
+    uint4 v[kMaxVec];
+#pragma unroll
+    for (int k = 0; k < kMaxVec; ++k) {
+      const int i = tid + k * kThreads, r = i / vpr, c = i % vpr;
+      if (r < rows) {
+        const int t = t_row0 + r;
+        const __half* src = isK ? ((t < a.T_cur) ? tail + (size_t)r * D
+                                                 : a.k_new + ((size_t)bh * a.n_new + (t - a.T_cur)) * D)
+                                : a.v_new + ((size_t)bh * a.n_new + (t - a.T_cur)) * D;
+        v[k] = __ldg(reinterpret_cast<const uint4*>(src) + c);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kMaxVec; ++k) {
+      const int i = tid + k * kThreads, r = i / vpr, c = i % vpr;
+      if (r < rows) reinterpret_cast<uint4*>(sX + r * D)[c ^ (r & 7)] = v[k];
+    }
   }
   __syncthreads();
 
@@ -269,35 +308,51 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
     // its lowest channel
     const int row = tid >> 1, half = tid & 1;
     const bool active = row < rows;                // both threads of a row agree
-    uint32_t c_best = 0xFFFFu, m = 0u;
-    uint32_t ab[32];
+    uint32_t c_best = 0xFFFFu;
+    __half2 m2 = __float2half2_rn(0.0f);
+    __half2 cm[8];                                 // per-chunk max |x|
     if (active) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const uint4 v = reinterpret_cast<const uint4*>(sX + row * D)[(8 * half + k) ^ (row & 7)];
-        ab[4 * k] = v.x & 0x7FFF7FFFu;
-        ab[4 * k + 1] = v.y & 0x7FFF7FFFu;
-        ab[4 * k + 2] = v.z & 0x7FFF7FFFu;
-        ab[4 * k + 3] = v.w & 0x7FFF7FFFu;
+        const uint32_t a4[4] = {v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu, v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu};
+        const __half2* h = reinterpret_cast<const __half2*>(a4);
+        cm[k] = __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3]));
       }
-      __half2 m2 = *reinterpret_cast<__half2*>(&ab[0]);
-#pragma unroll
-      for (int k = 1; k < 32; ++k) m2 = __hmax2(m2, *reinterpret_cast<__half2*>(&ab[k]));
-      const uint32_t mu = *reinterpret_cast<uint32_t*>(&m2);
-      m = max(mu & 0xFFFFu, mu >> 16);
+      m2 = __hmax2(__hmax2(__hmax2(cm[0], cm[1]), __hmax2(cm[2], cm[3])),
+                   __hmax2(__hmax2(cm[4], cm[5]), __hmax2(cm[6], cm[7])));
+      m2 = __hmax2(m2, __lowhigh2highlow(m2));     // both halves: the thread's max |x|
     }
-    m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    {
+      const uint32_t mine = *reinterpret_cast<uint32_t*>(&m2);
+      const uint32_t theirs = __shfl_xor_sync(0xffffffffu, mine, 1);
+      m2 = __hmax2(m2, *reinterpret_cast<const __half2*>(&theirs));   // the row's max |x|
+    }
     if (active) {
-      const uint32_t mm = m | (m << 16);
+      // first chunk holding the max, then its first word and half
+      int kc = 8;
 #pragma unroll
-      for (int k = 31; k >= 0; --k) {
-        const uint32_t eq = __vcmpeq2(ab[k], mm);
-        c_best = eq ? (uint32_t)(64 * half + 2 * k + ((eq & 0xFFFFu) ? 0 : 1)) : c_best;
+      for (int k = 7; k >= 0; --k) {
+        const __half2 e2 = __heq2(cm[k], m2);
+        kc = (*reinterpret_cast<const uint32_t*>(&e2) != 0u) ? k : kc;
+      }
+      if (kc < 8) {
+        const uint4 v = reinterpret_cast<const uint4*>(sX + row * D)[(8 * half + kc) ^ (row & 7)];
+        const uint32_t wv[4] = {v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu, v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu};
+        int idx = 0;
+#pragma unroll
+        for (int j = 3; j >= 0; --j) {
+          const __half2 e2 = __heq2(*reinterpret_cast<const __half2*>(&wv[j]), m2);
+          const uint32_t eu = *reinterpret_cast<const uint32_t*>(&e2);
+          idx = eu ? (2 * j + ((eu & 0xFFFFu) ? 0 : 1)) : idx;
+        }
+        c_best = 64 * half + 8 * kc + idx;
       }
     }
     const uint32_t other = __shfl_xor_sync(0xffffffffu, c_best, 1);
     if (active && half == 0) {
-      const uint32_t c = (c_best != 0xFFFFu) ? c_best : other;
+      uint32_t c = (c_best != 0xFFFFu) ? c_best : other;
+      c = min(c, (uint32_t)(D - 1));               // only NaN rows (out of contract) match nothing
       const int off = sw_off(row, D, (int)c);
       const uint32_t e = c | ((uint32_t)hbits(sX[off]) << 16);
       sO[row] = e;
