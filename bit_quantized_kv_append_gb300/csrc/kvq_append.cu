@@ -159,22 +159,25 @@ __device__ __forceinline__ int sw_off(int r, int D, int col) {
 }
 
 // Step D for one 32-channel chunk of row r: codes from the packed fp32 path,
-// exact division where a value sits near a rounding tie, outlier positions
-// from their stored value; returns the packed words.
+// the exact rule for the 8-channel groups holding a value near a rounding
+// tie, and the outlier positions' codes (computed in step C'); returns the
+// packed words.
 template <int BITS, bool KEYS>
 __device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv, const float4* sPk,
-                                           const float* sS, const uint32_t* sO, int D, int Bk, int rows,
-                                           int r, int ch, int grp, int n_out, uint32_t (&w)[BITS]) {
+                                           const float* sS, const uint32_t* sO, const uint8_t* sQ, int D,
+                                           int Bk, int r, int ch, int grp, int n_out, uint32_t (&w)[BITS]) {
+  constexpr int L = (1 << BITS) - 1;
   const float2 magic2 = make_float2(kMagic, kMagic), nmagic2 = make_float2(-kMagic, -kMagic);
   const float2 neg1 = make_float2(-1.0f, -1.0f);
   float4 vp = make_float4(0.f, 0.f, 0.f, 0.f);
   if (!KEYS) vp = sPv[grp * Bk + r];
   uint32_t mb[32];
-  float tmax = 0.0f;
+  float tm[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const uint4 v = *reinterpret_cast<const uint4*>(sX + r * D + ((((4 * ch + k) ^ (r & 7))) << 3));
     const uint32_t hw[4] = {v.x, v.y, v.z, v.w};
+    tm[k] = 0.0f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int e = 8 * k + 2 * j;
@@ -191,47 +194,39 @@ __device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv,
       const float2 y2 = __fmul2_rn(__fadd2_rn(x2, nz2), r2);
       const float2 m2 = __fadd2_rn(y2, magic2);
       const float2 t2 = __ffma2_rn(__fadd2_rn(m2, nmagic2), neg1, y2);   // y - rint(y)
-      tmax = fmaxf(tmax, fmaxf(fabsf(t2.x), fabsf(t2.y)));
+      tm[k] = fmaxf(tm[k], fmaxf(fabsf(t2.x), fabsf(t2.y)));           // NaN (outlier) ignored
       mb[e] = __float_as_uint(m2.x);
       mb[e + 1] = __float_as_uint(m2.y);
     }
   }
   pack_bits<BITS>(mb, w);
-  auto zsr_of = [&](int c, float& z, float& sc, float& rc) {
-    if (KEYS) {
-      z = -reinterpret_cast<const float*>(&sPk[c >> 1])[c & 1];
-      rc = reinterpret_cast<const float*>(&sPk[c >> 1])[2 + (c & 1)];
-      sc = sS[c];
-    } else {
-      z = -vp.x;
-      rc = vp.y;
-      sc = vp.z;
-    }
-  };
-  constexpr int L = (1 << BITS) - 1;
-  if (tmax > 0.5f - kTieGuard) {
-    // some value sits close to a rounding tie: those get the exact rule
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (tm[k] > 0.5f - kTieGuard) {
+      // a value of these 8 channels sits close to a rounding tie: exact rule
 #pragma unroll 1
-    for (int e = 0; e < 32; ++e) {
-      const int c = ch * 32 + e;
-      const float x = __half2float(sX[sw_off(r, D, c)]);
-      float z, sc, rc;
-      zsr_of(c, z, sc, rc);
-      const float y = __fmul_rn(__fsub_rn(x, z), rc);
-      const float t = y - rintf(y);
-      if (!(fabsf(t) > 0.5f - kTieGuard)) continue;   // NaN (outlier position) included: recomputed below
-      set_code<BITS>(w, e, exact_code(x, z, sc, rc, L));
+      for (int e = 8 * k; e < 8 * k + 8; ++e) {
+        const int c = ch * 32 + e;
+        const float x = __half2float(sX[sw_off(r, D, c)]);
+        float z, sc, rc;
+        if (KEYS) {
+          z = -reinterpret_cast<const float*>(&sPk[c >> 1])[c & 1];
+          rc = reinterpret_cast<const float*>(&sPk[c >> 1])[2 + (c & 1)];
+          sc = sS[c];
+        } else {
+          z = -vp.x;
+          rc = vp.y;
+          sc = vp.z;
+        }
+        const float y = __fmul_rn(__fsub_rn(x, z), rc);
+        if (!(fabsf(y - rintf(y)) > 0.5f - kTieGuard)) continue;   // NaN (outlier position) included
+        set_code<BITS>(w, e, exact_code(x, z, sc, rc, L));
+      }
     }
   }
-#pragma unroll 1
   for (int o = 0; o < n_out; ++o) {
-    const uint32_t ev = sO[o * Bk + r];
-    const int c = (int)(ev & 0xFFFFu);
-    if ((c >> 5) == ch) {
-      float z, sc, rc;
-      zsr_of(c, z, sc, rc);
-      set_code<BITS>(w, c & 31, exact_code(__half2float(__ushort_as_half((uint16_t)(ev >> 16))), z, sc, rc, L));
-    }
+    const int c = (int)(sO[o * Bk + r] & 0xFFFFu);
+    if ((c >> 5) == ch) set_code<BITS>(w, c & 31, sQ[o * Bk + r]);
   }
 }
 
@@ -275,6 +270,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   float4* sPk = sPv;                                                         // keys: [D/2] {-z0, -z1, 1/s0, 1/s1}
   float* sS = reinterpret_cast<float*>(sPv + Bk * kMaxGroups);               // keys: s per channel [D]
   __half2* sRed = reinterpret_cast<__half2*>(sS + D);                        // keys: [16][D/2] {min | max}
+  uint8_t* sQ = reinterpret_cast<uint8_t*>(sRed);                            // after C: outlier codes [n_out][Bk]
 
   // ---- A. stage rows in shared memory (16-byte vectors, all loads in flight
   // before the first store)
@@ -452,7 +448,32 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   }
   __syncthreads();
 
-  // ---- D. codes for every element (outlier positions recomputed), packed
+  // ---- C'. codes of the outlier positions, from their stored values
+  if (n_out > 0) {
+    const int bk_sh = __ffs(Bk) - 1, gv_sh = __ffs(d.Gv) - 1;
+    constexpr int L = (1 << BITS) - 1;
+    for (int it = tid; it < (n_out << bk_sh); it += kThreads) {
+      const int o = it >> bk_sh, r = it & (Bk - 1);
+      if (r >= rows) continue;
+      const uint32_t ev = sO[o * Bk + r];
+      const int c = (int)(ev & 0xFFFFu);
+      float z, sc, rc;
+      if (isK) {
+        z = -reinterpret_cast<const float*>(&sPk[c >> 1])[c & 1];
+        rc = reinterpret_cast<const float*>(&sPk[c >> 1])[2 + (c & 1)];
+        sc = sS[c];
+      } else {
+        const float4 vp = sPv[(c >> gv_sh) * Bk + r];
+        z = -vp.x;
+        rc = vp.y;
+        sc = vp.z;
+      }
+      sQ[o * Bk + r] = (uint8_t)exact_code(__half2float(__ushort_as_half((uint16_t)(ev >> 16))), z, sc, rc, L);
+    }
+    __syncthreads();
+  }
+
+  // ---- D. codes for every element, packed
   {
     constexpr int nch = D / 32;
     const int gv_sh = __ffs(d.Gv) - 1;
@@ -463,9 +484,9 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
       if (r >= rows) continue;
       uint32_t w[BITS];
       if (isK)
-        chunk_codes<BITS, true>(sX, sPv, sPk, sS, sO, D, Bk, rows, r, ch, 0, n_out, w);
+        chunk_codes<BITS, true>(sX, sPv, sPk, sS, sO, sQ, D, Bk, r, ch, 0, n_out, w);
       else
-        chunk_codes<BITS, false>(sX, sPv, sPk, sS, sO, D, Bk, rows, r, ch, (ch * 32) >> gv_sh, n_out, w);
+        chunk_codes<BITS, false>(sX, sPv, sPk, sS, sO, sQ, D, Bk, r, ch, (ch * 32) >> gv_sh, n_out, w);
       uint32_t* dst = reinterpret_cast<uint32_t*>(base + ((size_t)bh * d.T_max + (t_row0 + r)) * d.cb) + ch * BITS;
       if constexpr (BITS == 4) {
         *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
