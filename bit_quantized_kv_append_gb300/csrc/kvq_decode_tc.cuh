@@ -409,8 +409,9 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
 
   // ---- per-thread constants of the block preparation
   // queries: thread owns rotate-half pair qi and heads tid/64, tid/64 + 2, ...
+  // (one head: threads tid and tid + 64 write the two halves of pair qi)
   const int qi = tid & (HALF - 1);
-  const bool q_thread = (G > 1) || (tid < HALF);
+  constexpr bool q_thread = true;
   uint32_t q_off;
   {
     int rr, kq, s;
@@ -448,12 +449,19 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
       for (int sl = 0; sl < SL; ++sl) {
         const float2 rs = sl ? rot_compose(rr, r64) : rr;
         uint8_t* qa = reinterpret_cast<uint8_t*>(&s_qa[buf][sl][0][0]) + q_off;
+        if constexpr (G == 1) {
+          const float x = s_qp[0][qi], y = s_qp[0][qi + HALF];
+          const bool part = tid >= HALF;
+          const float v = part ? fmaf(y, rs.x, -x * rs.y) : fmaf(x, rs.x, y * rs.y);   // apply R(-t)
+          *reinterpret_cast<__half*>(qa + (part ? 2048 : 0)) = __float2half_rn(v);
+        } else {
 #pragma unroll
-        for (int gg = (G > 1 ? (tid >> 6) : 0); gg < G; gg += 2) {
-          const float x = s_qp[gg][qi], y = s_qp[gg][qi + HALF];
-          const float x2 = fmaf(x, rs.x, y * rs.y), y2 = fmaf(y, rs.x, -x * rs.y);   // apply R(-t)
-          *reinterpret_cast<__half*>(qa + 64 * gg) = __float2half_rn(x2);
-          *reinterpret_cast<__half*>(qa + 64 * gg + 2048) = __float2half_rn(y2);
+          for (int gg = tid >> 6; gg < G; gg += 2) {
+            const float x = s_qp[gg][qi], y = s_qp[gg][qi + HALF];
+            const float x2 = fmaf(x, rs.x, y * rs.y), y2 = fmaf(y, rs.x, -x * rs.y);   // apply R(-t)
+            *reinterpret_cast<__half*>(qa + 64 * gg) = __float2half_rn(x2);
+            *reinterpret_cast<__half*>(qa + 64 * gg + 2048) = __float2half_rn(y2);
+          }
         }
       }
     }
