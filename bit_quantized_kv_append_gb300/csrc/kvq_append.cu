@@ -52,6 +52,13 @@ struct AppendArgs {
 
 __device__ __forceinline__ uint16_t hbits(__half h) { return __half_as_ushort(h); }
 
+// fp32(h) + c, rounded once (the fp16 -> fp32 widening is exact).
+__device__ __forceinline__ float add_h_f(uint16_t h, float c) {
+  float d;
+  asm("add.rn.f32.f16 %0, %1, %2;" : "=f"(d) : "h"(h), "f"(c));
+  return d;
+}
+
 // 1/s to within 1 ulp (hardware approximation); 0 for s = 0. With it the
 // products below are within 4e-6 of the quotients for |y| < 16, inside the
 // tie guard.
@@ -106,7 +113,8 @@ __device__ __forceinline__ uint32_t group_params(float mn, float mx, bool any, f
   return (uint32_t)hbits(sh) | ((uint32_t)hbits(zh) << 16);
 }
 
-// Code-carrying bit patterns (float bits of y + kMagic) -> packed LSB-first words.
+// Code-carrying bit patterns (float bits of y + kMagic: the code in bits 0-3,
+// zeros up to bit 21) -> packed LSB-first words.
 template <int BITS>
 __device__ __forceinline__ void pack_bits(const uint32_t (&mb)[32], uint32_t (&w)[BITS]) {
   constexpr uint32_t M = (1u << BITS) - 1u;
@@ -117,7 +125,7 @@ __device__ __forceinline__ void pack_bits(const uint32_t (&mb)[32], uint32_t (&w
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const uint32_t lo = mb[8 * k + 2 * j], hi = mb[8 * k + 2 * j + 1];
-        byte[j] = (lo & 0xFu) | ((hi & 0xFu) << 4);
+        byte[j] = (lo & 0xFu) + (hi << 4);   // byte 0: two codes (a NaN-marked slot gives 0xF, patched later)
       }
       w[k] = __byte_perm(__byte_perm(byte[0], byte[1], 0x0040u), __byte_perm(byte[2], byte[3], 0x0040u), 0x5410u);
     }
@@ -181,7 +189,6 @@ __device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv,
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int e = 8 * k + 2 * j;
-      const float2 x2 = __half22float2(*reinterpret_cast<const __half2*>(&hw[j]));
       float2 nz2, r2;
       if (KEYS) {
         const float4 kp = sPk[(ch * 32 + e) >> 1];
@@ -191,7 +198,8 @@ __device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv,
         nz2 = make_float2(vp.x, vp.x);
         r2 = make_float2(vp.y, vp.y);
       }
-      const float2 y2 = __fmul2_rn(__fadd2_rn(x2, nz2), r2);
+      const float2 d2 = make_float2(add_h_f((uint16_t)(hw[j] & 0xFFFFu), nz2.x), add_h_f((uint16_t)(hw[j] >> 16), nz2.y));
+      const float2 y2 = __fmul2_rn(d2, r2);
       const float2 m2 = __fadd2_rn(y2, magic2);
       const float2 t2 = __ffma2_rn(__fadd2_rn(m2, nmagic2), neg1, y2);   // y - rint(y)
       tm[k] = fmaxf(tm[k], fmaxf(fabsf(t2.x), fabsf(t2.y)));           // NaN (outlier) ignored
