@@ -514,6 +514,9 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
   float m_frame = -INFINITY, fac = 1.0f;   // s_acc frame of head g; fac = 2^(m_run - m_frame)
   float zacc[4] = {0.f, 0.f, 0.f, 0.f};    // sum_t p z for head g, per 32-channel block
   float2 rr_next = make_float2(1.0f, 0.0f);
+  // R(BK) for pair qi: the next block's rotation is composed from this one,
+  // re-anchored on the exact table every 32 blocks (drift <= 32 roundings)
+  const float2 r_step = (a.rope && q_thread) ? __ldg(a.rope + (kLoOff + (1u << 6) + qi)) : make_float2(1.0f, 0.0f);
   __syncthreads();
   if (u0 < u1) {
     const float2 rr0 = block_rot(u0);
@@ -829,7 +832,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
     if (u + 1 < u1) {
       if (!mbar_wait(smem_addr(&s_bar[nstage]), nphase)) s_abort = 1;
       prep(u + 1, nstage, rr_next);
-      if (u + 2 < u1) rr_next = block_rot(u + 2);
+      if (u + 2 < u1) rr_next = ((u + 2 - u0) & 31) ? rot_compose(rr_next, r_step) : block_rot(u + 2);
     }
     __syncthreads();
     if (s_abort) {
