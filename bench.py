@@ -41,7 +41,8 @@ L2_BYTES = 129 * 2 ** 20
 # counts only if it was captured on these exact files.
 DECODE_SOURCES = {
     128: ["kvq_decode_tc.cuh", "kvq_tc_geom.cuh", "kvq_decode_tc_inst.cuh", "kvq_decode_tc_b4.cu",
-          "kvq_decode_tc_b3.cu", "kvq_decode_tc_b2.cu", "kvq_decode.cuh", "kvq_decode.cu", "kvq_common.cuh"],
+          "kvq_decode_tc_b3.cu", "kvq_decode_tc_b2.cu", "kvq_decode_tc_b4o.cu", "kvq_decode_tc_b3o.cu",
+          "kvq_decode_tc_b2o.cu", "kvq_decode.cuh", "kvq_decode.cu", "kvq_common.cuh"],
     64: ["kvq_decode.cuh", "kvq_decode.cu", "kvq_decode_inst.cuh", "kvq_common.cuh"],
 }
 DECODE_KERNEL = {128: "decode_tc_kernel", 64: "decode_partial_kernel"}

@@ -130,27 +130,27 @@ using TcLaunchFn = cudaError_t (*)(const DecodeArgs&, const tc::StageLayout&, co
                                    const CUtensorMap&, size_t, cudaStream_t);
 using TcOccFn = int (*)(size_t);
 
-template <int BITS, int SL>
+template <int BITS, int SL, bool OUTL>
 void pick_tc_g(int G, TcLaunchFn* f, TcOccFn* o) {
   switch (G) {
-    case 1: *f = launch_tc<BITS, 1, SL>; *o = tc_occupancy<BITS, 1, SL>; break;
-    case 2: *f = launch_tc<BITS, 2, SL>; *o = tc_occupancy<BITS, 2, SL>; break;
-    case 4: *f = launch_tc<BITS, 4, SL>; *o = tc_occupancy<BITS, 4, SL>; break;
-    default: *f = launch_tc<BITS, 8, SL>; *o = tc_occupancy<BITS, 8, SL>; break;
+    case 1: *f = launch_tc<BITS, 1, SL, OUTL>; *o = tc_occupancy<BITS, 1, SL, OUTL>; break;
+    case 2: *f = launch_tc<BITS, 2, SL, OUTL>; *o = tc_occupancy<BITS, 2, SL, OUTL>; break;
+    case 4: *f = launch_tc<BITS, 4, SL, OUTL>; *o = tc_occupancy<BITS, 4, SL, OUTL>; break;
+    default: *f = launch_tc<BITS, 8, SL, OUTL>; *o = tc_occupancy<BITS, 8, SL, OUTL>; break;
   }
 }
 
 template <int BITS>
-void pick_tc(int Bk, int G, TcLaunchFn* f, TcOccFn* o) {
-  if (Bk == 64) pick_tc_g<BITS, 1>(G, f, o);
-  else pick_tc_g<BITS, 2>(G, f, o);
+void pick_tc(int Bk, int G, bool outl, TcLaunchFn* f, TcOccFn* o) {
+  if (Bk == 64) outl ? pick_tc_g<BITS, 1, true>(G, f, o) : pick_tc_g<BITS, 1, false>(G, f, o);
+  else outl ? pick_tc_g<BITS, 2, true>(G, f, o) : pick_tc_g<BITS, 2, false>(G, f, o);
 }
 
-int cached_tc_occupancy(int dev, int bits, int Bk, int G, size_t smem, TcOccFn fn) {
+int cached_tc_occupancy(int dev, int bits, int Bk, int G, bool outl, size_t smem, TcOccFn fn) {
   struct Slot { size_t smem; int occ; };
-  static Slot cache[16][3][2][4];
+  static Slot cache[16][3][2][4][2];
   const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
-  Slot& s = cache[dev & 15][bits - 2][Bk == 128][gi];
+  Slot& s = cache[dev & 15][bits - 2][Bk == 128][gi][outl ? 1 : 0];
   if (s.occ == 0 || s.smem != smem) {
     s.occ = fn(smem);
     s.smem = smem;
@@ -200,11 +200,11 @@ cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, in
     TcLaunchFn fn = nullptr;
     TcOccFn occ_fn = nullptr;
     switch (d.bits) {
-      case 2: pick_tc<2>(d.Bk, G, &fn, &occ_fn); break;
-      case 3: pick_tc<3>(d.Bk, G, &fn, &occ_fn); break;
-      default: pick_tc<4>(d.Bk, G, &fn, &occ_fn); break;
+      case 2: pick_tc<2>(d.Bk, G, d.n_out > 0, &fn, &occ_fn); break;
+      case 3: pick_tc<3>(d.Bk, G, d.n_out > 0, &fn, &occ_fn); break;
+      default: pick_tc<4>(d.Bk, G, d.n_out > 0, &fn, &occ_fn); break;
     }
-    const int occ = cached_tc_occupancy(dev, d.bits, d.Bk, G, smem, occ_fn);
+    const int occ = cached_tc_occupancy(dev, d.bits, d.Bk, G, d.n_out > 0, smem, occ_fn);
     a.n_split = choose_splits(d.B * d.H_kv, units, sms * occ, a.S);
     e = fn(a, L, tk, tv, smem, st);
   } else {

@@ -340,7 +340,9 @@ __device__ __forceinline__ int acc_index(int w, int c, int h) {
 //   q . k:  D[head][token]   = sum_c A(q)[head][c] B(k)[c][token]
 //   P . V:  D[channel][head] = sum_t A(v)[channel][t] B(p*s)[t][head]
 // so the score fragment of a lane is exactly its B operand for P . V.
-template <int BITS, int G, int SL>
+// OUTL: the cache keeps outliers (n_out > 0); without them the outlier code
+// is not compiled in.
+template <int BITS, int G, int SL, bool OUTL>
 __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const DecodeArgs a, const StageLayout L,
                                                              const __grid_constant__ CUtensorMap tm_k,
                                                              const __grid_constant__ CUtensorMap tm_v) {
@@ -371,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
   const int units = a.n_full + (a.tail_len > 0 ? 1 : 0);
   const int u0 = (int)((long long)split * units / a.n_split);
   const int u1 = (int)((long long)(split + 1) * units / a.n_split);
-  const int n_out = d.n_out, ng = d.ng;
+  const int n_out = OUTL ? d.n_out : 0, ng = d.ng;
   const int gv_sh = __ffs(d.Gv) - 1, ng_sh = __ffs(ng) - 1;
   float* ws_base = a.ws + (((size_t)b * a.H_q + hkv * G) * a.S + split) * (kD + 2);
   const LaneOff lo = lane_offsets<BITS>(w, g, r);
@@ -886,10 +888,10 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
 
 }  // namespace tc
 
-template <int BITS, int G, int SL>
+template <int BITS, int G, int SL, bool OUTL>
 cudaError_t launch_tc(const DecodeArgs& a, const tc::StageLayout& L, const CUtensorMap& tk,
                       const CUtensorMap& tv, size_t smem, cudaStream_t st);
-template <int BITS, int G, int SL>
+template <int BITS, int G, int SL, bool OUTL>
 int tc_occupancy(size_t smem);
 
 }  // namespace kvq
