@@ -124,8 +124,14 @@ __device__ __forceinline__ float ex2(float x) {   // 2^x, hardware approximation
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Shared-memory float add without a returned value. Its callers sit between
+// two __syncwarp(), which order it against every other access to the sums.
 __device__ __forceinline__ void red_add(float* p, float v) {
-  asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(smem_addr(p)), "f"(v) : "memory");
+  asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(smem_addr(p)), "f"(v));
+}
+// Small non-negative integer as float without a conversion instruction.
+__device__ __forceinline__ float small_int_f(uint32_t q) {
+  return __int_as_float(0x4B000000 | q) - 8388608.0f;
 }
 __device__ __forceinline__ __half2 as_h2(uint32_t u) {
   __half2 h;
@@ -654,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
             const uint32_t e = ko[row * n_out + oi];
             const int c = (int)(e & (kD - 1));
             const uint32_t m = km[c];
-            const float xd = fmaf((float)tile_code<BITS>(kc, row, c), h2f((uint16_t)(m & 0xFFFFu)),
+            const float xd = fmaf(small_int_f(tile_code<BITS>(kc, row, c)), h2f((uint16_t)(m & 0xFFFFu)),
                                   h2f((uint16_t)(m >> 16)));
             int rr, kq, s;
             kslot<BITS>(c & (HALF - 1), rr, kq, s);
@@ -764,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
               const uint32_t e = vo[row * n_out + oi];
               const int c = (int)(e & (kD - 1));
               const float2 sz = __half22float2(as_h2(vm[(row << ng_sh) + (c >> gv_sh)]));
-              const float delta = h2f((uint16_t)(e >> 16)) - fmaf((float)tile_code<BITS>(vc, row, c), sz.x, sz.y);
+              const float delta = h2f((uint16_t)(e >> 16)) - fmaf(small_int_f(tile_code<BITS>(vc, row, c)), sz.x, sz.y);
               float* accs = reinterpret_cast<float*>(&s_acc[0][0][0][0]);
 #pragma unroll
               for (int h = 0; h < G; ++h) red_add(accs + acc_index<RQ>(w, c, h), s_p[w][h][lane] * delta);
