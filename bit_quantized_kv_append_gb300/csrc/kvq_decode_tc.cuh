@@ -129,6 +129,15 @@ __device__ __forceinline__ float ex2(float x) {   // 2^x, hardware approximation
 __device__ __forceinline__ void red_add(float* p, float v) {
   asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(smem_addr(p)), "f"(v));
 }
+// sin and cos of x in [0, 2^8): two-constant Cody-Waite reduction by 2 pi (the
+// high constant has 8 significant bits, so n * hi is exact for n < 2^16), then
+// the hardware approximations on [-pi, pi].
+__device__ __forceinline__ void sincos_small(float x, float& s, float& c) {
+  const float n = rintf(x * 0.15915494309189535f);
+  float r = fmaf(-n, 6.28125f, x);
+  r = fmaf(-n, 1.9353071795864769e-3f, r);
+  __sincosf(r, &s, &c);
+}
 // Small non-negative integer as float without a conversion instruction.
 __device__ __forceinline__ float small_int_f(uint32_t q) {
   return __int_as_float(0x4B000000 | q) - 8388608.0f;
@@ -367,6 +376,8 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
   __shared__ __align__(16) float4 s_acc[kWarps][8][8][RQ];    // P.V sums in the frame m_frame, fragment order
   __shared__ __align__(16) float4 s_tok[kWarps][16];          // key-outlier staging of one warp
   __shared__ float s_p[kWarps][G][16];                        // p * 2^(m - m_frame) for value outliers
+  __shared__ float s_vd[kWarps][16];                          // value-outlier x_out - x_dense of the warp's tokens
+  __shared__ float s_w[OUTL ? HALF : 1];                      // RoPE frequency of every channel pair
   __shared__ float s_wm[kWarps][G], s_wl[kWarps][G], s_wf[kWarps][G];
   __shared__ float s_z[kWarps][G][4];                         // zero-point sums per 32-channel block
 
@@ -508,6 +519,14 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
     }
     s_qp[gg][i] = x * (2.0f * a.scale_log2);        // doubled: the keys are halved
     s_qp[gg][i + HALF] = y * (2.0f * a.scale_log2);
+  }
+  if (OUTL && tid < HALF) {
+    float wi = 0.0f;                                 // RoPE off: R(j) = identity
+    if (a.rope) {
+      const float2 r1 = rope_fine(a.rope, d, 1, tid);   // (cos w, sin w), 0 < w <= 1
+      wi = atan2f(r1.y, r1.x);
+    }
+    s_w[tid] = wi;
   }
   {
     uint32_t* z = reinterpret_cast<uint32_t*>(&s_qa[0][0][0][0]);
@@ -664,10 +683,8 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
                                   h2f((uint16_t)(m >> 16)));
             int rr, kq, s;
             kslot<BITS>(c & (HALF - 1), rr, kq, s);
-            const uint8_t* rp =
-                reinterpret_cast<const uint8_t*>(rot_tab + rot_frag_index(w, nt_, kq, 4 * n_ + rr)) + slot_byte(s);
-            const float cs = __half2float(__ldg(reinterpret_cast<const __half*>(rp)));
-            const float sn = __half2float(__ldg(reinterpret_cast<const __half*>(rp + 8)));
+            float sn, cs;                                // R(j) of the token's pair, j < 64 in the slice
+            sincos_small((float)(row & 63) * s_w[c & (HALF - 1)], sn, cs);
             const bool first = c < HALF;
             s_tok[w][lane] = make_float4(0.5f * (h2f((uint16_t)(e >> 16)) - xd), first ? cs : -sn, first ? sn : cs,
                                          __int_as_float((kq * 32 + rr) * 16 + aslot_byte(s)));
@@ -763,21 +780,35 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
           }
         }
         __syncwarp();
-        if (lane < 16) {
-          const int row = 64 * sl + 16 * w + 8 * (lane >> 3) + tperm(lane & 7);
-          if (row < ntok) {
-            for (int oi = 0; oi < n_out; ++oi) {
-              const uint32_t e = vo[row * n_out + oi];
-              const int c = (int)(e & (kD - 1));
-              const float2 sz = __half22float2(as_h2(vm[(row << ng_sh) + (c >> gv_sh)]));
-              const float delta = h2f((uint16_t)(e >> 16)) - fmaf(small_int_f(tile_code<BITS>(vc, row, c)), sz.x, sz.y);
-              float* accs = reinterpret_cast<float*>(&s_acc[0][0][0][0]);
-#pragma unroll
-              for (int h = 0; h < G; ++h) red_add(accs + acc_index<RQ>(w, c, h), s_p[w][h][lane] * delta);
-            }
+        // token lanes 0..15; lanes whose outliers share a channel are summed by
+        // the lowest of them, so the shared sums take plain read-add-writes
+        const int row = 64 * sl + 16 * w + 8 * ((lane >> 3) & 1) + tperm(lane & 7);
+        float* accs = reinterpret_cast<float*>(&s_acc[0][0][0][0]);
+        for (int oi = 0; oi < n_out; ++oi) {
+          int c = -1 - lane;                             // never a channel: lanes 16..31, rows past the tail
+          if (lane < 16 && row < ntok) {
+            const uint32_t e = vo[row * n_out + oi];
+            c = (int)(e & (kD - 1));
+            const float2 sz = __half22float2(as_h2(vm[(row << ng_sh) + (c >> gv_sh)]));
+            s_vd[w][lane] = h2f((uint16_t)(e >> 16)) - fmaf(small_int_f(tile_code<BITS>(vc, row, c)), sz.x, sz.y);
           }
+          const uint32_t peers = __match_any_sync(0xffffffffu, c);
+          __syncwarp();
+          if (c >= 0 && (peers & ((1u << lane) - 1u)) == 0u) {
+            float sum[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) sum[h] = 0.0f;
+            for (uint32_t m = peers; m; m &= m - 1u) {
+              const int j = __ffs(m) - 1;
+              const float dj = s_vd[w][j];
+#pragma unroll
+              for (int h = 0; h < G; ++h) sum[h] = fmaf(s_p[w][h][j], dj, sum[h]);
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) accs[acc_index<RQ>(w, c, h)] += sum[h];
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
     }
 
