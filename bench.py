@@ -359,8 +359,7 @@ def run_decode(args, w, rank, world, device):
         qd.copy_(qh, non_blocking=True)
         c = caches[i % n_layers]
         c.reset(T)
-        c.append(kd, vd)
-        c.decode(qd, out=out)
+        c.decode_step(kd, vd, qd, out=out)          # kvq_decode_step: append + attention, one call
         oh.copy_(out, non_blocking=True)
 
     for i in range(args.warmup):
@@ -402,7 +401,8 @@ def run_decode(args, w, rank, world, device):
             "decode_call_ms": dec_mean,
         },
         "e2e": {"value": replica_throughput(w.B * args.steps, world, e2e_ms), "unit": "tokens/s",
-                "h2d_bytes_per_step": bytes_step_in, "d2h_bytes_per_step": bytes_step_out},
+                "h2d_bytes_per_step": bytes_step_in, "d2h_bytes_per_step": bytes_step_out,
+                "call": "kvq_decode_step from pinned host buffers"},
         "gpu_launches": 3 * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,

@@ -61,6 +61,25 @@ bool cache_ptrs_ok(const Dims& d, const kvq_cache& c) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
+// Host checks of kvq_decode_attn for a cache holding T_cur tokens.
+int decode_checks(const kvq_config* cfg, const Dims& d, const kvq_cache* cache, int32_t T_cur,
+                  const void* q, int32_t H_q, int32_t q_pos, const void* rope_tab, float sm_scale,
+                  const void* out, const void* workspace, size_t workspace_bytes) {
+  if (H_q < 1 || H_q % d.H_kv) return KVQ_ERR_UNSUPPORTED;
+  const int G = H_q / d.H_kv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return KVQ_ERR_UNSUPPORTED;
+  if (!cache || !cache_ptrs_ok(d, *cache) || T_cur < 1) return KVQ_ERR_ARG;
+  if (!q || !out || !workspace || !aligned16(q) || !aligned16(out) || !aligned16(workspace))
+    return KVQ_ERR_ARG;
+  if (q_pos < 0 || q_pos >= d.T_max || !isfinite(sm_scale)) return KVQ_ERR_ARG;
+  if (rope_tab && !aligned16(rope_tab)) return KVQ_ERR_ARG;
+  kvq_layout_t lay;
+  const int rc = kvq_layout(cfg, H_q, &lay);
+  if (rc) return rc;
+  if (workspace_bytes < lay.workspace_bytes) return KVQ_ERR_WORKSPACE;
+  return KVQ_OK;
+}
+
 // Scratch of kvq_decode_attn_noalloc: the split partials live in this
 // file-scope device array instead of a caller-provided workspace. Every device
 // that loads the library holds it until the process exits.
@@ -153,22 +172,36 @@ int kvq_decode_attn(const kvq_config* cfg, const kvq_cache* cache, const void* q
   Dims d;
   int rc = make_dims(cfg, &d);
   if (rc) return rc;
-  if (H_q < 1 || H_q % d.H_kv) return KVQ_ERR_UNSUPPORTED;
-  const int G = H_q / d.H_kv;
-  if (G != 1 && G != 2 && G != 4 && G != 8) return KVQ_ERR_UNSUPPORTED;
-  if (!cache || !cache_ptrs_ok(d, *cache) || cache->T_cur < 1) return KVQ_ERR_ARG;
-  if (!q || !out || !workspace || !aligned16(q) || !aligned16(out) || !aligned16(workspace))
-    return KVQ_ERR_ARG;
-  if (q_pos < 0 || q_pos >= d.T_max || !isfinite(sm_scale)) return KVQ_ERR_ARG;
-  if (rope_tab && !aligned16(rope_tab)) return KVQ_ERR_ARG;
-  kvq_layout_t lay;
-  rc = kvq_layout(cfg, H_q, &lay);
+  rc = decode_checks(cfg, d, cache, cache ? cache->T_cur : 0, q, H_q, q_pos, rope_tab, sm_scale, out,
+                     workspace, workspace_bytes);
   if (rc) return rc;
-  if (workspace_bytes < lay.workspace_bytes) return KVQ_ERR_WORKSPACE;
   return cuda_status(launch_decode(d, *cache, static_cast<const __half*>(q), H_q, q_pos,
                                    static_cast<const float2*>(rope_tab), sm_scale,
                                    static_cast<__half*>(out), static_cast<float*>(workspace),
                                    static_cast<cudaStream_t>(stream)));
+}
+
+int kvq_decode_step(const kvq_config* cfg, kvq_cache* cache, const void* k_new, const void* v_new,
+                    const void* q, int32_t H_q, const void* rope_tab, float sm_scale, void* out,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  Dims d;
+  int rc = make_dims(cfg, &d);
+  if (rc) return rc;
+  if (!cache || !cache_ptrs_ok(d, *cache)) return KVQ_ERR_ARG;
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_ARG;
+  if (cache->T_cur + 1 > d.T_max) return KVQ_ERR_CAPACITY;
+  const int32_t pos = cache->T_cur;                  // the new token's position
+  rc = decode_checks(cfg, d, cache, pos + 1, q, H_q, pos, rope_tab, sm_scale, out, workspace,
+                     workspace_bytes);
+  if (rc) return rc;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  rc = cuda_status(launch_append(d, *cache, static_cast<const __half*>(k_new),
+                                 static_cast<const __half*>(v_new), 1, st));
+  if (rc) return rc;
+  cache->T_cur = pos + 1;
+  return cuda_status(launch_decode(d, *cache, static_cast<const __half*>(q), H_q, pos,
+                                   static_cast<const float2*>(rope_tab), sm_scale,
+                                   static_cast<__half*>(out), static_cast<float*>(workspace), st));
 }
 
 int kvq_decode_attn_noalloc(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t H_q,

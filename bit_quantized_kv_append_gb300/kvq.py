@@ -5,7 +5,7 @@ only provides device memory and streams. There is no CPU fallback: if the
 library is missing, the calls raise.
 
 Entry points mirror include/kvq.h: ``layout``, ``rope_init``, ``append``,
-``decode_attn``. ``QuantizedKVCache`` owns one layer's buffers.
+``decode_attn``, ``decode_step``, ``decode_attn_noalloc``. ``QuantizedKVCache`` owns one layer's buffers.
 """
 from __future__ import annotations
 
@@ -20,7 +20,7 @@ import torch
 BUFFERS = ("k_codes", "k_meta", "k_tail", "k_outl", "v_codes", "v_meta", "v_outl")
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "KVQ_ERR_CAPACITY",
           4: "KVQ_ERR_WORKSPACE", 5: "KVQ_ERR_CUDA"}
-EXPORTS = ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_decode_attn",
+EXPORTS = ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_decode_attn", "kvq_decode_step",
            "kvq_decode_attn_noalloc", "kvq_status_string", "kvq_version")
 
 
@@ -66,12 +66,14 @@ def lib():
         L.kvq_append.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp, vp, i32, vp]
         L.kvq_decode_attn.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp, i32, i32,
                                       vp, ctypes.c_float, vp, vp, ctypes.c_size_t, vp]
+        L.kvq_decode_step.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp, vp, vp, i32,
+                                      vp, ctypes.c_float, vp, vp, ctypes.c_size_t, vp]
         L.kvq_decode_attn_noalloc.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp,
                                               i32, i32, vp, ctypes.c_float, vp, vp]
         L.kvq_status_string.argtypes = [ctypes.c_int]
         L.kvq_status_string.restype = ctypes.c_char_p
         L.kvq_version.restype = ctypes.c_char_p
-        for fn in ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_decode_attn",
+        for fn in ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_decode_attn", "kvq_decode_step",
                    "kvq_decode_attn_noalloc"):
             getattr(L, fn).restype = ctypes.c_int
         _LIB = L
@@ -126,6 +128,17 @@ def decode_attn(cfg: Config, ref: CacheRef, q: torch.Tensor, H_q: int, q_pos: in
     _check(lib().kvq_decode_attn(ctypes.byref(cfg), ctypes.byref(ref), _ptr(q), int(H_q), int(q_pos),
                                  _ptr(rope), float(sm_scale), _ptr(out), _ptr(workspace),
                                  workspace.numel(), _stream(stream)), "kvq_decode_attn")
+
+
+def decode_step(cfg: Config, ref: CacheRef, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor,
+                H_q: int, rope: Optional[torch.Tensor], sm_scale: float, out: torch.Tensor,
+                workspace: torch.Tensor, stream=None):
+    """kvq_decode_step: append one token per sequence, then decode attention
+    of q at the new token's position over every cached token (ref.T_cur
+    advances by one on success)."""
+    _check(lib().kvq_decode_step(ctypes.byref(cfg), ctypes.byref(ref), _ptr(k_new), _ptr(v_new), _ptr(q),
+                                 int(H_q), _ptr(rope), float(sm_scale), _ptr(out), _ptr(workspace),
+                                 workspace.numel(), _stream(stream)), "kvq_decode_step")
 
 
 def decode_attn_noalloc(cfg: Config, ref: CacheRef, q: torch.Tensor, H_q: int, q_pos: int,
@@ -219,4 +232,28 @@ class QuantizedKVCache:
         sm_scale = 1.0 / math.sqrt(c.D) if sm_scale is None else sm_scale
         decode_attn(self.cfg, self.ref(), q, self.H_q, q_pos, self.rope, sm_scale, out,
                     self.workspace, stream)
+        return out
+
+    def decode_step(self, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor,
+                    sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                    stream=None) -> torch.Tensor:
+        """One decode step: store the new token (k_new, v_new: fp16 [B, H_kv, 1, D],
+        pre-RoPE key) at position T_cur and attend q (fp16 [B, H_q, D], pre-RoPE,
+        at that position) over all T_cur + 1 tokens."""
+        c = self.cfg
+        for t in (k_new, v_new):
+            if t.dtype != torch.float16 or not t.is_contiguous() or t.device != self.device:
+                raise ValueError("k_new/v_new must be contiguous fp16 tensors on the cache device")
+            if tuple(t.shape) != (c.B, c.H_kv, 1, c.D):
+                raise ValueError(f"expected [B={c.B}, H_kv={c.H_kv}, 1, D={c.D}], got {tuple(t.shape)}")
+        if q.dtype != torch.float16 or not q.is_contiguous() or q.device != self.device:
+            raise ValueError("q must be a contiguous fp16 tensor on the cache device")
+        if tuple(q.shape) != (c.B, self.H_q, c.D):
+            raise ValueError(f"expected q [B={c.B}, H_q={self.H_q}, D={c.D}], got {tuple(q.shape)}")
+        if out is None:
+            out = torch.empty_like(q)
+        sm_scale = 1.0 / math.sqrt(c.D) if sm_scale is None else sm_scale
+        ref = self.ref()
+        decode_step(self.cfg, ref, k_new, v_new, q, self.H_q, self.rope, sm_scale, out, self.workspace, stream)
+        self.T_cur = ref.T_cur
         return out

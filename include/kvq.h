@@ -167,6 +167,30 @@ KVQ_API int kvq_decode_attn(const kvq_config* cfg, const kvq_cache* cache, const
                     int32_t q_pos, const void* rope_tab, float sm_scale, void* out,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+/* One decode step of one layer in a single stream-ordered call: append the
+ * new token of every sequence, then attend its query over all cached tokens
+ * including the new one (the serving workflow of mlqm.cn/news/1064729, §3.2
+ * and §4.2: a token is quantized as it arrives, a key block once its last
+ * token has arrived).
+ *   k_new, v_new: fp16 [B][H_kv][1][D], the new token's pre-RoPE key and
+ *                 value, stored at position T_cur exactly as kvq_append stores
+ *                 it (the value quantized at once; the key kept fp16 in K_TAIL
+ *                 until it completes its block, which is then quantized);
+ *   q:            fp16 [B][H_q][D], pre-RoPE, at position T_cur (the new token);
+ *   out:          fp16 [B][H_q][D], attention over positions 0 .. T_cur.
+ * The other arguments are those of kvq_decode_attn. The result and the cache
+ * are bit-identical to kvq_append(n_new = 1) followed by kvq_decode_attn with
+ * q_pos = T_cur on the same stream, which is what this call enqueues (two or
+ * three kernels, no synchronization). On success cache->T_cur += 1.
+ * Errors: every check of both operations runs before the first launch:
+ * KVQ_ERR_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CAPACITY (T_cur = T_max),
+ * KVQ_ERR_WORKSPACE; then nothing is launched and nothing changes.
+ * KVQ_ERR_CUDA from the append launch leaves T_cur unchanged; from the
+ * attention launch the append is already enqueued, so T_cur has advanced. */
+KVQ_API int kvq_decode_step(const kvq_config* cfg, kvq_cache* cache, const void* k_new, const void* v_new,
+                            const void* q, int32_t H_q, const void* rope_tab, float sm_scale, void* out,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
 /* kvq_decode_attn without a workspace argument, for callers that cannot
  * allocate device memory on the decode path: for example a serving engine
  * that reserves all device memory at start-up and forbids later cudaMalloc

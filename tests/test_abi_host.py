@@ -163,3 +163,32 @@ def test_rope_init_host_errors(lib):
     assert lib.kvq_rope_init(ctypes.byref(cfg), 1e4, p, lay.rope_bytes - 8, None) == 4
     assert lib.kvq_rope_init(ctypes.byref(cfg), 0.0, p, lay.rope_bytes, None) == 1
     assert lib.kvq_rope_init(ctypes.byref(cfg), 1e4, None, lay.rope_bytes, None) == 1
+
+
+def test_decode_step_host_errors(lib):
+    cfg = _cfg()
+    lay = kvq.layout(cfg, 8)
+    p = ctypes.c_void_p(FAKE)
+    ws = lay.workspace_bytes
+    r = _fake_cache(100)
+
+    def call(cache=r, k=p, v=p, q=p, H_q=8, rope=None, scale=0.1, out=p, w=p, wsb=ws, c=cfg):
+        return lib.kvq_decode_step(ctypes.byref(c), None if cache is None else ctypes.byref(cache), k, v, q,
+                                   H_q, rope, scale, out, w, wsb, None)
+
+    full = _fake_cache(256)
+    assert call(cache=full) == 3 and full.T_cur == 256      # no room for the new token
+    assert call(wsb=ws - 1) == 4
+    assert call(H_q=6) == 2
+    assert call(c=_cfg(bits=7)) == 2
+    assert call(cache=None) == 1
+    assert call(k=None) == 1
+    assert call(v=ctypes.c_void_p(FAKE + 8)) == 1
+    assert call(q=None) == 1
+    assert call(out=ctypes.c_void_p(FAKE + 2)) == 1
+    assert call(w=None) == 1
+    assert call(rope=ctypes.c_void_p(FAKE + 8)) == 1
+    assert call(scale=float("nan")) == 1
+    no_outl = _fake_cache(10, n_out=0)
+    assert call(cache=no_outl) == 1                          # n_out = 1 needs the outlier buffers
+    assert r.T_cur == 100                                    # nothing changed on any error
