@@ -43,6 +43,9 @@ DECODE_SOURCES = {
     128: ["kvq_decode_tc.cuh", "kvq_tc_geom.cuh", "kvq_decode_tc_inst.cuh", "kvq_decode_tc_b4.cu",
           "kvq_decode_tc_b3.cu", "kvq_decode_tc_b2.cu", "kvq_decode_tc_b4o.cu", "kvq_decode_tc_b3o.cu",
           "kvq_decode_tc_b2o.cu", "kvq_decode.cuh", "kvq_decode.cu", "kvq_common.cuh"],
+    "paged": ["kvq_decode_tc.cuh", "kvq_tc_geom.cuh", "kvq_decode_tc_inst.cuh", "kvq_decode_tc_b4p.cu",
+              "kvq_decode_tc_b3p.cu", "kvq_decode_tc_b2p.cu", "kvq_decode_tc_b4op.cu", "kvq_decode_tc_b3op.cu",
+              "kvq_decode_tc_b2op.cu", "kvq_decode.cuh", "kvq_decode.cu", "kvq_common.cuh"],
     64: ["kvq_decode.cuh", "kvq_decode.cu", "kvq_decode_inst.cuh", "kvq_common.cuh"],
 }
 DECODE_KERNEL = {128: "decode_tc_kernel", 64: "decode_partial_kernel"}

@@ -3,8 +3,10 @@
 The work runs in ``libkvq.so`` (hand-written sm_103a CUDA kernels behind the C
 ABI of ``include/kvq.h``); this package only builds and binds it.
 """
-from .kvq import (BUFFERS, EXPORTS, CacheRef, Config, KvqError, Layout, QuantizedKVCache, append,
-                  decode_attn, decode_attn_noalloc, layout, lib, make_config, rope_init)
+from .kvq import (BUFFERS, EXPORTS, CacheRef, Config, KvqError, Layout, PagedCacheRef, PagedKVCache,
+                  QuantizedKVCache, append, decode_attn, decode_attn_noalloc, decode_step, layout, lib,
+                  make_config, paged_append, paged_decode_attn, paged_layout, rope_init)
 
-__all__ = ["BUFFERS", "EXPORTS", "CacheRef", "Config", "KvqError", "Layout", "QuantizedKVCache",
-           "append", "decode_attn", "decode_attn_noalloc", "layout", "lib", "make_config", "rope_init"]
+__all__ = ["BUFFERS", "EXPORTS", "CacheRef", "Config", "KvqError", "Layout", "PagedCacheRef", "PagedKVCache",
+           "QuantizedKVCache", "append", "decode_attn", "decode_attn_noalloc", "decode_step", "layout", "lib",
+           "make_config", "paged_append", "paged_decode_attn", "paged_layout", "rope_init"]

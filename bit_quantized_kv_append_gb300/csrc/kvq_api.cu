@@ -61,6 +61,45 @@ bool cache_ptrs_ok(const Dims& d, const kvq_cache& c) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Pools, table and lengths of a paged cache; the block count keeps every
+// block index a valid 32-bit TMA coordinate.
+bool paged_ptrs_ok(const Dims& d, const kvq_paged_cache& c) {
+  const void* must[] = {c.k_codes, c.k_meta, c.k_tail, c.v_codes, c.v_meta};
+  for (const void* p : must)
+    if (!p || !aligned16(p)) return false;
+  if (d.n_out > 0) {
+    if (!c.k_outl || !c.v_outl || !aligned16(c.k_outl) || !aligned16(c.v_outl)) return false;
+  }
+  if (!c.block_table || !c.seq_len || !aligned4(c.block_table) || !aligned4(c.seq_len)) return false;
+  if (c.n_blocks < 1 || (int64_t)c.n_blocks * d.H_kv >= ((int64_t)1 << 31)) return false;
+  return c.max_len >= 0 && c.max_len <= d.T_max;
+}
+
+// The pools as the kernels' buffer set, and the paging information.
+kvq_cache pool_view(const kvq_paged_cache& c) {
+  kvq_cache v;
+  v.k_codes = c.k_codes;
+  v.k_meta = c.k_meta;
+  v.k_tail = c.k_tail;
+  v.k_outl = c.k_outl;
+  v.v_codes = c.v_codes;
+  v.v_meta = c.v_meta;
+  v.v_outl = c.v_outl;
+  v.T_cur = 0;
+  return v;
+}
+Paged paging(const Dims& d, const kvq_paged_cache& c) {
+  Paged pg;
+  pg.block_table = c.block_table;
+  pg.seq_len = c.seq_len;
+  pg.max_blocks = d.n_blk;
+  pg.n_blocks = c.n_blocks;
+  pg.max_len = c.max_len;
+  return pg;
+}
+
 // Host checks of kvq_decode_attn for a cache holding T_cur tokens.
 int decode_checks(const kvq_config* cfg, const Dims& d, const kvq_cache* cache, int32_t T_cur,
                   const void* q, int32_t H_q, int32_t q_pos, const void* rope_tab, float sm_scale,
@@ -228,6 +267,77 @@ int kvq_decode_attn_noalloc(const kvq_config* cfg, const kvq_cache* cache, const
                                    static_cast<const float2*>(rope_tab), sm_scale,
                                    static_cast<__half*>(out), scratch,
                                    static_cast<cudaStream_t>(stream), fit > 256 ? 256 : (int)fit));
+}
+
+int kvq_paged_layout(const kvq_config* cfg, int32_t n_blocks, int32_t H_q, kvq_layout_t* out) {
+  if (!cfg || !out) return KVQ_ERR_ARG;
+  Dims d;
+  int rc = make_dims(cfg, &d);
+  if (rc) return rc;
+  if (H_q < 1 || H_q % d.H_kv) return KVQ_ERR_UNSUPPORTED;
+  if (n_blocks < 1 || (int64_t)n_blocks * d.H_kv >= ((int64_t)1 << 31)) return KVQ_ERR_UNSUPPORTED;
+  kvq_layout_t base;
+  rc = kvq_layout(cfg, H_q, &base);
+  if (rc) return rc;
+  memset(out, 0, sizeof(*out));
+  const size_t rows = (size_t)d.H_kv * d.Bk;      // rows of one physical block, all heads
+  out->stream_bytes[KVQ_K_CODES] = rows * d.cb;
+  out->stream_bytes[KVQ_K_META] = (size_t)d.H_kv * d.D * 4;
+  out->stream_bytes[KVQ_K_TAIL] = k_tail_stream(d) * 2 * d.H_kv;   // per sequence
+  out->stream_bytes[KVQ_K_OUTL] = rows * d.n_out * 4;
+  out->stream_bytes[KVQ_V_CODES] = rows * d.cb;
+  out->stream_bytes[KVQ_V_META] = rows * d.ng * 4;
+  out->stream_bytes[KVQ_V_OUTL] = rows * d.n_out * 4;
+  for (int i = 0; i < KVQ_NBUF; ++i) {
+    out->bytes[i] = out->stream_bytes[i] * (i == KVQ_K_TAIL ? (size_t)d.B : (size_t)n_blocks);
+    out->cache_bytes += out->bytes[i];
+  }
+  out->fp16_equiv_bytes = 2 * (size_t)n_blocks * rows * d.D * 2;
+  out->rope_bytes = base.rope_bytes;
+  out->workspace_bytes = base.workspace_bytes;
+  out->n_out = d.n_out;
+  out->code_row_bytes = d.cb;
+  return KVQ_OK;
+}
+
+int kvq_paged_append(const kvq_config* cfg, kvq_paged_cache* cache, const void* k_new, const void* v_new,
+                     int32_t n_new, void* stream) {
+  Dims d;
+  int rc = make_dims(cfg, &d);
+  if (rc) return rc;
+  if (!cache || n_new < 0 || !paged_ptrs_ok(d, *cache)) return KVQ_ERR_ARG;
+  if (n_new == 0) return KVQ_OK;
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_ARG;
+  if ((int64_t)cache->max_len + n_new > d.T_max) return KVQ_ERR_CAPACITY;
+  const Paged pg = paging(d, *cache);
+  rc = cuda_status(launch_append(d, pool_view(*cache), static_cast<const __half*>(k_new),
+                                 static_cast<const __half*>(v_new), n_new, static_cast<cudaStream_t>(stream), &pg));
+  if (rc == KVQ_OK) cache->max_len += n_new;
+  return rc;
+}
+
+int kvq_paged_decode_attn(const kvq_config* cfg, const kvq_paged_cache* cache, const void* q, int32_t H_q,
+                          const void* rope_tab, float sm_scale, void* out, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  Dims d;
+  int rc = make_dims(cfg, &d);
+  if (rc) return rc;
+  if (H_q < 1 || H_q % d.H_kv) return KVQ_ERR_UNSUPPORTED;
+  const int G = H_q / d.H_kv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return KVQ_ERR_UNSUPPORTED;
+  if (!cache || !paged_ptrs_ok(d, *cache)) return KVQ_ERR_ARG;
+  if (!q || !out || !workspace || !aligned16(q) || !aligned16(out) || !aligned16(workspace))
+    return KVQ_ERR_ARG;
+  if (!isfinite(sm_scale)) return KVQ_ERR_ARG;
+  if (rope_tab && !aligned16(rope_tab)) return KVQ_ERR_ARG;
+  kvq_layout_t lay;
+  rc = kvq_layout(cfg, H_q, &lay);
+  if (rc) return rc;
+  if (workspace_bytes < lay.workspace_bytes) return KVQ_ERR_WORKSPACE;
+  const Paged pg = paging(d, *cache);
+  return cuda_status(launch_decode(d, pool_view(*cache), static_cast<const __half*>(q), H_q, 0,
+                                   static_cast<const float2*>(rope_tab), sm_scale, static_cast<__half*>(out),
+                                   static_cast<float*>(workspace), static_cast<cudaStream_t>(stream), 0, &pg));
 }
 
 const char* kvq_status_string(int status) {

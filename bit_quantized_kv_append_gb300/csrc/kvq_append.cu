@@ -48,7 +48,22 @@ struct AppendArgs {
   const __half* v_new;
   int T_cur, n_new, first_blk;
   int tail_in_kernel;  // 1: an unfinished last block's keys go to K_TAIL in this launch
+  const int32_t* block_table;  // paged cache (NULL: contiguous streams); then the
+  const int32_t* seq_len;      // position, first block and tail rule are per sequence
+  int max_blocks, n_blocks;
 };
+
+// Paged append: position of sequence b (its length, kept inside the capacity).
+__device__ __forceinline__ int paged_pos(const AppendArgs& a, int b) {
+  const int t = __ldg(a.seq_len + b), hi = a.d.T_max - a.n_new;
+  return t < 0 ? 0 : (t > hi ? hi : t);
+}
+// An append whose first block reads the old tail and whose last block is
+// unfinished and different writes that last block's keys in a second launch.
+__device__ __host__ __forceinline__ bool tail_deferred(int T_cur, int n_new, int Bk) {
+  const int first = T_cur / Bk, last = (T_cur + n_new - 1) / Bk;
+  return ((T_cur + n_new) % Bk) != 0 && first != last && (T_cur % Bk) != 0;
+}
 
 __device__ __forceinline__ uint16_t hbits(__half h) { return __half_as_ushort(h); }
 
@@ -245,11 +260,22 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   const int Bk = d.Bk, n_out = d.n_out;
   const int tid = threadIdx.x;
   const int bh = blockIdx.y;
+  const int b = bh / d.H_kv, h = bh - b * d.H_kv;
   const bool isK = blockIdx.z != 0;
-  const int blk = a.first_blk + blockIdx.x;
+  int T_cur = a.T_cur, first_blk = a.first_blk, tail_in_kernel = a.tail_in_kernel;
+  if (a.block_table) {
+    T_cur = paged_pos(a, b);
+    first_blk = T_cur / Bk;
+    if (first_blk + (int)blockIdx.x > (T_cur + a.n_new - 1) / Bk) return;   // this sequence touches fewer blocks
+    tail_in_kernel = tail_deferred(T_cur, a.n_new, Bk) ? 0 : 1;
+  }
+  const int blk = first_blk + blockIdx.x;
   const int t_blk0 = blk * Bk;
-  const int t_end = a.T_cur + a.n_new;
-  const int t_lo = max(t_blk0, a.T_cur);
+  // rows of this block in the code / value-metadata / outlier buffers: row_base + t
+  const size_t kblk = unit_block(d, a.block_table, a.max_blocks, a.n_blocks, b, h, blk);
+  const long long row_base = (long long)(kblk * Bk) - (long long)t_blk0;
+  const int t_end = T_cur + a.n_new;
+  const int t_lo = max(t_blk0, T_cur);
   const int t_hi = min(t_blk0 + Bk, t_end);
   const int nv = t_hi - t_lo;                      // new tokens in this block, >= 1
   const bool complete = t_blk0 + Bk <= t_end;
@@ -259,12 +285,12 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
 
   if (isK && !complete) {
     // unfinished block: keep the new keys as fp16 rows t % Bk of the tail
-    if (a.tail_in_kernel) {
+    if (tail_in_kernel) {
       for (int i = tid; i < nv * vpr; i += kThreads) {
         const int r = i / vpr, c = i % vpr;
         const int t = t_lo + r;
         reinterpret_cast<uint4*>(tail + (size_t)(t - t_blk0) * D)[c] = __ldg(
-            reinterpret_cast<const uint4*>(a.k_new + ((size_t)bh * a.n_new + (t - a.T_cur)) * D) + c);
+            reinterpret_cast<const uint4*>(a.k_new + ((size_t)bh * a.n_new + (t - T_cur)) * D) + c);
       }
     }
     return;
@@ -290,9 +316,9 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
       const int i = tid + k * kThreads, r = i / vpr, c = i % vpr;
       if (r < rows) {
         const int t = t_row0 + r;
-        const __half* src = isK ? ((t < a.T_cur) ? tail + (size_t)r * D
-                                                 : a.k_new + ((size_t)bh * a.n_new + (t - a.T_cur)) * D)
-                                : a.v_new + ((size_t)bh * a.n_new + (t - a.T_cur)) * D;
+        const __half* src = isK ? ((t < T_cur) ? tail + (size_t)r * D
+                                               : a.k_new + ((size_t)bh * a.n_new + (t - T_cur)) * D)
+                                : a.v_new + ((size_t)bh * a.n_new + (t - T_cur)) * D;
         v[k] = __ldg(reinterpret_cast<const uint4*>(src) + c);
       }
     }
@@ -305,7 +331,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   __syncthreads();
 
   // ---- B. dense-and-sparse split: per row, the n_out largest |x|
-  uint32_t* gout_base = (isK ? a.k_outl : a.v_outl) + ((size_t)bh * d.T_max + t_row0) * n_out;
+  uint32_t* gout_base = (isK ? a.k_outl : a.v_outl) + (size_t)(row_base + t_row0) * n_out;
   const __half nanh = __ushort_as_half((uint16_t)0x7E00u);   // marks outliers for step C
   if (n_out == 1 && D == 128) {
     // two threads per row, 64 channels each: the largest |x| (fp16 max), then
@@ -420,7 +446,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
       const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
       float2 sz;
       const uint32_t packed = group_params(mn, mx, !isnan(mn), Lf, &sz);
-      a.v_meta[((size_t)bh * d.T_max + (t_row0 + r)) * ng + g] = packed;
+      a.v_meta[(size_t)(row_base + t_row0 + r) * ng + g] = packed;
       sPv[g * Bk + r] = make_float4(-sz.y, rcp_or_zero(sz.x), sz.x, 0.0f);
     }
   } else {
@@ -447,7 +473,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
       }
       float2 sz;
       const uint32_t packed = group_params(mn, mx, !isnan(mn), Lf, &sz);
-      a.k_meta[((size_t)bh * d.n_blk + blk) * D + c] = packed;
+      a.k_meta[kblk * D + c] = packed;
       float* pk = reinterpret_cast<float*>(&sPk[cp]);
       pk[hc] = -sz.y;
       pk[2 + hc] = rcp_or_zero(sz.x);
@@ -495,7 +521,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
         chunk_codes<BITS, true>(sX, sPv, sPk, sS, sO, sQ, D, Bk, r, ch, 0, n_out, w);
       else
         chunk_codes<BITS, false>(sX, sPv, sPk, sS, sO, sQ, D, Bk, r, ch, (ch * 32) >> gv_sh, n_out, w);
-      uint32_t* dst = reinterpret_cast<uint32_t*>(base + ((size_t)bh * d.T_max + (t_row0 + r)) * d.cb) + ch * BITS;
+      uint32_t* dst = reinterpret_cast<uint32_t*>(base + (size_t)(row_base + t_row0 + r) * d.cb) + ch * BITS;
       if constexpr (BITS == 4) {
         *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
       } else if constexpr (BITS == 2) {
@@ -510,9 +536,16 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
 
 // Keys of the last, unfinished block of a multi-block append whose first block
 // read the old tail: written after the main launch so the two never overlap.
-__global__ void tail_copy_kernel(__half* __restrict__ k_tail, const __half* __restrict__ k_new,
+// Paged (a.seq_len set): each sequence decides from its own position.
+__global__ void tail_copy_kernel(const AppendArgs a, __half* __restrict__ k_tail, const __half* __restrict__ k_new,
                                  int Bk, int D, int n_new, int T_cur, int t_from, int t_to) {
   const int bh = blockIdx.y;
+  if (a.seq_len) {
+    T_cur = paged_pos(a, bh / a.d.H_kv);
+    if (!tail_deferred(T_cur, n_new, Bk)) return;
+    t_to = T_cur + n_new;
+    t_from = (t_to - 1) / Bk * Bk;
+  }
   const int vpr = D / 8;
   const int n = (t_to - t_from) * vpr;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
@@ -548,14 +581,16 @@ cudaError_t launch_bits(const AppendArgs& a, dim3 grid, size_t smem, cudaStream_
 
 }  // namespace
 
-cudaError_t launch_append(const Dims& d, const kvq_cache& c, const __half* k_new,
-                          const __half* v_new, int n_new, cudaStream_t st) {
-  const int T_cur = c.T_cur, t_end = T_cur + n_new;
-  const int first = T_cur / d.Bk, last = (t_end - 1) / d.Bk;
-  const bool last_unfinished = (t_end % d.Bk) != 0;
-  const bool first_reads_tail = (T_cur % d.Bk) != 0;
-  const bool defer_tail = last_unfinished && first != last && first_reads_tail;
+// Paged append: every sequence's length grows by n_new once its tokens are stored.
+__global__ void seq_len_advance_kernel(int32_t* seq_len, int B, int n_new, int T_max) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int t = seq_len[b], hi = T_max - n_new;
+  seq_len[b] = (t < 0 ? 0 : (t > hi ? hi : t)) + n_new;   // the position the append used, advanced
+}
 
+cudaError_t launch_append(const Dims& d, const kvq_cache& c, const __half* k_new,
+                          const __half* v_new, int n_new, cudaStream_t st, const Paged* pg) {
   AppendArgs a;
   a.d = d;
   a.k_codes = static_cast<uint8_t*>(c.k_codes);
@@ -567,12 +602,36 @@ cudaError_t launch_append(const Dims& d, const kvq_cache& c, const __half* k_new
   a.v_outl = static_cast<uint32_t*>(c.v_outl);
   a.k_new = k_new;
   a.v_new = v_new;
-  a.T_cur = T_cur;
   a.n_new = n_new;
-  a.first_blk = first;
-  a.tail_in_kernel = defer_tail ? 0 : 1;
+  a.block_table = pg ? pg->block_table : nullptr;
+  a.seq_len = pg ? pg->seq_len : nullptr;
+  a.max_blocks = pg ? pg->max_blocks : 0;
+  a.n_blocks = pg ? pg->n_blocks : 0;
 
-  const dim3 grid(last - first + 1, d.B * d.H_kv, 2);
+  int blocks_x;
+  bool defer_tail;
+  int t_from = 0, t_end = 0;
+  if (pg) {
+    // positions are per sequence on the device: size the grid for the most
+    // blocks n_new tokens can touch; the kernels read their own positions
+    a.T_cur = 0;
+    a.first_blk = 0;
+    a.tail_in_kernel = 1;
+    blocks_x = (n_new + d.Bk - 2) / d.Bk + 1;
+    defer_tail = n_new > 1;
+  } else {
+    const int T_cur = c.T_cur;
+    t_end = T_cur + n_new;
+    const int first = T_cur / d.Bk, last = (t_end - 1) / d.Bk;
+    defer_tail = tail_deferred(T_cur, n_new, d.Bk);
+    a.T_cur = T_cur;
+    a.first_blk = first;
+    a.tail_in_kernel = defer_tail ? 0 : 1;
+    blocks_x = last - first + 1;
+    t_from = last * d.Bk;
+  }
+
+  const dim3 grid(blocks_x, d.B * d.H_kv, 2);
   const size_t smem = append_smem(d);
   cudaError_t e;
   switch (d.bits) {
@@ -580,12 +639,20 @@ cudaError_t launch_append(const Dims& d, const kvq_cache& c, const __half* k_new
     case 3: e = launch_bits<3>(a, grid, smem, st); break;
     default: e = launch_bits<4>(a, grid, smem, st); break;
   }
-  if (e != cudaSuccess || !defer_tail) return e;
-  const int rows = t_end - last * d.Bk;
-  const int blocks = (rows * (d.D / 8) + 255) / 256;
-  tail_copy_kernel<<<dim3(blocks, d.B * d.H_kv), 256, 0, st>>>(
-      static_cast<__half*>(c.k_tail), k_new, d.Bk, d.D, n_new, T_cur, last * d.Bk, t_end);
-  return cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (defer_tail) {
+    const int rows = pg ? d.Bk - 1 : t_end - t_from;   // paged: at most Bk - 1 unfinished rows
+    const int blocks = (rows * (d.D / 8) + 255) / 256;
+    tail_copy_kernel<<<dim3(blocks, d.B * d.H_kv), 256, 0, st>>>(a, static_cast<__half*>(c.k_tail), k_new, d.Bk,
+                                                                 d.D, n_new, a.T_cur, t_from, t_end);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (pg) {
+    seq_len_advance_kernel<<<(d.B + 255) / 256, 256, 0, st>>>(pg->seq_len, d.B, n_new, d.T_max);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 }  // namespace kvq

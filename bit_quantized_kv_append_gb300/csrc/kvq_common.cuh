@@ -63,13 +63,41 @@ __device__ __forceinline__ float2 rot_compose(float2 a, float2 b) {
                      __fadd_rn(__fmul_rn(a.y, b.x), __fmul_rn(a.x, b.y)));
 }
 
+// Paged cache: physical key blocks of Bk tokens shared by the sequences
+// through a block table, and per-sequence lengths on the device.
+// block_table == nullptr selects the contiguous per-stream layout.
+struct Paged {
+  const int32_t* block_table = nullptr;  // [B][max_blocks]
+  int32_t* seq_len = nullptr;            // [B]
+  int max_blocks = 0;                    // T_max / Bk
+  int n_blocks = 0;                      // physical blocks in the pools
+  int max_len = 0;                       // host upper bound of every seq_len[b]
+};
+
+// Block index of key block u of stream (b, h) in the code, metadata and
+// outlier buffers, seen as [block][Bk rows] (key metadata: [block][D]).
+// Contiguous: (b H_kv + h) n_blk + u; paged: block_table[b][u] H_kv + h, a
+// table entry outside [0, n_blocks) clamped so that every access stays inside
+// the pools.
+__device__ __forceinline__ size_t unit_block(const Dims& d, const int32_t* table, int max_blocks, int n_blocks,
+                                             int b, int h, int u) {
+  if (table) {
+    int p = __ldg(table + (size_t)b * max_blocks + u);
+    p = p < 0 ? 0 : (p >= n_blocks ? n_blocks - 1 : p);
+    return (size_t)p * d.H_kv + h;
+  }
+  return ((size_t)b * d.H_kv + h) * d.n_blk + u;
+}
+
 // Launch helpers (defined in the kernel translation units).
 cudaError_t launch_rope_init(const Dims& d, double theta, float2* tab, cudaStream_t st);
+// pg: a paged cache (positions from pg->seq_len, advanced by n_new after the append).
 cudaError_t launch_append(const Dims& d, const kvq_cache& c, const __half* k_new,
-                          const __half* v_new, int n_new, cudaStream_t st);
+                          const __half* v_new, int n_new, cudaStream_t st, const Paged* pg = nullptr);
 // split_cap > 0 bounds the T splits (and the workspace stride) below max_splits().
+// pg: a paged cache (per-sequence lengths; q of sequence b at seq_len[b] - 1).
 cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, int H_q, int q_pos,
                           const float2* rope, float sm_scale, __half* out, float* ws,
-                          cudaStream_t st, int split_cap = 0);
+                          cudaStream_t st, int split_cap = 0, const Paged* pg = nullptr);
 
 }  // namespace kvq

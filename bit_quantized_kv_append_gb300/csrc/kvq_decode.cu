@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restri
     L = fmaf(w, ps[D + 1], L);
     acc = fmaf(w, ps[c], acc);
   }
-  out[(size_t)bhq * D + c] = __float2half_rn(acc / L);
+  out[(size_t)bhq * D + c] = __float2half_rn(L > 0.0f ? acc / L : 0.0f);   // a sequence without tokens: 0
 }
 
 using LaunchFn = cudaError_t (*)(const DecodeArgs&, cudaStream_t);
@@ -90,13 +90,16 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D map over a packed code buffer: [stream][token][row byte], box = one key
-// block of rows; INT4 rows (64 B) get the 64 B swizzle, INT2 rows (32 B) 32 B.
-bool encode_codes(CUtensorMap* m, const void* base, const Dims& d) {
+// 3-D map over a packed code buffer: [stream][T_max rows][row byte]
+// (contiguous cache) or [physical block x H_kv][Bk rows][row byte] (paged
+// pools, `pool_units` > 0); box = one key block. INT4 rows (64 B) get the
+// 64 B swizzle, INT2 rows (32 B) 32 B.
+bool encode_codes(CUtensorMap* m, const void* base, const Dims& d, size_t pool_units) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)d.cb, (cuuint64_t)d.T_max, (cuuint64_t)d.B * d.H_kv};
-  const cuuint64_t strides[2] = {(cuuint64_t)d.cb, (cuuint64_t)d.T_max * d.cb};
+  const cuuint64_t rows = pool_units ? (cuuint64_t)d.Bk : (cuuint64_t)d.T_max;
+  const cuuint64_t dims[3] = {(cuuint64_t)d.cb, rows, pool_units ? (cuuint64_t)pool_units : (cuuint64_t)d.B * d.H_kv};
+  const cuuint64_t strides[2] = {(cuuint64_t)d.cb, rows * d.cb};
   const cuuint32_t box[3] = {(cuuint32_t)d.cb, (cuuint32_t)d.Bk, 1};
   const cuuint32_t es[3] = {1, 1, 1};
   const CUtensorMapSwizzle sw = d.bits == 4   ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -130,27 +133,31 @@ using TcLaunchFn = cudaError_t (*)(const DecodeArgs&, const tc::StageLayout&, co
                                    const CUtensorMap&, size_t, cudaStream_t);
 using TcOccFn = int (*)(size_t);
 
-template <int BITS, int SL, bool OUTL>
+template <int BITS, int SL, bool OUTL, bool PAGED>
 void pick_tc_g(int G, TcLaunchFn* f, TcOccFn* o) {
   switch (G) {
-    case 1: *f = launch_tc<BITS, 1, SL, OUTL>; *o = tc_occupancy<BITS, 1, SL, OUTL>; break;
-    case 2: *f = launch_tc<BITS, 2, SL, OUTL>; *o = tc_occupancy<BITS, 2, SL, OUTL>; break;
-    case 4: *f = launch_tc<BITS, 4, SL, OUTL>; *o = tc_occupancy<BITS, 4, SL, OUTL>; break;
-    default: *f = launch_tc<BITS, 8, SL, OUTL>; *o = tc_occupancy<BITS, 8, SL, OUTL>; break;
+    case 1: *f = launch_tc<BITS, 1, SL, OUTL, PAGED>; *o = tc_occupancy<BITS, 1, SL, OUTL, PAGED>; break;
+    case 2: *f = launch_tc<BITS, 2, SL, OUTL, PAGED>; *o = tc_occupancy<BITS, 2, SL, OUTL, PAGED>; break;
+    case 4: *f = launch_tc<BITS, 4, SL, OUTL, PAGED>; *o = tc_occupancy<BITS, 4, SL, OUTL, PAGED>; break;
+    default: *f = launch_tc<BITS, 8, SL, OUTL, PAGED>; *o = tc_occupancy<BITS, 8, SL, OUTL, PAGED>; break;
   }
 }
 
+template <int BITS, bool PAGED>
+void pick_tc_p(int Bk, int G, bool outl, TcLaunchFn* f, TcOccFn* o) {
+  if (Bk == 64) outl ? pick_tc_g<BITS, 1, true, PAGED>(G, f, o) : pick_tc_g<BITS, 1, false, PAGED>(G, f, o);
+  else outl ? pick_tc_g<BITS, 2, true, PAGED>(G, f, o) : pick_tc_g<BITS, 2, false, PAGED>(G, f, o);
+}
 template <int BITS>
-void pick_tc(int Bk, int G, bool outl, TcLaunchFn* f, TcOccFn* o) {
-  if (Bk == 64) outl ? pick_tc_g<BITS, 1, true>(G, f, o) : pick_tc_g<BITS, 1, false>(G, f, o);
-  else outl ? pick_tc_g<BITS, 2, true>(G, f, o) : pick_tc_g<BITS, 2, false>(G, f, o);
+void pick_tc(int Bk, int G, bool outl, bool paged, TcLaunchFn* f, TcOccFn* o) {
+  paged ? pick_tc_p<BITS, true>(Bk, G, outl, f, o) : pick_tc_p<BITS, false>(Bk, G, outl, f, o);
 }
 
-int cached_tc_occupancy(int dev, int bits, int Bk, int G, bool outl, size_t smem, TcOccFn fn) {
+int cached_tc_occupancy(int dev, int bits, int Bk, int G, bool outl, bool paged, size_t smem, TcOccFn fn) {
   struct Slot { size_t smem; int occ; };
-  static Slot cache[16][3][2][4][2];
+  static Slot cache[16][3][2][4][2][2];
   const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
-  Slot& s = cache[dev & 15][bits - 2][Bk == 128][gi][outl ? 1 : 0];
+  Slot& s = cache[dev & 15][bits - 2][Bk == 128][gi][outl ? 1 : 0][paged ? 1 : 0];
   if (s.occ == 0 || s.smem != smem) {
     s.occ = fn(smem);
     s.smem = smem;
@@ -162,7 +169,7 @@ int cached_tc_occupancy(int dev, int bits, int Bk, int G, bool outl, size_t smem
 
 cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, int H_q, int q_pos,
                           const float2* rope, float sm_scale, __half* out, float* ws,
-                          cudaStream_t st, int split_cap) {
+                          cudaStream_t st, int split_cap, const Paged* pg) {
   DecodeArgs a;
   a.d = d;
   a.k_codes = static_cast<const uint8_t*>(c.k_codes);
@@ -175,9 +182,14 @@ cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, in
   a.q = q;
   a.rope = rope;
   a.ws = ws;
-  a.T = c.T_cur;
-  a.n_full = c.T_cur / d.Bk;
-  a.tail_len = c.T_cur % d.Bk;
+  // paged: the grid is sized for the longest sequence; each CTA reads its own length
+  a.T = pg ? pg->max_len : c.T_cur;
+  a.n_full = a.T / d.Bk;
+  a.tail_len = a.T % d.Bk;
+  a.block_table = pg ? pg->block_table : nullptr;
+  a.seq_len = pg ? pg->seq_len : nullptr;
+  a.max_blocks = pg ? pg->max_blocks : 0;
+  a.n_blocks = pg ? pg->n_blocks : 0;
   a.H_q = H_q;
   a.q_pos = q_pos;
   a.S = (split_cap > 0 && split_cap < max_splits(d)) ? split_cap : max_splits(d);
@@ -193,18 +205,20 @@ cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, in
 
   if (d.D == 128) {
     CUtensorMap tk, tv;
-    if (!encode_codes(&tk, c.k_codes, d) || !encode_codes(&tv, c.v_codes, d))
+    const size_t n_units = pg ? (size_t)pg->n_blocks * d.H_kv : 0;
+    if (!encode_codes(&tk, c.k_codes, d, n_units) || !encode_codes(&tv, c.v_codes, d, n_units))
       return cudaErrorInvalidValue;
     const tc::StageLayout L = stage_layout(d);
     const size_t smem = (size_t)tc::ring_stages(d.Bk) * L.stage_bytes + 1024;
     TcLaunchFn fn = nullptr;
     TcOccFn occ_fn = nullptr;
+    const bool paged = pg != nullptr;
     switch (d.bits) {
-      case 2: pick_tc<2>(d.Bk, G, d.n_out > 0, &fn, &occ_fn); break;
-      case 3: pick_tc<3>(d.Bk, G, d.n_out > 0, &fn, &occ_fn); break;
-      default: pick_tc<4>(d.Bk, G, d.n_out > 0, &fn, &occ_fn); break;
+      case 2: pick_tc<2>(d.Bk, G, d.n_out > 0, paged, &fn, &occ_fn); break;
+      case 3: pick_tc<3>(d.Bk, G, d.n_out > 0, paged, &fn, &occ_fn); break;
+      default: pick_tc<4>(d.Bk, G, d.n_out > 0, paged, &fn, &occ_fn); break;
     }
-    const int occ = cached_tc_occupancy(dev, d.bits, d.Bk, G, d.n_out > 0, smem, occ_fn);
+    const int occ = cached_tc_occupancy(dev, d.bits, d.Bk, G, d.n_out > 0, paged, smem, occ_fn);
     a.n_split = choose_splits(d.B * d.H_kv, units, sms * occ, a.S);
     e = fn(a, L, tk, tv, smem, st);
   } else {

@@ -42,7 +42,30 @@ struct DecodeArgs {
   float* ws;
   int T, n_full, tail_len, H_q, q_pos, n_split, S;
   float scale_log2;    // sm_scale * log2(e)
+  const int32_t* block_table;  // paged cache (NULL: contiguous streams)
+  const int32_t* seq_len;      // paged: tokens of each sequence
+  int max_blocks, n_blocks;
 };
+
+// Tokens, full key blocks, tail length and query position of sequence b.
+struct SeqExtent {
+  int T, n_full, tail_len, q_pos;
+};
+__device__ __forceinline__ SeqExtent seq_extent(const DecodeArgs& a, int b) {
+  SeqExtent e;
+  if (a.block_table) {
+    const int cap = a.max_blocks * a.d.Bk;
+    const int t = __ldg(a.seq_len + b);
+    e.T = t < 0 ? 0 : (t > cap ? cap : t);
+    e.q_pos = e.T > 0 ? e.T - 1 : 0;
+  } else {
+    e.T = a.T;
+    e.q_pos = a.q_pos;
+  }
+  e.n_full = e.T / a.d.Bk;
+  e.tail_len = e.T - e.n_full * a.d.Bk;
+  return e;
+}
 
 template <int N, int I = 0, typename F>
 __device__ __forceinline__ void static_for(F&& f) {
@@ -175,7 +198,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const Decod
   const int bh = blockIdx.y;
   const int b = bh / d.H_kv, hkv = bh % d.H_kv;
   const int split = blockIdx.x;
-  const int units = a.n_full + (a.tail_len > 0 ? 1 : 0);
+  const SeqExtent ex = seq_extent(a, b);
+  const int units = ex.n_full + (ex.tail_len > 0 ? 1 : 0);
   const int u0 = (int)((long long)split * units / a.n_split);
   const int u1 = (int)((long long)(split + 1) * units / a.n_split);
   const int n_out = d.n_out;
@@ -186,8 +210,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const Decod
     const __half* qh = a.q + ((size_t)b * a.H_q + hkv * G + g) * D;
     float u = __half2float(qh[i]), v = __half2float(qh[i + HALF]);
     if (a.rope) {
-      const float2 r = rot_compose(rope_block(a.rope, d, a.q_pos / Bk, i),
-                                   rope_fine(a.rope, d, a.q_pos % Bk, i));
+      const float2 r = rot_compose(rope_block(a.rope, d, ex.q_pos / Bk, i),
+                                   rope_fine(a.rope, d, ex.q_pos % Bk, i));
       const float u2 = fmaf(u, r.x, -v * r.y);
       const float v2 = fmaf(v, r.x, u * r.y);
       u = u2;
@@ -209,12 +233,13 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const Decod
 #pragma unroll
   for (int g = 0; g < G; ++g) o[g][0] = o[g][1] = 0.0f;
 
-  const size_t stream_tok = (size_t)bh * d.T_max;
 
   for (int u = u0; u < u1; ++u) {
-    const bool is_tail = (u == a.n_full);
+    const bool is_tail = (u == ex.n_full);
+    const size_t kblk = unit_block(d, a.block_table, a.max_blocks, a.n_blocks, b, hkv, u);
+    const size_t row0 = kblk * Bk;     // row of the block's first token
     const int t0 = u * Bk;
-    const int ntok = is_tail ? a.tail_len : Bk;
+    const int ntok = is_tail ? ex.tail_len : Bk;
     __syncthreads();  // previous block's shared data fully consumed
 
     // ---- 1. query back-rotated by t0; key params
@@ -232,7 +257,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const Decod
     }
     if (!is_tail) {
       for (int c = tid; c < D; c += NT) {
-        const uint32_t w = __ldg(a.k_meta + ((size_t)bh * d.n_blk + u) * D + c);
+        const uint32_t w = __ldg(a.k_meta + kblk * D + c);
         s_ks[c] = h2f((uint16_t)(w & 0xFFFF));
         s_kz[c] = h2f((uint16_t)(w >> 16));
       }
@@ -249,7 +274,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const Decod
       if (j < ntok) {
         const int t = t0 + j;
         if (!is_tail) {
-          const uint8_t* rowp = a.k_codes + (stream_tok + t) * CB;
+          const uint8_t* rowp = a.k_codes + (row0 + j) * CB;
           Row<CB> row;
           row.load(rowp);
           if (Bk == 128) {
@@ -262,7 +287,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const Decod
           if (ph == 0) {
             // dense-and-sparse: replace the dense value at each outlier channel
             for (int k = 0; k < n_out; ++k) {
-              const uint32_t e = __ldg(a.k_outl + (stream_tok + t) * n_out + k);
+              const uint32_t e = __ldg(a.k_outl + (row0 + j) * n_out + k);
               const int c = (int)(e & 0xFFFF);
               const float xo = h2f((uint16_t)(e >> 16));
               const float xd = fmaf((float)code_at<BITS>(rowp, c), s_ks[c], s_kz[c]);
@@ -338,7 +363,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(const Decod
       o[g][1] *= s_alpha[g];
     }
     for (int jj = tp; jj < ntok; jj += NTP) {
-      const size_t t = stream_tok + t0 + jj;
+      const size_t t = row0 + jj;
       const uint8_t* rowp = a.v_codes + t * CB;
       uint32_t q0, q1;
       if constexpr (BITS == 4) {

@@ -356,8 +356,9 @@ __device__ __forceinline__ int acc_index(int w, int c, int h) {
 //   P . V:  D[channel][head] = sum_t A(v)[channel][t] B(p*s)[t][head]
 // so the score fragment of a lane is exactly its B operand for P . V.
 // OUTL: the cache keeps outliers (n_out > 0); without them the outlier code
-// is not compiled in.
-template <int BITS, int G, int SL, bool OUTL>
+// is not compiled in. PAGED: a paged, ragged batch (block table, per-sequence
+// lengths); the contiguous instantiation holds none of that code.
+template <int BITS, int G, int SL, bool OUTL, bool PAGED>
 __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const DecodeArgs a, const StageLayout L,
                                                              const __grid_constant__ CUtensorMap tm_k,
                                                              const __grid_constant__ CUtensorMap tm_v) {
@@ -387,7 +388,22 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
   const int bh = blockIdx.y;
   const int b = bh / d.H_kv, hkv = bh % d.H_kv;
   const int split = blockIdx.x;
-  const int units = a.n_full + (a.tail_len > 0 ? 1 : 0);
+  // paged: this sequence's full blocks and tail length, read from shared memory per block
+  __shared__ int s_ext[PAGED ? 2 : 1];
+  const SeqExtent ex = seq_extent(a, b);
+  const int units = ex.n_full + (ex.tail_len > 0 ? 1 : 0);
+  if (PAGED && tid == 0) {
+    s_ext[0] = ex.n_full;
+    s_ext[PAGED ? 1 : 0] = ex.tail_len;
+  }
+  auto n_full_b = [&]() -> int {
+    if constexpr (PAGED) return s_ext[0];
+    else return a.n_full;
+  };
+  auto tail_len_b = [&]() -> int {
+    if constexpr (PAGED) return s_ext[PAGED ? 1 : 0];
+    else return a.tail_len;
+  };
   const int u0 = (int)((long long)split * units / a.n_split);
   const int u1 = (int)((long long)(split + 1) * units / a.n_split);
   const int n_out = OUTL ? d.n_out : 0, ng = d.ng;
@@ -400,19 +416,24 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
   uint8_t* ring = dsmem + ((1024u - (smem_addr(dsmem) & 1023u)) & 1023u);
   const uint32_t ring_s = smem_addr(ring);
 
-  // (thread 0) copies of unit u into ring stage `stage`
-  auto issue = [&](int u, int stage) {
+  // (thread 0) copies of unit u, key block `kblk` (unit_block), into ring
+  // stage `stage`; the code maps are [stream][T_max rows] (contiguous) or
+  // [block][Bk rows] (paged), the other buffers are indexed by block
+  auto unit_blk = [&](int u) -> size_t {
+    return unit_block(d, PAGED ? a.block_table : nullptr, a.max_blocks, a.n_blocks, b, hkv, u);
+  };
+  auto issue = [&](int u, size_t kblk, int stage) {
     const uint32_t bar = smem_addr(&s_bar[stage]);
     const uint32_t base = ring_s + stage * L.stage_bytes;
-    const int t0 = u * BK;
+    const int y = PAGED ? 0 : u * BK, z = PAGED ? (int)kblk : bh;
     mbar_arrive_expect_tx(bar, L.tx_bytes);
-    tma_load_3d(base + L.kc, &tm_k, 0, t0, bh, bar);
-    tma_load_3d(base + L.vc, &tm_v, 0, t0, bh, bar);
-    bulk_load(base + L.km, static_cast<const uint8_t*>(s_src[0]) + (size_t)u * L.km_bytes, L.km_bytes, bar);
-    bulk_load(base + L.vm, static_cast<const uint8_t*>(s_src[1]) + (size_t)u * L.vm_bytes, L.vm_bytes, bar);
+    tma_load_3d(base + L.kc, &tm_k, 0, y, z, bar);
+    tma_load_3d(base + L.vc, &tm_v, 0, y, z, bar);
+    bulk_load(base + L.km, static_cast<const uint8_t*>(s_src[0]) + kblk * L.km_bytes, L.km_bytes, bar);
+    bulk_load(base + L.vm, static_cast<const uint8_t*>(s_src[1]) + kblk * L.vm_bytes, L.vm_bytes, bar);
     if (n_out > 0) {
-      bulk_load(base + L.ko, static_cast<const uint8_t*>(s_src[2]) + (size_t)u * L.outl_bytes, L.outl_bytes, bar);
-      bulk_load(base + L.vo, static_cast<const uint8_t*>(s_src[3]) + (size_t)u * L.outl_bytes, L.outl_bytes, bar);
+      bulk_load(base + L.ko, static_cast<const uint8_t*>(s_src[2]) + kblk * L.outl_bytes, L.outl_bytes, bar);
+      bulk_load(base + L.vo, static_cast<const uint8_t*>(s_src[3]) + kblk * L.outl_bytes, L.outl_bytes, bar);
     }
   };
   auto wait_unit = [&](int u) -> bool {
@@ -484,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
         }
       }
     }
-    if (u != a.n_full) {
+    if (u != n_full_b()) {
       const uint32_t m = reinterpret_cast<const uint32_t*>(st + L.km)[tid];
       const uint32_t mh = as_u32(__hmul2(as_h2(m), __float2half2_rn(0.5f)));
       uint8_t* kz = reinterpret_cast<uint8_t*>(&s_kz[buf][0][0][0]) + kz_off;
@@ -499,20 +520,23 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     s_abort = 0;
-    s_src[0] = a.k_meta + (size_t)bh * d.n_blk * kD;
-    s_src[1] = a.v_meta + (size_t)bh * d.T_max * ng;
-    s_src[2] = a.k_outl + (size_t)bh * d.T_max * n_out;
-    s_src[3] = a.v_outl + (size_t)bh * d.T_max * n_out;
+    s_src[0] = a.k_meta;
+    s_src[1] = a.v_meta;
+    s_src[2] = a.k_outl;
+    s_src[3] = a.v_outl;
   }
   __syncthreads();
-  if (tid == 0)
-    for (int k = 0; k < NST && u0 + k < u1; ++k) issue(u0 + k, k);
+  __shared__ size_t s_next_blk;   // paged (thread 0): block of the next unit to issue, looked up a block ahead
+  if (tid == 0) {
+    for (int k = 0; k < NST && u0 + k < u1; ++k) issue(u0 + k, unit_blk(u0 + k), k);
+    if (PAGED && u0 + NST < u1) s_next_blk = unit_blk(u0 + NST);
+  }
   for (int e = tid; e < G * HALF; e += kThreads) {
     const int gg = e / HALF, i = e % HALF;
     const __half* qh = a.q + ((size_t)b * a.H_q + hkv * G + gg) * kD;
     float x = __half2float(qh[i]), y = __half2float(qh[i + HALF]);
     if (a.rope) {
-      const float2 rr = rot_compose(rope_block(a.rope, d, a.q_pos / BK, i), rope_fine(a.rope, d, a.q_pos % BK, i));
+      const float2 rr = rot_compose(rope_block(a.rope, d, ex.q_pos / BK, i), rope_fine(a.rope, d, ex.q_pos % BK, i));
       const float x2 = fmaf(x, rr.x, -y * rr.y), y2 = fmaf(y, rr.x, x * rr.y);
       x = x2;
       y = y2;
@@ -582,8 +606,8 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
     const int k = u - u0, buf = k & 1;
     const int nstage = (stage + 1 == NST) ? 0 : stage + 1;
     const uint32_t nphase = phase ^ (nstage == 0 ? 1u : 0u);
-    const bool is_tail = (u == a.n_full);
-    const int ntok = is_tail ? a.tail_len : BK;
+    const bool is_tail = (u == n_full_b());
+    const int ntok = is_tail ? tail_len_b() : BK;
     const uint8_t* st = ring + stage * L.stage_bytes;
     const uint8_t* kc = st + L.kc;
     const uint8_t* vc = st + L.vc;
@@ -878,7 +902,14 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
       abort_split(u + 1);
       return;
     }
-    if (tid == 0 && u + NST < u1) issue(u + NST, stage);
+    if (tid == 0 && u + NST < u1) {
+      if constexpr (PAGED) {
+        issue(u + NST, s_next_blk, stage);
+        if (u + NST + 1 < u1) s_next_blk = unit_blk(u + NST + 1);
+      } else {
+        issue(u + NST, unit_blk(u + NST), stage);
+      }
+    }
     stage = nstage;
     phase = nphase;
   }
@@ -925,10 +956,10 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
 
 }  // namespace tc
 
-template <int BITS, int G, int SL, bool OUTL>
+template <int BITS, int G, int SL, bool OUTL, bool PAGED>
 cudaError_t launch_tc(const DecodeArgs& a, const tc::StageLayout& L, const CUtensorMap& tk,
                       const CUtensorMap& tv, size_t smem, cudaStream_t st);
-template <int BITS, int G, int SL, bool OUTL>
+template <int BITS, int G, int SL, bool OUTL, bool PAGED>
 int tc_occupancy(size_t smem);
 
 }  // namespace kvq

@@ -2,5 +2,5 @@
 #include "kvq_decode_tc_inst.cuh"
 
 namespace kvq {
-KVQ_INSTANTIATE_TC(2, false)
+KVQ_INSTANTIATE_TC(2, false, false)
 }  // namespace kvq

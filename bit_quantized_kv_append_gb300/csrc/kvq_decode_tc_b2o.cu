@@ -2,5 +2,5 @@
 #include "kvq_decode_tc_inst.cuh"
 
 namespace kvq {
-KVQ_INSTANTIATE_TC(2, true)
+KVQ_INSTANTIATE_TC(2, true, false)
 }  // namespace kvq

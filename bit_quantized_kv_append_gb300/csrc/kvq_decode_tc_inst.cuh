@@ -6,10 +6,10 @@
 
 namespace kvq {
 
-template <int BITS, int G, int SL, bool OUTL>
+template <int BITS, int G, int SL, bool OUTL, bool PAGED>
 cudaError_t launch_tc(const DecodeArgs& a, const tc::StageLayout& L, const CUtensorMap& tk,
                       const CUtensorMap& tv, size_t smem, cudaStream_t st) {
-  auto kern = tc::decode_tc_kernel<BITS, G, SL, OUTL>;
+  auto kern = tc::decode_tc_kernel<BITS, G, SL, OUTL, PAGED>;
   static size_t smem_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -23,9 +23,9 @@ cudaError_t launch_tc(const DecodeArgs& a, const tc::StageLayout& L, const CUten
   return cudaGetLastError();
 }
 
-template <int BITS, int G, int SL, bool OUTL>
+template <int BITS, int G, int SL, bool OUTL, bool PAGED>
 int tc_occupancy(size_t smem) {
-  auto kern = tc::decode_tc_kernel<BITS, G, SL, OUTL>;
+  auto kern = tc::decode_tc_kernel<BITS, G, SL, OUTL, PAGED>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return 1;
   int n = 0;
@@ -33,19 +33,19 @@ int tc_occupancy(size_t smem) {
   return n < 1 ? 1 : n;
 }
 
-#define KVQ_TC_ONE(BITS, G, SL, OUTL)                                                                \
-  template cudaError_t launch_tc<BITS, G, SL, OUTL>(const DecodeArgs&, const tc::StageLayout&,       \
-                                                    const CUtensorMap&, const CUtensorMap&, size_t,  \
-                                                    cudaStream_t);                                   \
-  template int tc_occupancy<BITS, G, SL, OUTL>(size_t);
-#define KVQ_INSTANTIATE_TC(BITS, OUTL) \
-  KVQ_TC_ONE(BITS, 1, 1, OUTL)         \
-  KVQ_TC_ONE(BITS, 2, 1, OUTL)         \
-  KVQ_TC_ONE(BITS, 4, 1, OUTL)         \
-  KVQ_TC_ONE(BITS, 8, 1, OUTL)         \
-  KVQ_TC_ONE(BITS, 1, 2, OUTL)         \
-  KVQ_TC_ONE(BITS, 2, 2, OUTL)         \
-  KVQ_TC_ONE(BITS, 4, 2, OUTL)         \
-  KVQ_TC_ONE(BITS, 8, 2, OUTL)
+#define KVQ_TC_ONE(BITS, G, SL, OUTL, PAGED)                                                          \
+  template cudaError_t launch_tc<BITS, G, SL, OUTL, PAGED>(const DecodeArgs&, const tc::StageLayout&,     \
+                                                           const CUtensorMap&, const CUtensorMap&, size_t, \
+                                                           cudaStream_t);                                  \
+  template int tc_occupancy<BITS, G, SL, OUTL, PAGED>(size_t);
+#define KVQ_INSTANTIATE_TC(BITS, OUTL, PAGED) \
+  KVQ_TC_ONE(BITS, 1, 1, OUTL, PAGED)         \
+  KVQ_TC_ONE(BITS, 2, 1, OUTL, PAGED)         \
+  KVQ_TC_ONE(BITS, 4, 1, OUTL, PAGED)         \
+  KVQ_TC_ONE(BITS, 8, 1, OUTL, PAGED)         \
+  KVQ_TC_ONE(BITS, 1, 2, OUTL, PAGED)         \
+  KVQ_TC_ONE(BITS, 2, 2, OUTL, PAGED)         \
+  KVQ_TC_ONE(BITS, 4, 2, OUTL, PAGED)         \
+  KVQ_TC_ONE(BITS, 8, 2, OUTL, PAGED)
 
 }  // namespace kvq

@@ -5,7 +5,10 @@ only provides device memory and streams. There is no CPU fallback: if the
 library is missing, the calls raise.
 
 Entry points mirror include/kvq.h: ``layout``, ``rope_init``, ``append``,
-``decode_attn``, ``decode_step``, ``decode_attn_noalloc``. ``QuantizedKVCache`` owns one layer's buffers.
+``decode_attn``, ``decode_step``, ``decode_attn_noalloc``, ``paged_layout``,
+``paged_append``, ``paged_decode_attn``. ``QuantizedKVCache`` owns one layer's
+buffers; ``PagedKVCache`` owns the pools, block table and lengths of a paged,
+ragged batch.
 """
 from __future__ import annotations
 
@@ -21,6 +24,7 @@ BUFFERS = ("k_codes", "k_meta", "k_tail", "k_outl", "v_codes", "v_meta", "v_outl
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "KVQ_ERR_CAPACITY",
           4: "KVQ_ERR_WORKSPACE", 5: "KVQ_ERR_CUDA"}
 EXPORTS = ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_decode_attn", "kvq_decode_step",
+           "kvq_paged_layout", "kvq_paged_append", "kvq_paged_decode_attn",
            "kvq_decode_attn_noalloc", "kvq_status_string", "kvq_version")
 
 
@@ -48,6 +52,12 @@ class CacheRef(ctypes.Structure):
     _fields_ = [(name, ctypes.c_void_p) for name in BUFFERS] + [("T_cur", ctypes.c_int32)]
 
 
+class PagedCacheRef(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_void_p) for name in BUFFERS] + [
+        ("block_table", ctypes.c_void_p), ("seq_len", ctypes.c_void_p),
+        ("n_blocks", ctypes.c_int32), ("max_len", ctypes.c_int32)]
+
+
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvq.so")
 _LIB = None
 
@@ -68,13 +78,17 @@ def lib():
                                       vp, ctypes.c_float, vp, vp, ctypes.c_size_t, vp]
         L.kvq_decode_step.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp, vp, vp, i32,
                                       vp, ctypes.c_float, vp, vp, ctypes.c_size_t, vp]
+        L.kvq_paged_layout.argtypes = [ctypes.POINTER(Config), i32, i32, ctypes.POINTER(Layout)]
+        L.kvq_paged_append.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(PagedCacheRef), vp, vp, i32, vp]
+        L.kvq_paged_decode_attn.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(PagedCacheRef), vp, i32, vp,
+                                            ctypes.c_float, vp, vp, ctypes.c_size_t, vp]
         L.kvq_decode_attn_noalloc.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp,
                                               i32, i32, vp, ctypes.c_float, vp, vp]
         L.kvq_status_string.argtypes = [ctypes.c_int]
         L.kvq_status_string.restype = ctypes.c_char_p
         L.kvq_version.restype = ctypes.c_char_p
         for fn in ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_decode_attn", "kvq_decode_step",
-                   "kvq_decode_attn_noalloc"):
+                   "kvq_paged_layout", "kvq_paged_append", "kvq_paged_decode_attn", "kvq_decode_attn_noalloc"):
             getattr(L, fn).restype = ctypes.c_int
         _LIB = L
     return _LIB
@@ -257,3 +271,130 @@ class QuantizedKVCache:
         decode_step(self.cfg, ref, k_new, v_new, q, self.H_q, self.rope, sm_scale, out, self.workspace, stream)
         self.T_cur = ref.T_cur
         return out
+
+
+# ----------------------------------------------------------------------------- paged, ragged batches
+def paged_layout(cfg: Config, n_blocks: int, H_q: int) -> Layout:
+    out = Layout()
+    _check(lib().kvq_paged_layout(ctypes.byref(cfg), int(n_blocks), int(H_q), ctypes.byref(out)), "kvq_paged_layout")
+    return out
+
+
+def paged_append(cfg: Config, ref: PagedCacheRef, k_new: torch.Tensor, v_new: torch.Tensor, n_new: int,
+                 stream=None):
+    _check(lib().kvq_paged_append(ctypes.byref(cfg), ctypes.byref(ref), _ptr(k_new), _ptr(v_new), int(n_new),
+                                  _stream(stream)), "kvq_paged_append")
+
+
+def paged_decode_attn(cfg: Config, ref: PagedCacheRef, q: torch.Tensor, H_q: int, rope: Optional[torch.Tensor],
+                      sm_scale: float, out: torch.Tensor, workspace: torch.Tensor, stream=None):
+    _check(lib().kvq_paged_decode_attn(ctypes.byref(cfg), ctypes.byref(ref), _ptr(q), int(H_q), _ptr(rope),
+                                       float(sm_scale), _ptr(out), _ptr(workspace), workspace.numel(),
+                                       _stream(stream)), "kvq_paged_decode_attn")
+
+
+class PagedKVCache:
+    """One layer of a paged, ragged batch: pools of n_blocks physical key
+    blocks (Bk tokens x H_kv heads each) shared by B sequences through
+    ``block_table`` [B, T_max // Bk] (int32, device; the caller assigns
+    blocks), per-sequence lengths ``seq_len`` [B] (int32, device), and each
+    sequence's fp16 tail of keys. ``lengths`` mirrors seq_len on the host."""
+
+    def __init__(self, B, H_kv, D, T_max, n_blocks, bits=4, key_block=64, value_group=64, outlier_frac=0.0,
+                 H_q=None, rope_theta=0.0, device="cuda", rope_table: Optional[torch.Tensor] = None):
+        self.cfg = make_config(B, H_kv, D, T_max, bits, key_block, value_group, outlier_frac)
+        self.H_q = H_q or H_kv
+        self.n_blocks = int(n_blocks)
+        self.layout = paged_layout(self.cfg, self.n_blocks, self.H_q)
+        self.device = torch.device(device)
+        if self.device.type == "cuda" and self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
+        self.buffers = {name: torch.empty(self.layout.bytes[i], dtype=torch.uint8, device=self.device)
+                        for i, name in enumerate(BUFFERS)}
+        self.block_table = torch.zeros((B, T_max // key_block), dtype=torch.int32, device=self.device)
+        self.seq_len = torch.zeros(B, dtype=torch.int32, device=self.device)
+        self.lengths = [0] * B
+        self.workspace = torch.empty(self.layout.workspace_bytes, dtype=torch.uint8, device=self.device)
+        self.rope_theta = float(rope_theta)
+        self.rope = rope_table
+        if self.rope is None and self.rope_theta > 0:
+            self.rope = torch.empty(self.layout.rope_bytes, dtype=torch.uint8, device=self.device)
+            rope_init(self.cfg, self.rope_theta, self.rope)
+
+    @property
+    def n_out(self) -> int:
+        return self.layout.n_out
+
+    def ref(self, seq: Optional[int] = None) -> PagedCacheRef:
+        """The whole batch, or (seq = b) a one-sequence view for kvq_config.B = 1."""
+        r = PagedCacheRef()
+        for name in BUFFERS:
+            t = self.buffers[name]
+            setattr(r, name, None if t.numel() == 0 else t.data_ptr())
+        r.block_table = self.block_table.data_ptr()
+        r.seq_len = self.seq_len.data_ptr()
+        r.n_blocks = self.n_blocks
+        r.max_len = max(self.lengths) if seq is None else self.lengths[seq]
+        if seq is not None:
+            r.block_table += seq * self.block_table.shape[1] * 4
+            r.seq_len += seq * 4
+            r.k_tail += seq * self.layout.stream_bytes[BUFFERS.index("k_tail")]
+        return r
+
+    def _cfg_one(self) -> Config:
+        c = self.cfg
+        return make_config(1, c.H_kv, c.D, c.T_max, c.bits, c.key_block, c.value_group, c.outlier_frac)
+
+    def _check_kv(self, k_new, v_new, B):
+        c = self.cfg
+        for t in (k_new, v_new):
+            if t.dtype != torch.float16 or not t.is_contiguous() or t.device != self.device:
+                raise ValueError("k_new/v_new must be contiguous fp16 tensors on the cache device")
+            if t.dim() != 4 or t.shape[0] != B or t.shape[1] != c.H_kv or t.shape[3] != c.D:
+                raise ValueError(f"expected [B={B}, H_kv={c.H_kv}, n, D={c.D}], got {tuple(t.shape)}")
+        if k_new.shape != v_new.shape:
+            raise ValueError("k_new and v_new shapes differ")
+
+    def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
+        """n new tokens for every sequence (k_new, v_new: fp16 [B, H_kv, n, D]),
+        each stored at its own length."""
+        self._check_kv(k_new, v_new, self.cfg.B)
+        n = k_new.shape[2]
+        paged_append(self.cfg, self.ref(), k_new, v_new, n, stream)
+        self.lengths = [x + n for x in self.lengths]
+
+    def append_seq(self, b: int, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
+        """n new tokens of sequence b alone (k_new, v_new: fp16 [1, H_kv, n, D])."""
+        self._check_kv(k_new, v_new, 1)
+        n = k_new.shape[2]
+        paged_append(self._cfg_one(), self.ref(b), k_new, v_new, n, stream)
+        self.lengths[b] += n
+
+    def decode(self, q: torch.Tensor, sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+        """q: fp16 [B, H_q, D], pre-RoPE; sequence b's query sits at its newest token."""
+        c = self.cfg
+        if q.dtype != torch.float16 or not q.is_contiguous() or q.device != self.device:
+            raise ValueError("q must be a contiguous fp16 tensor on the cache device")
+        if tuple(q.shape) != (c.B, self.H_q, c.D):
+            raise ValueError(f"expected q [B={c.B}, H_q={self.H_q}, D={c.D}], got {tuple(q.shape)}")
+        if out is None:
+            out = torch.empty_like(q)
+        sm_scale = 1.0 / math.sqrt(c.D) if sm_scale is None else sm_scale
+        paged_decode_attn(self.cfg, self.ref(), q, self.H_q, self.rope, sm_scale, out, self.workspace, stream)
+        return out
+
+    def views(self) -> dict:
+        """Typed views of the pools ([n_blocks, H_kv, ...]) and of K_TAIL ([B, H_kv, Bk, D])."""
+        c = self.cfg
+        n_out, cb, N, H, Bk = self.layout.n_out, self.layout.code_row_bytes, self.n_blocks, c.H_kv, c.key_block
+        bf = self.buffers
+        return {
+            "k_codes": bf["k_codes"].view(N, H, Bk, cb),
+            "k_meta": bf["k_meta"].view(torch.int16).view(N, H, c.D, 2),
+            "k_tail": bf["k_tail"].view(torch.float16).view(c.B, H, Bk, c.D),
+            "k_outl": bf["k_outl"].view(torch.int16).view(N, H, Bk, n_out, 2),
+            "v_codes": bf["v_codes"].view(N, H, Bk, cb),
+            "v_meta": bf["v_meta"].view(torch.int16).view(N, H, Bk, c.D // c.value_group, 2),
+            "v_outl": bf["v_outl"].view(torch.int16).view(N, H, Bk, n_out, 2),
+        }

@@ -215,6 +215,68 @@ KVQ_API int kvq_decode_attn_noalloc(const kvq_config* cfg, const kvq_cache* cach
                                     int32_t H_q, int32_t q_pos, const void* rope_tab,
                                     float sm_scale, void* out, void* stream);
 
+/* ---- Paged, ragged batches (continuous batching; mlqm.cn/news/1002276 §5.2-5.3
+ * name continuous batching and PagedAttention as the serving setting of a
+ * quantized cache). The sequences of a batch hold different numbers of
+ * tokens and share pools of physical key blocks through a block table.
+ * Each physical block holds Bk consecutive tokens of one sequence for all
+ * H_kv heads, encoded exactly as in the contiguous cache:
+ *   K_CODES [n_blocks][H_kv][Bk][D*bits/8]   K_META [n_blocks][H_kv][D][2]
+ *   K_OUTL  [n_blocks][H_kv][Bk][n_out][2]   V_CODES [n_blocks][H_kv][Bk][D*bits/8]
+ *   V_META  [n_blocks][H_kv][Bk][D/Gv][2]    V_OUTL  [n_blocks][H_kv][Bk][n_out][2]
+ *   K_TAIL  [B][H_kv][Bk][D]                 fp16 keys of each sequence's unfinished block
+ * For these calls kvq_config.B is the number of sequences (rows of the block
+ * table) and T_max the capacity of one sequence (block-table row length
+ * T_max / Bk). Token t of sequence b lives in physical block
+ * block_table[b][t / Bk], row t % Bk. The caller owns the pools and the
+ * table and hands out the blocks (any physical block may serve any
+ * sequence); a table entry outside [0, n_blocks) is clamped into the pool,
+ * which keeps every access in bounds but gives undefined values. */
+typedef struct kvq_paged_cache {
+  void* k_codes;                /* pools, layouts above */
+  void* k_meta;
+  void* k_tail;
+  void* k_outl;                 /* may be NULL when n_out = 0 */
+  void* v_codes;
+  void* v_meta;
+  void* v_outl;                 /* may be NULL when n_out = 0 */
+  const int32_t* block_table;   /* device [B][T_max / Bk] */
+  int32_t* seq_len;             /* device [B]: tokens stored per sequence */
+  int32_t n_blocks;             /* physical blocks in each pool */
+  int32_t max_len;              /* host: an upper bound of every seq_len[b] (sizes the grids) */
+} kvq_paged_cache;
+
+/* Sizes of the pools for n_blocks physical blocks (bytes[]), per physical
+ * block for the pools and per sequence for K_TAIL (stream_bytes[]), and the
+ * decode workspace for H_q query heads. fp16_equiv_bytes is the fp16 K and V
+ * of the pools' capacity. Host-only and pure.
+ * Errors: KVQ_ERR_ARG (NULL), KVQ_ERR_UNSUPPORTED (cfg, H_q, n_blocks < 1 or
+ * n_blocks * H_kv >= 2^31). */
+KVQ_API int kvq_paged_layout(const kvq_config* cfg, int32_t n_blocks, int32_t H_q, kvq_layout_t* out);
+
+/* kvq_append for a paged cache: n_new tokens for every sequence b, stored at
+ * positions seq_len[b] .. seq_len[b] + n_new - 1 (each sequence at its own
+ * position, read on the device), with the same encoding as kvq_append; then
+ * seq_len[b] += n_new on the device, stream-ordered after the stores, and
+ * cache->max_len += n_new. The blocks those positions fall in must already be
+ * in the block table. A single sequence can be appended alone by passing
+ * B = 1 and pointers to its table row, seq_len entry and K_TAIL stream.
+ *   k_new, v_new: fp16 [B][H_kv][n_new][D].
+ * Errors: KVQ_ERR_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CAPACITY
+ * (max_len + n_new > T_max), KVQ_ERR_CUDA. */
+KVQ_API int kvq_paged_append(const kvq_config* cfg, kvq_paged_cache* cache, const void* k_new,
+                             const void* v_new, int32_t n_new, void* stream);
+
+/* kvq_decode_attn for a paged cache: sequence b attends over its own
+ * seq_len[b] tokens with its query at position seq_len[b] - 1 (the newest
+ * token); a sequence with no tokens gets out = 0. Other arguments and the
+ * workspace size (kvq_paged_layout or kvq_layout of the same cfg) as for
+ * kvq_decode_attn. Errors: KVQ_ERR_ARG, KVQ_ERR_UNSUPPORTED,
+ * KVQ_ERR_WORKSPACE, KVQ_ERR_CUDA. */
+KVQ_API int kvq_paged_decode_attn(const kvq_config* cfg, const kvq_paged_cache* cache, const void* q,
+                                  int32_t H_q, const void* rope_tab, float sm_scale, void* out,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
 /* Static, human-readable name of a status code. */
 KVQ_API const char* kvq_status_string(int status);
 

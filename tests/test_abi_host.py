@@ -192,3 +192,61 @@ def test_decode_step_host_errors(lib):
     no_outl = _fake_cache(10, n_out=0)
     assert call(cache=no_outl) == 1                          # n_out = 1 needs the outlier buffers
     assert r.T_cur == 100                                    # nothing changed on any error
+
+
+def test_paged_layout_sizes(lib):
+    cfg = _cfg(B=3, H_kv=2, D=128, T_max=256, bits=3, key_block=128, value_group=32, outlier_frac=0.01)
+    lay = kvq.paged_layout(cfg, 10, 8)
+    H, Bk, D, cb, ng = 2, 128, 128, 48, 4
+    per_block = [H * Bk * cb, H * D * 4, H * Bk * D * 2, H * Bk * 1 * 4, H * Bk * cb, H * Bk * ng * 4, H * Bk * 4]
+    assert list(lay.stream_bytes) == per_block
+    assert list(lay.bytes) == [x * (3 if i == 2 else 10) for i, x in enumerate(per_block)]
+    assert lay.workspace_bytes == kvq.layout(cfg, 8).workspace_bytes
+    out = kvq.Layout()
+    assert lib.kvq_paged_layout(ctypes.byref(cfg), 0, 8, ctypes.byref(out)) == 2
+    assert lib.kvq_paged_layout(ctypes.byref(cfg), 10, 3, ctypes.byref(out)) == 2
+    assert lib.kvq_paged_layout(ctypes.byref(cfg), 1 << 30, 8, ctypes.byref(out)) == 2   # blocks x heads >= 2^31
+
+
+def _fake_paged(max_len=0, n_blocks=8, n_out=1):
+    r = kvq.PagedCacheRef()
+    for i, n in enumerate(kvq.BUFFERS):
+        setattr(r, n, FAKE * (i + 1) if (n_out or "outl" not in n) else None)
+    r.block_table = FAKE * 9
+    r.seq_len = FAKE * 10
+    r.n_blocks = n_blocks
+    r.max_len = max_len
+    return r
+
+
+def test_paged_host_errors(lib):
+    cfg = _cfg()                                     # T_max 256, Bk 64, n_out 1
+    p = ctypes.c_void_p(FAKE)
+    r = _fake_paged(200)
+    app = lambda c=r, n=1, k=p, v=p, cf=cfg: lib.kvq_paged_append(ctypes.byref(cf), None if c is None else ctypes.byref(c),
+                                                                 k, v, n, None)
+    assert app(n=57) == 3 and r.max_len == 200       # 200 + 57 > 256
+    assert app(n=-1) == 1
+    assert app(n=0) == 0
+    assert app(c=None) == 1
+    assert app(k=None) == 1
+    assert app(v=ctypes.c_void_p(FAKE + 4)) == 1
+    assert app(cf=_cfg(bits=9)) == 2
+    for field, val in (("block_table", None), ("seq_len", FAKE + 2), ("n_blocks", 0), ("max_len", -1),
+                       ("max_len", 300), ("k_tail", FAKE + 8)):
+        bad = _fake_paged(10)
+        setattr(bad, field, val)
+        assert app(c=bad) == 1, field
+    assert app(c=_fake_paged(10, n_out=0)) == 1       # n_out = 1 needs the outlier pools
+    lay = kvq.layout(cfg, 8)
+    ws = lay.workspace_bytes
+    dec = lambda c=r, q=p, H_q=8, rope=None, scale=0.1, out=p, w=p, wsb=ws: lib.kvq_paged_decode_attn(
+        ctypes.byref(cfg), None if c is None else ctypes.byref(c), q, H_q, rope, scale, out, w, wsb, None)
+    assert dec(wsb=ws - 1) == 4
+    assert dec(H_q=6) == 2
+    assert dec(c=None) == 1
+    assert dec(q=None) == 1
+    assert dec(out=ctypes.c_void_p(FAKE + 2)) == 1
+    assert dec(rope=ctypes.c_void_p(FAKE + 8)) == 1
+    assert dec(scale=float("inf")) == 1
+    assert dec(c=_fake_paged(10, n_blocks=-3)) == 1
