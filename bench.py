@@ -489,6 +489,111 @@ def run_prefill(args, w, rank, world, device):
     }
 
 
+def paged_lengths(w):
+    """Ragged prefill lengths of the paged workload: T (B - b) / B tokens for
+    sequence b, rounded down to whole key blocks (at least one block)."""
+    return [max(w.key_block, w.T * (w.B - b) // w.B // w.key_block * w.key_block) for b in range(w.B)]
+
+
+def run_paged(args, w, rank, world, device):
+    """Decode step of a paged, ragged batch: every sequence appends one token
+    at its own position (kvq_paged_append) and attends over all of its tokens
+    (kvq_paged_decode_attn); the sequences' key blocks sit in one pool in a
+    seeded random order. The sequences grow by one token per step."""
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import bit_quantized_kv_append_gb300 as kvq
+
+    Bk = w.key_block
+    lens = paged_lengths(w)
+    grow = args.warmup + args.steps + 2
+    T_max = (max(lens) + grow + Bk - 1) // Bk * Bk
+    per_seq = [(L + grow + Bk - 1) // Bk for L in lens]
+    n_blocks = sum(per_seq) + 8
+    cache = kvq.PagedKVCache(w.B, w.H_kv, w.D, T_max, n_blocks, w.bits, Bk, w.value_group, w.outlier_frac,
+                             H_q=w.H_q, rope_theta=w.rope_theta, device=device)
+    rng = np.random.default_rng(1000 + w.seed)
+    perm = rng.permutation(n_blocks)
+    table = np.zeros((w.B, T_max // Bk), np.int32)
+    k = 0
+    for b, nb in enumerate(per_seq):
+        table[b, :nb] = perm[k:k + nb]
+        k += nb
+    cache.block_table.copy_(torch.from_numpy(table))
+    chunk = 1 << 15
+    for t0 in range(0, max(lens), chunk):
+        n = min(chunk, max(lens) - t0)
+        K, V = ki.kv_torch(w, 0, t0, n, device)
+        for b, L in enumerate(lens):
+            if t0 < L:
+                m = min(n, L - t0)
+                cache.append_seq(b, K[b:b + 1, :, :m].contiguous(), V[b:b + 1, :, :m].contiguous())
+        del K, V
+    k1, v1 = ki.kv_torch(w, 0, max(lens), 1, device)     # the step's new token of every sequence
+    q = ki.queries_torch(w, 0, 1, device)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        cache.append(k1, v1)
+        if ev is not None:
+            ev[0].record(stream)
+        cache.decode(q, out=out)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    lens_t0 = list(cache.lengths)
+    clocks = ClockSampler(physical_gpu(torch.cuda.current_device()))
+    clocks.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_end)
+    dec_ms = [a.elapsed_time(b) for a, b in evs]
+    ms, dec_mean = max_over_ranks([ms, statistics.mean(dec_ms)], device)
+    # algorithmic bytes of the average decode call (lengths after each step's append)
+    one = w.replace(B=1)
+    alg = statistics.mean(sum(decode_alg_bytes(one, L + 1 + i) for L in lens_t0) for i in range(args.steps))
+    peak, peak_kind = measured_peaks()
+    achieved = alg / (dec_mean * 1e-3) / 1e9
+    sha = source_sha(DECODE_SOURCES["paged"])
+    return {
+        "metric": "decode-attn tokens/s (one layer; B query tokens per step), paged ragged batch",
+        "value": replica_throughput(w.B * args.steps, world, ms), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": f"u{w.bits}/f16/f32", "data": "synthetic",
+        "config": {
+            "workload": (f"{w.name} paged: B={w.B} H_q={w.H_q} H_kv={w.H_kv} D={w.D} lengths={lens_t0} (+1 per "
+                         f"step) INT{w.bits} key_block={Bk} value_group={w.value_group} outliers={w.outlier_frac} "
+                         f"rope_theta={w.rope_theta} pool={n_blocks} blocks, shuffled block table"),
+            "step": "kvq_paged_append of 1 token per sequence + kvq_paged_decode_attn",
+            "l2": f"inputs larger than L2 (pools {cache.layout.cache_bytes / 1e9:.2f} GB > 129 MB); no flush",
+            "parallelism": f"replicas x{world}",
+            "decode_call_ms": dec_mean,
+        },
+        "gpu_launches": 4 * args.steps,      # append + length advance, decode + combine
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": peak_kind,
+                     "kernel": "decode_tc_kernel paged (+ decode_combine_kernel: one kvq_paged_decode_attn call)",
+                     "alg_bytes_per_launch": alg,
+                     "traffic": profile_traffic(f"decode_tc_kernel_{w.name}_paged.txt", sha), "source_sha": sha},
+        "clocks": clk,
+    }
+
+
 def run_reference(args, w):
     """The CPU oracle as the reference arm: each step a bounded sample of the
     workload's decode step, extrapolated to the full step."""
@@ -526,7 +631,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--workload", default="mha7b", choices=list(ki.WORKLOADS))
-    ap.add_argument("--mode", default="decode", choices=["decode", "prefill"])
+    ap.add_argument("--mode", default="decode", choices=["decode", "prefill", "paged"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -552,13 +657,13 @@ def main():
         dist.barrier()
     device = torch.device("cuda", local_rank if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(device)
-    line = (run_prefill if args.mode == "prefill" else run_decode)(args, w, rank, world, device)
+    line = {"prefill": run_prefill, "paged": run_paged, "decode": run_decode}[args.mode](args, w, rank, world, device)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(w) if args.mode == "decode" else cpu_baseline_prefill(w)
+            line["cpu_baseline"] = cpu_baseline_prefill(w) if args.mode == "prefill" else cpu_baseline(w)
         print(json.dumps(line), flush=True)
 
 
