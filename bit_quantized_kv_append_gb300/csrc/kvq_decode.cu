@@ -70,6 +70,18 @@ int choose_splits(int streams, int units, int slots, int max_split) {
   return best;
 }
 
+// Paged, ragged batches: every sequence gets the same number of splits, so a
+// CTA's work follows its sequence's length. When a uniform batch of the
+// longest length would fill a single wave, twice its splits leave the
+// hardware scheduler shorter CTAs to even the load out across the SMs.
+int paged_splits(const Dims& d, int units_max, int slots, int max_split) {
+  int n = choose_splits(d.B * d.H_kv, units_max, slots, max_split);
+  if ((long long)n * d.B * d.H_kv <= slots) n *= 2;
+  if (n > units_max) n = units_max;
+  if (n > max_split) n = max_split;
+  return n < 1 ? 1 : n;
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -219,7 +231,7 @@ cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, in
       default: pick_tc<4>(d.Bk, G, d.n_out > 0, paged, &fn, &occ_fn); break;
     }
     const int occ = cached_tc_occupancy(dev, d.bits, d.Bk, G, d.n_out > 0, paged, smem, occ_fn);
-    a.n_split = choose_splits(d.B * d.H_kv, units, sms * occ, a.S);
+    a.n_split = paged ? paged_splits(d, units, sms * occ, a.S) : choose_splits(d.B * d.H_kv, units, sms * occ, a.S);
     e = fn(a, L, tk, tv, smem, st);
   } else {
     LaunchFn fn = nullptr;
@@ -230,7 +242,7 @@ cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, in
       default: pick_g<4, 64>(G, &fn, &occ_fn); break;
     }
     const int occ = cached_occupancy(dev, d.bits, d.D, G, occ_fn);
-    a.n_split = choose_splits(d.B * d.H_kv, units, sms * occ, a.S);
+    a.n_split = pg ? paged_splits(d, units, sms * occ, a.S) : choose_splits(d.B * d.H_kv, units, sms * occ, a.S);
     e = fn(a, st);
   }
   if (e != cudaSuccess) return e;
