@@ -24,7 +24,7 @@ int make_dims(const kvq_config* cfg, Dims* d) {
   if (!cfg || !d) return KVQ_ERR_ARG;
   const kvq_config& c = *cfg;
   if (c.B < 1 || c.H_kv < 1 || c.T_max < 1) return KVQ_ERR_UNSUPPORTED;
-  if (c.bits < 2 || c.bits > 4) return KVQ_ERR_UNSUPPORTED;
+  if (c.bits != 2 && c.bits != 3 && c.bits != 4 && c.bits != 8) return KVQ_ERR_UNSUPPORTED;
   if (c.D != 64 && c.D != 128) return KVQ_ERR_UNSUPPORTED;
   if (c.key_block != 64 && c.key_block != 128) return KVQ_ERR_UNSUPPORTED;
   if (c.value_group != 32 && c.value_group != 64 && c.value_group != 128) return KVQ_ERR_UNSUPPORTED;

@@ -32,7 +32,11 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxGroups = 4;       // D / Gv <= 128 / 32
-constexpr float kTieGuard = 1e-5f;  // |t| above 0.5 - guard: recompute the chunk exactly
+// |t| above 0.5 - guard: recompute the chunk exactly. The guard exceeds the
+// distance between y and the binary32 quotient, at most 2^-22 |y| (below
+// 3.9e-6 for codes under 16, 6.2e-5 for the 8-bit codes under 256).
+template <int BITS>
+constexpr float tie_guard() { return BITS <= 4 ? 1e-5f : 1e-4f; }
 constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23: x + kMagic rounds x to an integer (ties even)
 
 struct AppendArgs {
@@ -85,8 +89,9 @@ __device__ __forceinline__ float rcp_or_zero(float s) {
 
 // clamp(rint(fl((x - z) / s)), 0, L) in binary32 round-to-nearest (0 when
 // s = 0), computed without a division: y = (x - z) * r with r within 1 ulp of
-// 1/s is within 4e-6 of the binary32 quotient Q = fl((x - z) / s) when
-// |y| < 16. Away from the half-integers the rounding of y is that of Q. Near
+// 1/s is within 2^-22 |y| of the binary32 quotient Q = fl((x - z) / s) (4e-6
+// for |y| < 16, 6.2e-5 for |y| < 256). Away from the half-integers the
+// rounding of y is that of Q. Near
 // a half-integer h the exact residual rho = (x - z) - h*s (one fma, exact) and
 // half an ulp of h, times s (exact), tell whether Q rounds to h (then ties go
 // to the even integer) or to a neighbour. Beyond [-0.75, L + 0.75] the clamp
@@ -144,6 +149,11 @@ __device__ __forceinline__ void pack_bits(const uint32_t (&mb)[32], uint32_t (&w
       }
       w[k] = __byte_perm(__byte_perm(byte[0], byte[1], 0x0040u), __byte_perm(byte[2], byte[3], 0x0040u), 0x5410u);
     }
+  } else if constexpr (BITS == 8) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)   // low byte of each pattern is the code
+      w[k] = __byte_perm(__byte_perm(mb[4 * k], mb[4 * k + 1], 0x0040u),
+                         __byte_perm(mb[4 * k + 2], mb[4 * k + 3], 0x0040u), 0x5410u);
   } else {
 #pragma unroll
     for (int k = 0; k < BITS; ++k) w[k] = 0u;
@@ -225,7 +235,7 @@ __device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv,
   pack_bits<BITS>(mb, w);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    if (tm[k] > 0.5f - kTieGuard) {
+    if (tm[k] > 0.5f - tie_guard<BITS>()) {
       // a value of these 8 channels sits close to a rounding tie: exact rule
 #pragma unroll 1
       for (int e = 8 * k; e < 8 * k + 8; ++e) {
@@ -242,7 +252,7 @@ __device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv,
           sc = vp.z;
         }
         const float y = __fmul_rn(__fsub_rn(x, z), rc);
-        if (!(fabsf(y - rintf(y)) > 0.5f - kTieGuard)) continue;   // NaN (outlier position) included
+        if (!(fabsf(y - rintf(y)) > 0.5f - tie_guard<BITS>())) continue;   // NaN (outlier position) included
         set_code<BITS>(w, e, exact_code(x, z, sc, rc, L));
       }
     }
@@ -522,7 +532,10 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
       else
         chunk_codes<BITS, false>(sX, sPv, sPk, sS, sO, sQ, D, Bk, r, ch, (ch * 32) >> gv_sh, n_out, w);
       uint32_t* dst = reinterpret_cast<uint32_t*>(base + (size_t)(row_base + t_row0 + r) * d.cb) + ch * BITS;
-      if constexpr (BITS == 4) {
+      if constexpr (BITS == 8) {
+        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      } else if constexpr (BITS == 4) {
         *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
       } else if constexpr (BITS == 2) {
         *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
@@ -637,6 +650,7 @@ cudaError_t launch_append(const Dims& d, const kvq_cache& c, const __half* k_new
   switch (d.bits) {
     case 2: e = launch_bits<2>(a, grid, smem, st); break;
     case 3: e = launch_bits<3>(a, grid, smem, st); break;
+    case 8: e = launch_bits<8>(a, grid, smem, st); break;
     default: e = launch_bits<4>(a, grid, smem, st); break;
   }
   if (e != cudaSuccess) return e;

@@ -44,9 +44,9 @@ void pick_g(int G, LaunchFn* f, OccFn* o) {
 
 // Occupancy (CTAs per SM) of each kernel variant, per device, computed once.
 int cached_occupancy(int dev, int bits, int D, int G, OccFn fn) {
-  static int cache[16][3][2][4];
+  static int cache[16][4][2][4];
   const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
-  int& slot = cache[dev & 15][bits - 2][D == 128][gi];
+  int& slot = cache[dev & 15][bits == 8 ? 3 : bits - 2][D == 128][gi];
   if (slot == 0) slot = fn();
   return slot;
 }
@@ -215,7 +215,7 @@ cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, in
   if (e != cudaSuccess) return e;
   const int units = a.n_full + (a.tail_len > 0 ? 1 : 0);
 
-  if (d.D == 128) {
+  if (d.D == 128 && d.bits != 8) {
     CUtensorMap tk, tv;
     const size_t n_units = pg ? (size_t)pg->n_blocks * d.H_kv : 0;
     if (!encode_codes(&tk, c.k_codes, d, n_units) || !encode_codes(&tv, c.v_codes, d, n_units))
@@ -239,6 +239,7 @@ cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, in
     switch (d.bits) {
       case 2: pick_g<2, 64>(G, &fn, &occ_fn); break;
       case 3: pick_g<3, 64>(G, &fn, &occ_fn); break;
+      case 8: d.D == 64 ? pick_g<8, 64>(G, &fn, &occ_fn) : pick_g<8, 128>(G, &fn, &occ_fn); break;
       default: pick_g<4, 64>(G, &fn, &occ_fn); break;
     }
     const int occ = cached_occupancy(dev, d.bits, d.D, G, occ_fn);

@@ -22,14 +22,15 @@ int partial_occupancy() {
   return n < 1 ? 1 : n;
 }
 
-#define KVQ_INSTANTIATE_DECODE(BITS)                                               \
-  template cudaError_t launch_partial<BITS, 64, 1>(const DecodeArgs&, cudaStream_t);  \
-  template cudaError_t launch_partial<BITS, 64, 2>(const DecodeArgs&, cudaStream_t);  \
-  template cudaError_t launch_partial<BITS, 64, 4>(const DecodeArgs&, cudaStream_t);  \
-  template cudaError_t launch_partial<BITS, 64, 8>(const DecodeArgs&, cudaStream_t);  \
-  template int partial_occupancy<BITS, 64, 1>();                                    \
-  template int partial_occupancy<BITS, 64, 2>();                                    \
-  template int partial_occupancy<BITS, 64, 4>();                                    \
-  template int partial_occupancy<BITS, 64, 8>();
+#define KVQ_INSTANTIATE_DECODE_D(BITS, D)                                          \
+  template cudaError_t launch_partial<BITS, D, 1>(const DecodeArgs&, cudaStream_t);   \
+  template cudaError_t launch_partial<BITS, D, 2>(const DecodeArgs&, cudaStream_t);   \
+  template cudaError_t launch_partial<BITS, D, 4>(const DecodeArgs&, cudaStream_t);   \
+  template cudaError_t launch_partial<BITS, D, 8>(const DecodeArgs&, cudaStream_t);   \
+  template int partial_occupancy<BITS, D, 1>();                                     \
+  template int partial_occupancy<BITS, D, 2>();                                     \
+  template int partial_occupancy<BITS, D, 4>();                                     \
+  template int partial_occupancy<BITS, D, 8>();
+#define KVQ_INSTANTIATE_DECODE(BITS) KVQ_INSTANTIATE_DECODE_D(BITS, 64)
 
 }  // namespace kvq

@@ -70,6 +70,8 @@ WORKLOADS = {
     "int3": Workload("int3", 4, 32, 8, 128, 131072, 3, 128, 32, 0.01, 5e5, 4),
     "int2": Workload("int2", 4, 32, 8, 128, 131072, 2, 128, 32, 0.01, 5e5, 4),
     "long1m": Workload("long1m", 1, 32, 8, 128, 1 << 20, 4, 64, 64, 0.01, 5e5, 5, layers=32),
+    # 8-bit variant of the "gqa8b" shape (the prefill-append variant at INT8)
+    "int8": Workload("int8", 4, 32, 8, 128, 131072, 8, 64, 64, 0.01, 5e5, 6),
 }
 
 

@@ -71,10 +71,10 @@ def test_layout_sizes(lib, name):
     assert lay.fp16_equiv_bytes == 2 * S * T_max * w.D * 2
     for b in lay.stream_bytes:
         assert b % 16 == 0          # every stream starts 16-byte aligned
-    # packed INT4 + metadata is ~30% of fp16; INT2 well under 25%
+    # packed INT4 + metadata is ~30% of fp16; INT2 well under 25%; INT8 ~55%
     ratio = lay.cache_bytes / lay.fp16_equiv_bytes
     if w.T >= 32768:                 # the fp16 tail is a fixed cost on tiny caches
-        assert ratio < {4: 0.32, 3: 0.27, 2: 0.21}[w.bits]
+        assert ratio < {8: 0.56, 4: 0.32, 3: 0.27, 2: 0.21}[w.bits]
 
 
 def _cfg(**kw):

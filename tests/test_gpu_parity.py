@@ -38,6 +38,9 @@ SMALL = {
     "d64_g2_two_outliers": (W("d64", 2, 4, 2, 64, 333, 3, 64, 32, 0.04, 1e4, 6), 333, [333]),
     "g8_gv128": (W("g8", 1, 16, 2, 128, 300, 4, 64, 128, 0.01, 5e5, 7), 300, [300]),
     "g1_d64_int2_norope": (W("g1", 3, 2, 2, 64, 200, 2, 128, 64, 0.0, 0.0, 8), 200, [200]),
+    # 8-bit codes (decode on the CUDA-core kernel at both head dims)
+    "int8_gqa_outliers": (W("int8", 2, 8, 2, 128, 300, 8, 64, 64, 0.01, 5e5, 41), 300, [130, 1, 169]),
+    "int8_d64_bk128_gv32": (W("int8d64", 1, 4, 2, 64, 260, 8, 128, 32, 0.0, 1e4, 42), 260, [260]),
 }
 
 
@@ -113,8 +116,9 @@ def _planted_inputs(w, T):
     return K, V
 
 
-def test_planted_degenerate_groups():
-    w = W("planted", 1, 4, 2, 128, 200, 4, 64, 64, 0.01, 1e4, 13)
+@pytest.mark.parametrize("bits", [4, 8])
+def test_planted_degenerate_groups(bits):
+    w = W("planted", 1, 4, 2, 128, 200, bits, 64, 64, 0.01, 1e4, 13)
     T = 200
     K, V = _planted_inputs(w, T)
     cache = tl.make_cache(w, 256)
@@ -130,6 +134,27 @@ def test_planted_degenerate_groups():
     # fp16 values up to 65504 in V: compare relative to the value range
     got = tl.q_of_streams(out, w, streams).astype(np.float64)
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) < 1e-2
+
+
+def test_int8_value_ties():
+    """8-bit value groups whose quotients (x - z) / s are exact half-integers:
+    min 0 and max 255/16 give s = 1/16 exactly, so x = (k + 1/2)/16 sits on a
+    rounding tie (ties to the even code)."""
+    w = W("ties8", 1, 4, 2, 128, 64, 8, 64, 64, 0.0, 0.0, 14)
+    rng = np.random.default_rng(14)
+    K = rng.standard_normal((1, 2, 64, 128)).astype(np.float16)
+    V = rng.standard_normal((1, 2, 64, 128)).astype(np.float16)
+    for t in range(64):
+        ks = rng.integers(0, 255, size=62)
+        V[0, 0, t, 0] = 0.0
+        V[0, 0, t, 1] = 255 / 16
+        V[0, 0, t, 2:64] = ((ks + 0.5) / 16).astype(np.float16)
+    assert np.all(V[0, 0, :, 2:64].astype(np.float64) * 16 % 1 == 0.5)
+    cache = tl.make_cache(w, 64)
+    cache.append(torch.from_numpy(K).cuda(), torch.from_numpy(V).cuda())
+    enc = tl.oracle_encode(w, K[0], V[0])
+    tl.sync()
+    tl.compare_streams(cache, [(0, 0), (0, 1)], enc, 64)
 
 
 def test_capacity_and_noop():

@@ -51,7 +51,7 @@ def test_half_decode_exact():
 
 
 # -------------------------------------------------------------- grid round trip
-@pytest.mark.parametrize("bits", [2, 3, 4])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 def test_grid_round_trip_values_and_keys(bits):
     """Values already on the grid z + q*s come back exactly (codes, s, z, x)."""
     L = (1 << bits) - 1
@@ -127,7 +127,7 @@ def test_error_bound_and_outliers_exact(bits, Bk, Gv, n_out):
 
 
 # -------------------------------------------------------------- brute force codes
-@pytest.mark.parametrize("bits", [2, 3, 4])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 def test_codes_brute_force(bits):
     """The code is the nearest level (ties to even), unless fp32 rounding sits on a tie."""
     L = (1 << bits) - 1
