@@ -124,11 +124,6 @@ __device__ __forceinline__ float ex2(float x) {   // 2^x, hardware approximation
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// Shared-memory float add without a returned value. Its callers sit between
-// two __syncwarp(), which order it against every other access to the sums.
-__device__ __forceinline__ void red_add(float* p, float v) {
-  asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(smem_addr(p)), "f"(v));
-}
 // sin and cos of x in [0, 2^8): two-constant Cody-Waite reduction by 2 pi (the
 // high constant has 8 significant bits, so n * hi is exact for n < 2^16), then
 // the hardware approximations on [-pi, pi].
