@@ -104,8 +104,8 @@ EncodeTiledFn encode_fn() {
 
 // 3-D map over a packed code buffer: [stream][T_max rows][row byte]
 // (contiguous cache) or [physical block x H_kv][Bk rows][row byte] (paged
-// pools, `pool_units` > 0); box = one key block. INT4 rows (64 B) get the
-// 64 B swizzle, INT2 rows (32 B) 32 B.
+// pools, `pool_units` > 0); box = one key block. INT8 rows (128 B) get the
+// 128 B swizzle, INT4 rows (64 B) 64 B, INT2 rows (32 B) 32 B.
 bool encode_codes(CUtensorMap* m, const void* base, const Dims& d, size_t pool_units) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -114,7 +114,8 @@ bool encode_codes(CUtensorMap* m, const void* base, const Dims& d, size_t pool_u
   const cuuint64_t strides[2] = {(cuuint64_t)d.cb, rows * d.cb};
   const cuuint32_t box[3] = {(cuuint32_t)d.cb, (cuuint32_t)d.Bk, 1};
   const cuuint32_t es[3] = {1, 1, 1};
-  const CUtensorMapSwizzle sw = d.bits == 4   ? CU_TENSOR_MAP_SWIZZLE_64B
+  const CUtensorMapSwizzle sw = d.bits == 8   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : d.bits == 4 ? CU_TENSOR_MAP_SWIZZLE_64B
                                 : d.bits == 2 ? CU_TENSOR_MAP_SWIZZLE_32B
                                               : CU_TENSOR_MAP_SWIZZLE_NONE;
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
@@ -167,9 +168,9 @@ void pick_tc(int Bk, int G, bool outl, bool paged, TcLaunchFn* f, TcOccFn* o) {
 
 int cached_tc_occupancy(int dev, int bits, int Bk, int G, bool outl, bool paged, size_t smem, TcOccFn fn) {
   struct Slot { size_t smem; int occ; };
-  static Slot cache[16][3][2][4][2][2];
+  static Slot cache[16][4][2][4][2][2];
   const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
-  Slot& s = cache[dev & 15][bits - 2][Bk == 128][gi][outl ? 1 : 0][paged ? 1 : 0];
+  Slot& s = cache[dev & 15][bits == 8 ? 3 : bits - 2][Bk == 128][gi][outl ? 1 : 0][paged ? 1 : 0];
   if (s.occ == 0 || s.smem != smem) {
     s.occ = fn(smem);
     s.smem = smem;
@@ -215,7 +216,7 @@ cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, in
   if (e != cudaSuccess) return e;
   const int units = a.n_full + (a.tail_len > 0 ? 1 : 0);
 
-  if (d.D == 128 && d.bits != 8) {
+  if (d.D == 128) {
     CUtensorMap tk, tv;
     const size_t n_units = pg ? (size_t)pg->n_blocks * d.H_kv : 0;
     if (!encode_codes(&tk, c.k_codes, d, n_units) || !encode_codes(&tv, c.v_codes, d, n_units))
@@ -228,6 +229,7 @@ cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, in
     switch (d.bits) {
       case 2: pick_tc<2>(d.Bk, G, d.n_out > 0, paged, &fn, &occ_fn); break;
       case 3: pick_tc<3>(d.Bk, G, d.n_out > 0, paged, &fn, &occ_fn); break;
+      case 8: pick_tc<8>(d.Bk, G, d.n_out > 0, paged, &fn, &occ_fn); break;
       default: pick_tc<4>(d.Bk, G, d.n_out > 0, paged, &fn, &occ_fn); break;
     }
     const int occ = cached_tc_occupancy(dev, d.bits, d.Bk, G, d.n_out > 0, paged, smem, occ_fn);
@@ -239,7 +241,7 @@ cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, in
     switch (d.bits) {
       case 2: pick_g<2, 64>(G, &fn, &occ_fn); break;
       case 3: pick_g<3, 64>(G, &fn, &occ_fn); break;
-      case 8: d.D == 64 ? pick_g<8, 64>(G, &fn, &occ_fn) : pick_g<8, 128>(G, &fn, &occ_fn); break;
+      case 8: pick_g<8, 64>(G, &fn, &occ_fn); break;
       default: pick_g<4, 64>(G, &fn, &occ_fn); break;
     }
     const int occ = cached_occupancy(dev, d.bits, d.D, G, occ_fn);

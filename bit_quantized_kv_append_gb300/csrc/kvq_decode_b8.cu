@@ -1,8 +1,6 @@
-// Decode partial kernels for 8-bit codes (head_dim 64 and 128; the
-// tensor-core kernel's fragment geometry covers 2-4 bit codes).
+// Decode partial kernels for 8-bit codes (head_dim 64).
 #include "kvq_decode_inst.cuh"
 
 namespace kvq {
-KVQ_INSTANTIATE_DECODE_D(8, 64)
-KVQ_INSTANTIATE_DECODE_D(8, 128)
+KVQ_INSTANTIATE_DECODE(8)
 }  // namespace kvq

@@ -182,7 +182,8 @@ static __device__ const uint4 g_rot_identity[kRotFragQuads] = {KVQ_ROT_ID256, KV
 // Byte offset of (row, byte) in a code tile as the TMA swizzle lays it out.
 template <int BITS>
 __device__ __forceinline__ uint32_t code_off(int row, int byte) {
-  if constexpr (BITS == 4) return row * 64 + ((((byte >> 4) ^ ((row >> 1) & 3)) << 4) | (byte & 15));
+  if constexpr (BITS == 8) return row * 128 + ((((byte >> 4) ^ (row & 7)) << 4) | (byte & 15));
+  else if constexpr (BITS == 4) return row * 64 + ((((byte >> 4) ^ ((row >> 1) & 3)) << 4) | (byte & 15));
   else if constexpr (BITS == 2) return row * 32 + ((((byte >> 4) ^ ((row >> 2) & 1)) << 4) | (byte & 15));
   else return row * 48 + byte;
 }
@@ -202,7 +203,7 @@ struct LaneOff {
   uint32_t kf, kp;      // key: first-half and partner codes
   uint32_t ksh;         // INT3: bit shift of the lane's 48-bit key window
   uint32_t vb, vx;      // value tile: row base and swizzle (chunk c at vb + ((c << 4) ^ vx))
-  uint32_t vsh;         // INT3: bit shift of the lane's value codes
+  uint32_t vsh;         // INT3: bit shift of the lane's value codes; INT8: the lane's 16-byte chunk in a 32-byte group
   uint32_t sel0, sel1;  // byte_perm selectors of the lane's value bytes
 };
 
@@ -213,7 +214,16 @@ __device__ __forceinline__ LaneOff lane_offsets(int w, int g, int r) {
   o.ksh = o.vsh = o.sel0 = o.sel1 = 0u;
   const int tk = tperm(g), tv = tperm(2 * r);
   const int krow = 16 * w + tk, vrow = 16 * w + tv;
-  if constexpr (BITS == 4) {
+  if constexpr (BITS == 8) {
+    // 128-byte rows, 128 B swizzle (16-byte chunk ^ row % 8): first-half
+    // channels [16r, 16r + 16) are chunk r, their partners chunk 4 + r
+    const int ksw = krow & 7;
+    o.kf = 128 * krow + ((r ^ ksw) << 4);
+    o.kp = 128 * krow + (((4 + r) ^ ksw) << 4);
+    o.vb = 128 * vrow + 4 * (g & 3);
+    o.vx = (uint32_t)((vrow & 7) << 4);
+    o.vsh = (uint32_t)(g >> 2);
+  } else if constexpr (BITS == 4) {
     const int ksw = (tk >> 1) & 3, vsw = (tv >> 1) & 3, bb = 2 * (g & 1);
     o.kf = 64 * krow + (((r >> 1) ^ ksw) << 4) + 8 * (r & 1);
     o.kp = 64 * krow + (((2 + (r >> 1)) ^ ksw) << 4) + 8 * (r & 1);
@@ -266,6 +276,13 @@ __device__ __forceinline__ KeyWords key_words(const uint8_t* kc, const LaneOff& 
   return k;
 }
 
+// INT8: exact integer codes (half2) of a word's bytes (0, 1) -> x0 and
+// (2, 3) -> x1 (byte b becomes the fp16 1024 + b, then 1024 is taken off).
+__device__ __forceinline__ void key_codes8(uint32_t W, uint32_t& x0, uint32_t& x1) {
+  x0 = fix1(__byte_perm(W, kMagic, 0x7150u));
+  x1 = fix1(__byte_perm(W, kMagic, 0x7352u));
+}
+
 // Exact integer codes (half2) of k-step kq's slots (0, 1) -> x0 and (2, 3)
 // -> x1 from one half's code words, in kchan order.
 template <int BITS>
@@ -300,7 +317,14 @@ __device__ __forceinline__ void key_codes(const uint32_t (&wd)[2], uint32_t ksh,
 template <int BITS>
 __device__ __forceinline__ void value_pair(const uint8_t* vc, const LaneOff& o, int sl, int rp, int c4,
                                            uint32_t (&b)[4]) {
-  if constexpr (BITS == 4) {
+  if constexpr (BITS == 8) {
+    // rows t (even) and t + 1: their swizzles differ in the low bit only
+    const uint8_t* p = vc + o.vb + 8192 * sl + 1024 * rp;
+    const uint32_t ca = (((2 * c4 + o.vsh) << 4) ^ o.vx);
+    const uint32_t A = ld_s32(p + ca), B = ld_s32(p + 128 + (ca ^ 16u));
+#pragma unroll
+    for (int e = 0; e < 4; ++e) b[e] = __byte_perm(A, B, (uint32_t)(e | ((e + 4) << 8))) & 0x00FF00FFu;
+  } else if constexpr (BITS == 4) {
     const uint8_t* p = vc + (o.vb + ((c4 << 4) ^ o.vx)) + 4096 * sl + 512 * rp;
     const uint32_t A = ld_s32(p), B = ld_s32(p + 64);
     const uint32_t x0 = __byte_perm(A, B, o.sel0), x1 = __byte_perm(A, B, o.sel1);
@@ -334,7 +358,8 @@ __device__ __forceinline__ void value_pair(const uint8_t* vc, const LaneOff& o, 
 // Power of two that undoes the subnormal encoding of value code b[e].
 template <int BITS>
 __device__ __forceinline__ float value_scale(int e) {
-  if constexpr (BITS == 4) return (e & 1) ? 1048576.0f : 16777216.0f;         // 2^20 : 2^24
+  if constexpr (BITS == 8) return 16777216.0f;                                  // 2^24
+  else if constexpr (BITS == 4) return (e & 1) ? 1048576.0f : 16777216.0f;    // 2^20 : 2^24
   else if constexpr (BITS == 2) return 16777216.0f / (float)(1 << (2 * e));    // 2^(24-2e)
   else return (e & 1) ? 2097152.0f : 16777216.0f;                             // 2^21 : 2^24
 }
@@ -623,8 +648,17 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
         for (int h = 0; h < KVQ_TC_QK_CHAINS; ++h) acc[nt][h][0] = acc[nt][h][1] = acc[nt][h][2] = acc[nt][h][3] = 0.0f;
       if (!is_tail) {
         KeyWords kw[2];
+        uint4 k8f[2], k8p[2];   // INT8: the lane's 16 first-half and 16 partner codes of each n-tile
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) kw[nt] = key_words<BITS>(kc, lo, 64 * sl + 8 * nt);
+        for (int nt = 0; nt < 2; ++nt) {
+          if constexpr (BITS == 8) {
+            const uint8_t* rowp = kc + 128 * (64 * sl + 8 * nt);
+            k8f[nt] = *reinterpret_cast<const uint4*>(rowp + lo.kf);
+            k8p[nt] = *reinterpret_cast<const uint4*>(rowp + lo.kp);
+          } else {
+            kw[nt] = key_words<BITS>(kc, lo, 64 * sl + 8 * nt);
+          }
+        }
 #pragma unroll
         for (int kq = 0; kq < 4; ++kq) {
           const uint4 qf = s_qa[buf][sl][kq][lane], qp = s_qa[buf][sl][kq + 4][lane];
@@ -632,8 +666,15 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
             uint32_t f0, f1, p0, p1;
-            key_codes<BITS>(kw[nt].f, lo.ksh, kq, f0, f1);
-            key_codes<BITS>(kw[nt].p, lo.ksh, kq, p0, p1);
+            if constexpr (BITS == 8) {
+              const uint32_t wf[4] = {k8f[nt].x, k8f[nt].y, k8f[nt].z, k8f[nt].w};
+              const uint32_t wp[4] = {k8p[nt].x, k8p[nt].y, k8p[nt].z, k8p[nt].w};
+              key_codes8(wf[kq], f0, f1);
+              key_codes8(wp[kq], p0, p1);
+            } else {
+              key_codes<BITS>(kw[nt].f, lo.ksh, kq, f0, f1);
+              key_codes<BITS>(kw[nt].p, lo.ksh, kq, p0, p1);
+            }
             const __half2 xf0 = __hfma2(as_h2(f0), as_h2(zf.x), as_h2(zf.z));
             const __half2 xf1 = __hfma2(as_h2(f1), as_h2(zf.y), as_h2(zf.w));
             const __half2 xp0 = __hfma2(as_h2(p0), as_h2(zp.x), as_h2(zp.z));

@@ -1,0 +1,6 @@
+// Tensor-core decode kernels (head_dim 128) for 8-bit codes, caches without outliers, paged batches.
+#include "kvq_decode_tc_inst.cuh"
+
+namespace kvq {
+KVQ_INSTANTIATE_TC(8, false, true)
+}  // namespace kvq

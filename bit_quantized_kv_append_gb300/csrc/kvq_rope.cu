@@ -63,10 +63,11 @@ cudaError_t launch_rope_init(const Dims& d, double theta, float2* tab, cudaStrea
   const int threads = 256;
   const int blocks = (int)((n + threads - 1) / threads < 4096 ? (n + threads - 1) / threads : 4096);
   rope_init_kernel<<<blocks, threads, 0, st>>>(d, theta, tab);
-  if (d.D == tc::kD && d.bits != 8) {   // the tensor-core kernel's table (2-4 bit codes)
+  if (d.D == tc::kD) {
     uint4* frag = reinterpret_cast<uint4*>(tab + rope_frag_off(d));
     const int fb = tc::kRotFragQuads / threads;
-    if (d.bits == 4) rope_frag_kernel<4><<<fb, threads, 0, st>>>(theta, frag);
+    if (d.bits == 8) rope_frag_kernel<8><<<fb, threads, 0, st>>>(theta, frag);
+    else if (d.bits == 4) rope_frag_kernel<4><<<fb, threads, 0, st>>>(theta, frag);
     else if (d.bits == 3) rope_frag_kernel<3><<<fb, threads, 0, st>>>(theta, frag);
     else rope_frag_kernel<2><<<fb, threads, 0, st>>>(theta, frag);
   }

@@ -63,9 +63,7 @@ typedef enum kvq_status {
 #define KVQ_MAX_OUTLIERS 8  /* largest n_out per vector */
 
 /* One layer's cache shape. Supported: bits in {2, 3, 4, 8} (8: the 8-bit
- * variant of Quanto's block-wise scheme, page 3 "Quanto"; its decode runs on
- * the CUDA-core kernel, the others on the tensor-core kernel at D = 128);
- * D in {64, 128};
+ * width of Quanto's block-wise scheme, page 3 "Quanto"); D in {64, 128};
  * key_block in {64, 128}; value_group in {32, 64, 128} dividing D;
  * T_max > 0 a multiple of key_block and < 2^24; B, H_kv >= 1, B*H_kv <= 65535;
  * outlier_frac = 0 (no outliers) or in (0, 1]: n_out = max(1, floor(frac*D)),
