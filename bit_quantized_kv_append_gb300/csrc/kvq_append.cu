@@ -36,7 +36,7 @@ constexpr int kMaxGroups = 4;       // D / Gv <= 128 / 32
 // distance between y and the binary32 quotient, at most 2^-22 |y| (below
 // 3.9e-6 for codes under 16, 6.2e-5 for the 8-bit codes under 256).
 template <int BITS>
-constexpr float tie_guard() { return BITS <= 4 ? 1e-5f : 1e-4f; }
+__host__ __device__ constexpr float tie_guard() { return BITS <= 4 ? 1e-5f : 1e-4f; }
 constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23: x + kMagic rounds x to an integer (ties even)
 
 struct AppendArgs {
@@ -192,9 +192,8 @@ __device__ __forceinline__ int sw_off(int r, int D, int col) {
 }
 
 // Step D for one 32-channel chunk of row r: codes from the packed fp32 path,
-// the exact rule for the 8-channel groups holding a value near a rounding
-// tie, and the outlier positions' codes (computed in step C'); returns the
-// packed words.
+// the exact rule for the elements near a rounding tie, and the outlier
+// positions' codes (computed in step C'); returns the packed words.
 template <int BITS, bool KEYS>
 __device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv, const float4* sPk,
                                            const float* sS, const uint32_t* sO, const uint8_t* sQ, int D,
@@ -205,12 +204,12 @@ __device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv,
   float4 vp = make_float4(0.f, 0.f, 0.f, 0.f);
   if (!KEYS) vp = sPv[grp * Bk + r];
   uint32_t mb[32];
-  float tm[4];
+  uint32_t near = 0u;   // bit e: element e's quotient is within the guard of a rounding tie
+  constexpr float kNear = 0.5f - tie_guard<BITS>();
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const uint4 v = *reinterpret_cast<const uint4*>(sX + r * D + ((((4 * ch + k) ^ (r & 7))) << 3));
     const uint32_t hw[4] = {v.x, v.y, v.z, v.w};
-    tm[k] = 0.0f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int e = 8 * k + 2 * j;
@@ -227,35 +226,31 @@ __device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv,
       const float2 y2 = __fmul2_rn(d2, r2);
       const float2 m2 = __fadd2_rn(y2, magic2);
       const float2 t2 = __ffma2_rn(__fadd2_rn(m2, nmagic2), neg1, y2);   // y - rint(y)
-      tm[k] = fmaxf(tm[k], fmaxf(fabsf(t2.x), fabsf(t2.y)));           // NaN (outlier) ignored
+      // NaN (an outlier position) compares false
+      near |= (fabsf(t2.x) > kNear ? 1u : 0u) << e;
+      near |= (fabsf(t2.y) > kNear ? 1u : 0u) << (e + 1);
       mb[e] = __float_as_uint(m2.x);
       mb[e + 1] = __float_as_uint(m2.y);
     }
   }
   pack_bits<BITS>(mb, w);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    if (tm[k] > 0.5f - tie_guard<BITS>()) {
-      // a value of these 8 channels sits close to a rounding tie: exact rule
-#pragma unroll 1
-      for (int e = 8 * k; e < 8 * k + 8; ++e) {
-        const int c = ch * 32 + e;
-        const float x = __half2float(sX[sw_off(r, D, c)]);
-        float z, sc, rc;
-        if (KEYS) {
-          z = -reinterpret_cast<const float*>(&sPk[c >> 1])[c & 1];
-          rc = reinterpret_cast<const float*>(&sPk[c >> 1])[2 + (c & 1)];
-          sc = sS[c];
-        } else {
-          z = -vp.x;
-          rc = vp.y;
-          sc = vp.z;
-        }
-        const float y = __fmul_rn(__fsub_rn(x, z), rc);
-        if (!(fabsf(y - rintf(y)) > 0.5f - tie_guard<BITS>())) continue;   // NaN (outlier position) included
-        set_code<BITS>(w, e, exact_code(x, z, sc, rc, L));
-      }
+  // the few elements near a tie: exact rule, one element at a time
+  while (near) {
+    const int e = __ffs(near) - 1;
+    near &= near - 1u;
+    const int c = ch * 32 + e;
+    const float x = __half2float(sX[sw_off(r, D, c)]);
+    float z, sc, rc;
+    if (KEYS) {
+      z = -reinterpret_cast<const float*>(&sPk[c >> 1])[c & 1];
+      rc = reinterpret_cast<const float*>(&sPk[c >> 1])[2 + (c & 1)];
+      sc = sS[c];
+    } else {
+      z = -vp.x;
+      rc = vp.y;
+      sc = vp.z;
     }
+    set_code<BITS>(w, e, exact_code(x, z, sc, rc, L));
   }
   for (int o = 0; o < n_out; ++o) {
     const int c = (int)(sO[o * Bk + r] & 0xFFFFu);
@@ -344,60 +339,53 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   uint32_t* gout_base = (isK ? a.k_outl : a.v_outl) + (size_t)(row_base + t_row0) * n_out;
   const __half nanh = __ushort_as_half((uint16_t)0x7E00u);   // marks outliers for step C
   if (n_out == 1 && D == 128) {
-    // two threads per row, 64 channels each: the largest |x| (fp16 max), then
-    // its lowest channel
-    const int row = tid >> 1, half = tid & 1;
-    const bool active = row < rows;                // both threads of a row agree
-    uint32_t c_best = 0xFFFFu;
-    __half2 m2 = __float2half2_rn(0.0f);
-    __half2 cm[8];                                 // per-chunk max |x|
-    if (active) {
+    // four threads per row, 32 channels (four 16-byte chunks) each. The fp16
+    // magnitude bits (x & 0x7FFF) order like |x|, so the largest |x| is an
+    // unsigned 16-bit maximum; then the lowest channel holding it.
+    const int quarter = tid & 3;
+    for (int r0 = 0; r0 < rows; r0 += kThreads / 4) {     // same trip count in every thread
+      const int row = r0 + (tid >> 2);
+      const bool active = row < rows;                     // the four threads of a row agree
+      uint32_t cmax[4] = {0u, 0u, 0u, 0u};               // per chunk, max magnitude in both halves
+      if (active) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint4 v = reinterpret_cast<const uint4*>(sX + row * D)[(8 * half + k) ^ (row & 7)];
-        const uint32_t a4[4] = {v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu, v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu};
-        const __half2* h = reinterpret_cast<const __half2*>(a4);
-        cm[k] = __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3]));
-      }
-      m2 = __hmax2(__hmax2(__hmax2(cm[0], cm[1]), __hmax2(cm[2], cm[3])),
-                   __hmax2(__hmax2(cm[4], cm[5]), __hmax2(cm[6], cm[7])));
-      m2 = __hmax2(m2, __lowhigh2highlow(m2));     // both halves: the thread's max |x|
-    }
-    {
-      const uint32_t mine = *reinterpret_cast<uint32_t*>(&m2);
-      const uint32_t theirs = __shfl_xor_sync(0xffffffffu, mine, 1);
-      m2 = __hmax2(m2, *reinterpret_cast<const __half2*>(&theirs));   // the row's max |x|
-    }
-    if (active) {
-      // first chunk holding the max, then its first word and half
-      int kc = 8;
-#pragma unroll
-      for (int k = 7; k >= 0; --k) {
-        const __half2 e2 = __heq2(cm[k], m2);
-        kc = (*reinterpret_cast<const uint32_t*>(&e2) != 0u) ? k : kc;
-      }
-      if (kc < 8) {
-        const uint4 v = reinterpret_cast<const uint4*>(sX + row * D)[(8 * half + kc) ^ (row & 7)];
-        const uint32_t wv[4] = {v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu, v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu};
-        int idx = 0;
-#pragma unroll
-        for (int j = 3; j >= 0; --j) {
-          const __half2 e2 = __heq2(*reinterpret_cast<const __half2*>(&wv[j]), m2);
-          const uint32_t eu = *reinterpret_cast<const uint32_t*>(&e2);
-          idx = eu ? (2 * j + ((eu & 0xFFFFu) ? 0 : 1)) : idx;
+        for (int k = 0; k < 4; ++k) {
+          const uint4 v = reinterpret_cast<const uint4*>(sX + row * D)[(4 * quarter + k) ^ (row & 7)];
+          cmax[k] = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                             __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
         }
-        c_best = 64 * half + 8 * kc + idx;
       }
-    }
-    const uint32_t other = __shfl_xor_sync(0xffffffffu, c_best, 1);
-    if (active && half == 0) {
-      uint32_t c = (c_best != 0xFFFFu) ? c_best : other;
-      c = min(c, (uint32_t)(D - 1));               // only NaN rows (out of contract) match nothing
-      const int off = sw_off(row, D, (int)c);
-      const uint32_t e = c | ((uint32_t)hbits(sX[off]) << 16);
-      sO[row] = e;
-      gout_base[row] = e;
-      sX[off] = nanh;
+      uint32_t mx = __vmaxu2(__vmaxu2(cmax[0], cmax[1]), __vmaxu2(cmax[2], cmax[3]));
+      mx = max(mx & 0xFFFFu, mx >> 16);
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));  // the row's largest magnitude
+      uint32_t c_best = 0xFFFFu;
+      if (active) {
+        int kc = 4;                                       // first chunk holding it
+#pragma unroll
+        for (int k = 3; k >= 0; --k) kc = (max(cmax[k] & 0xFFFFu, cmax[k] >> 16) == mx) ? k : kc;
+        if (kc < 4) {
+          const uint4 v = reinterpret_cast<const uint4*>(sX + row * D)[(4 * quarter + kc) ^ (row & 7)];
+          const uint32_t wv[4] = {v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu, v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu};
+          int idx = 8;
+#pragma unroll
+          for (int j = 3; j >= 0; --j) {
+            idx = ((wv[j] >> 16) == mx) ? 2 * j + 1 : idx;
+            idx = ((wv[j] & 0xFFFFu) == mx) ? 2 * j : idx;
+          }
+          c_best = 32 * quarter + 8 * kc + idx;
+        }
+      }
+      c_best = min(c_best, __shfl_xor_sync(0xffffffffu, c_best, 1));
+      c_best = min(c_best, __shfl_xor_sync(0xffffffffu, c_best, 2));
+      if (active && quarter == 0) {
+        const uint32_t c = min(c_best, (uint32_t)(D - 1));
+        const int off = sw_off(row, D, (int)c);
+        const uint32_t e = c | ((uint32_t)hbits(sX[off]) << 16);
+        sO[row] = e;
+        gout_base[row] = e;
+        sX[off] = nanh;
+      }
     }
   } else if (n_out > 0) {
     // a warp per row: keys |x| bits (15) above (255 - channel); the max is the
