@@ -312,26 +312,44 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   uint8_t* sQ = reinterpret_cast<uint8_t*>(sRed);                            // after C: outlier codes [n_out][Bk]
 
   // ---- A. stage rows in shared memory (16-byte vectors, all loads in flight
-  // before the first store)
+  // before the first store). Thread: vector c of rows r0, r0 + RPI, ... A row's
+  // source is the old tail (keys before T_cur) or the new rows. With 64-token
+  // blocks the sources are addressed from two linear bases; with 128-token
+  // blocks (every vector slot in use) per-vector addressing measured faster.
   {
     constexpr int kMaxVec = 128 * vpr / kThreads;  // rows <= 128
+    constexpr int RPI = kThreads / vpr;            // rows per pass (a multiple of 8)
+    const int c = tid % vpr, r0 = tid / vpr;
     uint4 v[kMaxVec];
+    if (Bk == 64) {
+      const long long new_row0 = (long long)bh * a.n_new + (t_row0 - T_cur);   // new-row index of staged row 0
+      const __half* new_base = (isK ? a.k_new : a.v_new) + new_row0 * D;
+      const int r_split = isK ? T_cur - t_row0 : 0;  // rows below come from the tail
 #pragma unroll
-    for (int k = 0; k < kMaxVec; ++k) {
-      const int i = tid + k * kThreads, r = i / vpr, c = i % vpr;
-      if (r < rows) {
-        const int t = t_row0 + r;
-        const __half* src = isK ? ((t < T_cur) ? tail + (size_t)r * D
-                                               : a.k_new + ((size_t)bh * a.n_new + (t - T_cur)) * D)
-                                : a.v_new + ((size_t)bh * a.n_new + (t - T_cur)) * D;
-        v[k] = __ldg(reinterpret_cast<const uint4*>(src) + c);
+      for (int k = 0; k < kMaxVec; ++k) {
+        const int r = r0 + k * RPI;
+        if (r < rows) {
+          const __half* src = (r < r_split ? tail : new_base) + (size_t)r * D;
+          v[k] = __ldg(reinterpret_cast<const uint4*>(src) + c);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < kMaxVec; ++k) {
+        const int r = r0 + k * RPI;
+        if (r < rows) {
+          const int t = t_row0 + r;
+          const __half* src = isK ? ((t < T_cur) ? tail + (size_t)r * D
+                                                 : a.k_new + ((size_t)bh * a.n_new + (t - T_cur)) * D)
+                                  : a.v_new + ((size_t)bh * a.n_new + (t - T_cur)) * D;
+          v[k] = __ldg(reinterpret_cast<const uint4*>(src) + c);
+        }
       }
     }
+    uint4* dst = reinterpret_cast<uint4*>(sX + r0 * D) + (c ^ (r0 & 7));   // (r0 + k RPI) & 7 == r0 & 7
 #pragma unroll
-    for (int k = 0; k < kMaxVec; ++k) {
-      const int i = tid + k * kThreads, r = i / vpr, c = i % vpr;
-      if (r < rows) reinterpret_cast<uint4*>(sX + r * D)[c ^ (r & 7)] = v[k];
-    }
+    for (int k = 0; k < kMaxVec; ++k)
+      if (r0 + k * RPI < rows) dst[k * RPI * vpr] = v[k];
   }
   __syncthreads();
 
