@@ -25,6 +25,8 @@
 //      Outlier positions are recomputed from their stored value.
 // All rounding follows the library's stated arithmetic: binary32 RN subtract
 // and divide, fp16 round-up for the scale, round-half-even codes.
+#include <atomic>
+
 #include "kvq_common.cuh"
 
 namespace kvq {
@@ -583,12 +585,15 @@ size_t append_smem(const Dims& d) {
 
 template <int BITS, int D>
 cudaError_t launch_bd(const AppendArgs& a, dim3 grid, size_t smem, cudaStream_t st) {
-  static bool attr_set = false;  // per device the attribute is idempotent
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(append_kernel<BITS, D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+  // the shared-memory limit is a per-device function attribute: set it once on each device
+  static std::atomic<bool> attr_set[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (!attr_set[dev & 63].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(append_kernel<BITS, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[dev & 63].store(true, std::memory_order_release);
   }
   append_kernel<BITS, D><<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();

@@ -3,6 +3,8 @@
 // splits (log-sum-exp in base 2) into the fp16 output.
 #include <cuda.h>
 
+#include <mutex>
+
 #include "kvq_decode_tc.cuh"
 
 namespace kvq {
@@ -44,8 +46,10 @@ void pick_g(int G, LaunchFn* f, OccFn* o) {
 
 // Occupancy (CTAs per SM) of each kernel variant, per device, computed once.
 int cached_occupancy(int dev, int bits, int D, int G, OccFn fn) {
+  static std::mutex mu;
   static int cache[16][4][2][4];
   const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+  std::lock_guard<std::mutex> lock(mu);
   int& slot = cache[dev & 15][bits == 8 ? 3 : bits - 2][D == 128][gi];
   if (slot == 0) slot = fn();
   return slot;
@@ -87,18 +91,17 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// The driver's tensor-map encoder, looked up once (thread-safe static init).
 EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+      return reinterpret_cast<EncodeTiledFn>(p);
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -168,8 +171,10 @@ void pick_tc(int Bk, int G, bool outl, bool paged, TcLaunchFn* f, TcOccFn* o) {
 
 int cached_tc_occupancy(int dev, int bits, int Bk, int G, bool outl, bool paged, size_t smem, TcOccFn fn) {
   struct Slot { size_t smem; int occ; };
+  static std::mutex mu;
   static Slot cache[16][4][2][4][2][2];
   const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+  std::lock_guard<std::mutex> lock(mu);
   Slot& s = cache[dev & 15][bits == 8 ? 3 : bits - 2][Bk == 128][gi][outl ? 1 : 0][paged ? 1 : 0];
   if (s.occ == 0 || s.smem != smem) {
     s.occ = fn(smem);

@@ -2,6 +2,8 @@
 // one translation unit per code width so the instantiations build in parallel.
 #pragma once
 
+#include <atomic>
+
 #include "kvq_decode_tc.cuh"
 
 namespace kvq {
@@ -10,13 +12,17 @@ template <int BITS, int G, int SL, bool OUTL, bool PAGED>
 cudaError_t launch_tc(const DecodeArgs& a, const tc::StageLayout& L, const CUtensorMap& tk,
                       const CUtensorMap& tv, size_t smem, cudaStream_t st) {
   auto kern = tc::decode_tc_kernel<BITS, G, SL, OUTL, PAGED>;
-  static size_t smem_set[64] = {};
+  // largest dynamic shared memory requested so far, per device (a function attribute per device)
+  static std::atomic<size_t> smem_set[64];
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (smem_set[dev & 63] < smem) {
+  cudaError_t e0 = cudaGetDevice(&dev);
+  if (e0 != cudaSuccess) return e0;
+  if (smem_set[dev & 63].load(std::memory_order_acquire) < smem) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    smem_set[dev & 63] = smem;
+    size_t cur = smem_set[dev & 63].load(std::memory_order_relaxed);
+    while (cur < smem && !smem_set[dev & 63].compare_exchange_weak(cur, smem, std::memory_order_acq_rel)) {
+    }
   }
   const dim3 grid(a.n_split, a.d.B * a.d.H_kv);
   kern<<<grid, tc::kThreads, smem, st>>>(a, L, tk, tv);
