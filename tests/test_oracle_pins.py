@@ -89,7 +89,8 @@ def test_grid_round_trip_values_and_keys(bits):
 
 
 # -------------------------------------------------------------- error bound
-@pytest.mark.parametrize("bits,Bk,Gv,n_out", [(4, 64, 64, 1), (3, 128, 32, 1), (2, 128, 32, 2), (4, 64, 32, 0)])
+@pytest.mark.parametrize("bits,Bk,Gv,n_out", [(4, 64, 64, 1), (3, 128, 32, 1), (2, 128, 32, 2), (4, 64, 32, 0),
+                                             (8, 64, 64, 1)])
 def test_error_bound_and_outliers_exact(bits, Bk, Gv, n_out):
     """|x - x_hat| <= s/2 + 2^-20 (M - m) on dense elements; outliers exact."""
     w = ki.WORKLOADS["gqa8b"]
