@@ -24,6 +24,17 @@
 //   |x| then ascending index; a group with max == min has s = 0 and codes 0; a
 //   group whose every element is an outlier has s = 0, z = 0.
 //
+//   Same page, KVQuant "Non-Uniform KV Cache Quantization": codes may instead
+//     index a calibrated table of levels (a non-uniform grid). Reading: 2^b
+//     sorted levels 0 = l_0 < ... < l_L = 1 on the group's normalized range;
+//     r = fp16_round_up(fp32(max) - fp32(min)) (the range) takes the scale's
+//     slot; u = fp32(fp32(x - z) / r); the code is the nearest level (the
+//     number of binary32 midpoints fp32(0.5 (l_k + l_k+1)) below u; ties to the
+//     lower level); x_hat = z + r * l_code. The table is fitted offline by
+//     one-dimensional k-means (Lloyd) on normalized calibration values with the
+//     end levels held at 0 and 1 (the pages' sensitivity weighting needs
+//     gradients of a model and is left out).
+//
 // Build: g++ -O2 -ffp-contract=off -fPIC -shared (no fast-math, no SIMD
 // intrinsics), so every float operation below is one IEEE-754 binary32 or
 // binary64 operation rounded to nearest.
@@ -156,6 +167,74 @@ int quantize_one(uint16_t x, uint16_t s, uint16_t z, int bits) {
   return static_cast<int>(std::min<double>(n, L));
 }
 
+// ---------------------------------------------------------------- non-uniform codes
+// Range and zero of one group for a level table: r = fp16_round_up(max - min)
+// in binary32, z = min (fp16, -0 stored as +0); an all-outlier group has r = z = 0.
+void group_params_nuq(const std::vector<uint16_t>& elems, uint16_t* r_out, uint16_t* z_out) {
+  if (elems.empty()) {
+    *r_out = 0;
+    *z_out = 0;
+    return;
+  }
+  double mn = INFINITY, mx = -INFINITY;
+  for (uint16_t e : elems) {
+    const double v = half_to_double(e);
+    mn = std::min(mn, v);
+    mx = std::max(mx, v);
+  }
+  uint16_t zb = 0;
+  for (uint16_t e : elems) {
+    if (half_to_double(e) == mn) { zb = e; break; }
+  }
+  if (mn == 0.0) zb = 0;
+  *r_out = float_to_half_up(static_cast<float>(mx) - static_cast<float>(mn));   // binary32, RN, then up
+  *z_out = zb;
+}
+
+// Binary32 midpoints between consecutive levels.
+std::vector<float> level_mids(const float* levels, int L) {
+  std::vector<float> mids(L);
+  for (int k = 0; k < L; ++k) mids[k] = (levels[k] + levels[k + 1]) * 0.5f;
+  return mids;
+}
+
+// Code of one element against a level table: the nearest level of
+// u = fp32(fp32(x - z) / r), i.e. the number of midpoints below u.
+int quantize_nuq(uint16_t x, uint16_t r, uint16_t z, const std::vector<float>& mids) {
+  if ((r & 0x7FFF) == 0) return 0;
+  const float d = half_to_float(x) - half_to_float(z);       // binary32, RN
+  const float u = d / half_to_float(r);                      // binary32, RN
+  int q = 0;
+  for (float m : mids)
+    if (u > m) ++q;
+  return q;
+}
+
+// One-dimensional k-means (Lloyd) of samples u in [0, 1] into 2^b levels,
+// starting from the uniform grid k / L; the end levels stay at 0 and 1, an
+// interior level moves to the mean of the samples nearest to it (a level
+// with no samples stays). binary64 throughout; the result is rounded to binary32.
+void nuq_fit(const double* u, size_t n, int bits, int iters, float* levels_out) {
+  const int L = (1 << bits) - 1;
+  std::vector<double> lv(L + 1);
+  for (int k = 0; k <= L; ++k) lv[k] = static_cast<double>(k) / L;
+  std::vector<double> sum(L + 1), cnt(L + 1), mids(L);
+  for (int it = 0; it < iters; ++it) {
+    for (int k = 0; k < L; ++k) mids[k] = 0.5 * (lv[k] + lv[k + 1]);
+    std::fill(sum.begin(), sum.end(), 0.0);
+    std::fill(cnt.begin(), cnt.end(), 0.0);
+    for (size_t i = 0; i < n; ++i) {
+      int q = 0;
+      while (q < L && u[i] > mids[q]) ++q;                      // the nearest level, ties to the lower
+      sum[q] += u[i];
+      cnt[q] += 1.0;
+    }
+    for (int k = 1; k < L; ++k)
+      if (cnt[k] > 0) lv[k] = sum[k] / cnt[k];
+  }
+  for (int k = 0; k <= L; ++k) levels_out[k] = static_cast<float>(lv[k]);
+}
+
 // LSB-first bit packing of one row: element d occupies bits [b*d, b*d + b).
 void pack_row(const int* codes, int D, int bits, uint8_t* out) {
   const int nbytes = D * bits / 8;
@@ -192,10 +271,19 @@ bool is_outlier(const uint16_t* idx, int n_out, int c) {
 }
 
 // Encode one (batch, kv-head) stream of T tokens.
+// levels: a level table (non-uniform codes) or nullptr (uniform grid).
 void encode_stream(const Shape& sh, const uint16_t* K, const uint16_t* V,
                    uint8_t* k_codes, uint16_t* k_meta, uint16_t* k_tail, uint16_t* k_outl,
-                   uint8_t* v_codes, uint16_t* v_meta, uint16_t* v_outl) {
+                   uint8_t* v_codes, uint16_t* v_meta, uint16_t* v_outl, const float* levels) {
   const int D = sh.D, T = sh.T, n_out = sh.n_out, bits = sh.bits;
+  const std::vector<float> mids = levels ? level_mids(levels, (1 << bits) - 1) : std::vector<float>();
+  auto params = [&](const std::vector<uint16_t>& dense, uint16_t* s, uint16_t* z) {
+    if (levels) group_params_nuq(dense, s, z);
+    else group_params(dense, bits, s, z);
+  };
+  auto code = [&](uint16_t x, uint16_t s, uint16_t z) {
+    return levels ? quantize_nuq(x, s, z, mids) : quantize_one(x, s, z, bits);
+  };
   const int rb = sh.row_bytes();
   const int ng = D / sh.Gv;
   std::vector<uint16_t> oi(std::max(n_out, 1)), ov(std::max(n_out, 1));
@@ -214,10 +302,10 @@ void encode_stream(const Shape& sh, const uint16_t* K, const uint16_t* V,
       for (int c = g * sh.Gv; c < (g + 1) * sh.Gv; ++c)
         if (!is_outlier(oi.data(), n_out, c)) dense.push_back(x[c]);
       uint16_t s, z;
-      group_params(dense, bits, &s, &z);
+      params(dense, &s, &z);
       v_meta[(static_cast<size_t>(t) * ng + g) * 2 + 0] = s;
       v_meta[(static_cast<size_t>(t) * ng + g) * 2 + 1] = z;
-      for (int c = g * sh.Gv; c < (g + 1) * sh.Gv; ++c) codes[c] = quantize_one(x[c], s, z, bits);
+      for (int c = g * sh.Gv; c < (g + 1) * sh.Gv; ++c) codes[c] = code(x[c], s, z);
     }
     pack_row(codes.data(), D, bits, v_codes + static_cast<size_t>(t) * rb);
   }
@@ -243,14 +331,14 @@ void encode_stream(const Shape& sh, const uint16_t* K, const uint16_t* V,
       for (int j = 0; j < sh.Bk; ++j)
         if (!is_outlier(&blk_idx[static_cast<size_t>(j) * n_out], n_out, c))
           dense.push_back(K[static_cast<size_t>(t0 + j) * D + c]);
-      group_params(dense, bits, &s_c[c], &z_c[c]);
+      params(dense, &s_c[c], &z_c[c]);
       k_meta[(static_cast<size_t>(b) * D + c) * 2 + 0] = s_c[c];
       k_meta[(static_cast<size_t>(b) * D + c) * 2 + 1] = z_c[c];
     }
     for (int j = 0; j < sh.Bk; ++j) {
       const int t = t0 + j;
       for (int c = 0; c < D; ++c)
-        codes[c] = quantize_one(K[static_cast<size_t>(t) * D + c], s_c[c], z_c[c], bits);
+        codes[c] = code(K[static_cast<size_t>(t) * D + c], s_c[c], z_c[c]);
       pack_row(codes.data(), D, bits, k_codes + static_cast<size_t>(t) * rb);
     }
   }
@@ -260,10 +348,15 @@ void encode_stream(const Shape& sh, const uint16_t* K, const uint16_t* V,
                 sizeof(uint16_t) * D);
 }
 
-// x_hat = q * s + z (binary64), outlier positions restored, tail keys as fp16.
+// x_hat = q * s + z (binary64; with a level table z + r * l_q), outlier
+// positions restored, tail keys as fp16.
 void dequant_stream(const Shape& sh, const uint8_t* k_codes, const uint16_t* k_meta,
                     const uint16_t* k_tail, const uint16_t* k_outl, const uint8_t* v_codes,
-                    const uint16_t* v_meta, const uint16_t* v_outl, double* Kh, double* Vh) {
+                    const uint16_t* v_meta, const uint16_t* v_outl, double* Kh, double* Vh,
+                    const float* levels) {
+  auto value = [&](int q, double s, double z) {
+    return levels ? z + s * static_cast<double>(levels[q]) : q * s + z;
+  };
   const int D = sh.D, T = sh.T, n_out = sh.n_out, bits = sh.bits;
   const int rb = sh.row_bytes();
   const int ng = D / sh.Gv;
@@ -274,7 +367,7 @@ void dequant_stream(const Shape& sh, const uint8_t* k_codes, const uint16_t* k_m
       const int g = c / sh.Gv;
       const double s = half_to_double(v_meta[(static_cast<size_t>(t) * ng + g) * 2 + 0]);
       const double z = half_to_double(v_meta[(static_cast<size_t>(t) * ng + g) * 2 + 1]);
-      Vh[static_cast<size_t>(t) * D + c] = unpack_one(vr, c, bits) * s + z;
+      Vh[static_cast<size_t>(t) * D + c] = value(unpack_one(vr, c, bits), s, z);
     }
     for (int k = 0; k < n_out; ++k) {
       const uint16_t i = v_outl[(static_cast<size_t>(t) * n_out + k) * 2 + 0];
@@ -287,7 +380,7 @@ void dequant_stream(const Shape& sh, const uint8_t* k_codes, const uint16_t* k_m
       for (int c = 0; c < D; ++c) {
         const double s = half_to_double(k_meta[(static_cast<size_t>(b) * D + c) * 2 + 0]);
         const double z = half_to_double(k_meta[(static_cast<size_t>(b) * D + c) * 2 + 1]);
-        Kh[static_cast<size_t>(t) * D + c] = unpack_one(kr, c, bits) * s + z;
+        Kh[static_cast<size_t>(t) * D + c] = value(unpack_one(kr, c, bits), s, z);
       }
       for (int k = 0; k < n_out; ++k) {
         const uint16_t i = k_outl[(static_cast<size_t>(t) * n_out + k) * 2 + 0];
@@ -376,10 +469,28 @@ bool shape_ok(int T, int D, int bits, int Bk, int Gv, int n_out) {
 
 extern "C" {
 
+int kvqo_encode_levels(int P, int T, int D, int bits, int Bk, int Gv, int n_out, const uint16_t* K,
+                       const uint16_t* V, uint8_t* k_codes, uint16_t* k_meta, uint16_t* k_tail,
+                       uint16_t* k_outl, uint8_t* v_codes, uint16_t* v_meta, uint16_t* v_outl,
+                       const float* levels, int nthreads);
+int kvqo_dequant_levels(int P, int T, int D, int bits, int Bk, int Gv, int n_out, const uint8_t* k_codes,
+                        const uint16_t* k_meta, const uint16_t* k_tail, const uint16_t* k_outl,
+                        const uint8_t* v_codes, const uint16_t* v_meta, const uint16_t* v_outl,
+                        double* Kh, double* Vh, const float* levels, int nthreads);
+
 int kvqo_encode(int P, int T, int D, int bits, int Bk, int Gv, int n_out, const uint16_t* K,
                 const uint16_t* V, uint8_t* k_codes, uint16_t* k_meta, uint16_t* k_tail,
                 uint16_t* k_outl, uint8_t* v_codes, uint16_t* v_meta, uint16_t* v_outl,
                 int nthreads) {
+  return kvqo_encode_levels(P, T, D, bits, Bk, Gv, n_out, K, V, k_codes, k_meta, k_tail, k_outl, v_codes,
+                            v_meta, v_outl, nullptr, nthreads);
+}
+
+// levels: 2^bits sorted binary32 levels (non-uniform codes) or NULL (uniform).
+int kvqo_encode_levels(int P, int T, int D, int bits, int Bk, int Gv, int n_out, const uint16_t* K,
+                       const uint16_t* V, uint8_t* k_codes, uint16_t* k_meta, uint16_t* k_tail,
+                       uint16_t* k_outl, uint8_t* v_codes, uint16_t* v_meta, uint16_t* v_outl,
+                       const float* levels, int nthreads) {
   if (!shape_ok(T, D, bits, Bk, Gv, n_out) || P < 0) return 1;
   const Shape sh{T, D, bits, Bk, Gv, n_out};
   const size_t td = static_cast<size_t>(T) * D;
@@ -393,7 +504,7 @@ int kvqo_encode(int P, int T, int D, int bits, int Bk, int Gv, int n_out, const 
     std::memset(k_outl + p * ol, 0, ol * sizeof(uint16_t));
     std::memset(k_tail + p * kt, 0, kt * sizeof(uint16_t));
     encode_stream(sh, K + p * td, V + p * td, k_codes + p * rows, k_meta + p * km, k_tail + p * kt,
-                  k_outl + p * ol, v_codes + p * rows, v_meta + p * vm, v_outl + p * ol);
+                  k_outl + p * ol, v_codes + p * rows, v_meta + p * vm, v_outl + p * ol, levels);
   });
   return 0;
 }
@@ -402,6 +513,14 @@ int kvqo_dequant(int P, int T, int D, int bits, int Bk, int Gv, int n_out, const
                  const uint16_t* k_meta, const uint16_t* k_tail, const uint16_t* k_outl,
                  const uint8_t* v_codes, const uint16_t* v_meta, const uint16_t* v_outl,
                  double* Kh, double* Vh, int nthreads) {
+  return kvqo_dequant_levels(P, T, D, bits, Bk, Gv, n_out, k_codes, k_meta, k_tail, k_outl, v_codes, v_meta,
+                             v_outl, Kh, Vh, nullptr, nthreads);
+}
+
+int kvqo_dequant_levels(int P, int T, int D, int bits, int Bk, int Gv, int n_out, const uint8_t* k_codes,
+                        const uint16_t* k_meta, const uint16_t* k_tail, const uint16_t* k_outl,
+                        const uint8_t* v_codes, const uint16_t* v_meta, const uint16_t* v_outl,
+                        double* Kh, double* Vh, const float* levels, int nthreads) {
   if (!shape_ok(T, D, bits, Bk, Gv, n_out) || P < 0) return 1;
   const Shape sh{T, D, bits, Bk, Gv, n_out};
   const size_t td = static_cast<size_t>(T) * D;
@@ -412,7 +531,7 @@ int kvqo_dequant(int P, int T, int D, int bits, int Bk, int Gv, int n_out, const
   const size_t vm = static_cast<size_t>(T) * (D / Gv) * 2;
   parallel_for(P, nthreads, [&](int p) {
     dequant_stream(sh, k_codes + p * rows, k_meta + p * km, k_tail + p * kt, k_outl + p * ol,
-                   v_codes + p * rows, v_meta + p * vm, v_outl + p * ol, Kh + p * td, Vh + p * td);
+                   v_codes + p * rows, v_meta + p * vm, v_outl + p * ol, Kh + p * td, Vh + p * td, levels);
   });
   return 0;
 }
@@ -448,6 +567,27 @@ int kvqo_group_params(int n, const uint16_t* x, const uint8_t* excluded, int bit
 
 int kvqo_quantize(int n, const uint16_t* x, uint16_t s, uint16_t z, int bits, int* codes) {
   for (int i = 0; i < n; ++i) codes[i] = quantize_one(x[i], s, z, bits);
+  return 0;
+}
+
+int kvqo_group_params_levels(int n, const uint16_t* x, const uint8_t* excluded, uint16_t* r, uint16_t* z) {
+  std::vector<uint16_t> dense;
+  for (int i = 0; i < n; ++i)
+    if (!excluded || !excluded[i]) dense.push_back(x[i]);
+  group_params_nuq(dense, r, z);
+  return 0;
+}
+
+int kvqo_quantize_levels(int n, const uint16_t* x, uint16_t r, uint16_t z, int bits, const float* levels,
+                         int* codes) {
+  const std::vector<float> mids = level_mids(levels, (1 << bits) - 1);
+  for (int i = 0; i < n; ++i) codes[i] = quantize_nuq(x[i], r, z, mids);
+  return 0;
+}
+
+int kvqo_fit_levels(size_t n, const double* u, int bits, int iters, float* levels) {
+  if (bits < 1 || bits > 8 || iters < 0) return 1;
+  nuq_fit(u, n, bits, iters, levels);
   return 0;
 }
 

@@ -50,6 +50,11 @@ def lib():
         L.kvqo_half_to_double.restype = ctypes.c_double
         L.kvqo_pack_row.argtypes = [i, P, i, P]
         L.kvqo_rope.argtypes = [i, P, d, d, P]
+        L.kvqo_encode_levels.argtypes = [i] * 7 + [P] * 10 + [i]
+        L.kvqo_dequant_levels.argtypes = [i] * 7 + [P] * 10 + [i]
+        L.kvqo_group_params_levels.argtypes = [i, P, P, P, P]
+        L.kvqo_quantize_levels.argtypes = [i, P, ctypes.c_uint16, ctypes.c_uint16, i, P, P]
+        L.kvqo_fit_levels.argtypes = [ctypes.c_size_t, P, i, i, P]
         _lib = L
     return _lib
 
@@ -62,8 +67,10 @@ def default_threads() -> int:
     return max(1, os.cpu_count() or 1)
 
 
-def encode(K, V, bits, Bk, Gv, n_out, nthreads=None):
-    """Encode streams K, V [P, T, D] fp16; same dict layout as ``oracle_np.encode``."""
+def encode(K, V, bits, Bk, Gv, n_out, nthreads=None, levels=None):
+    """Encode streams K, V [P, T, D] fp16; same dict layout as ``oracle_np.encode``.
+    ``levels``: a table of 2^bits sorted levels in [0, 1] (non-uniform codes;
+    the scale slot then holds the group's range), or None (uniform grid)."""
     K = np.ascontiguousarray(K, dtype=np.float16)
     V = np.ascontiguousarray(V, dtype=np.float16)
     P, T, D = K.shape
@@ -78,23 +85,33 @@ def encode(K, V, bits, Bk, Gv, n_out, nthreads=None):
         "v_meta": np.zeros((P, T, D // Gv, 2), np.uint16),
         "v_outl": np.zeros((P, T, n_out, 2), np.uint16),
     }
-    rc = lib().kvqo_encode(P, T, D, bits, Bk, Gv, n_out, _p(K), _p(V), _p(out["k_codes"]),
-                           _p(out["k_meta"]), _p(out["k_tail"]), _p(out["k_outl"]),
-                           _p(out["v_codes"]), _p(out["v_meta"]), _p(out["v_outl"]),
-                           nthreads or default_threads())
+    lv = None if levels is None else _levels(levels, bits)
+    rc = lib().kvqo_encode_levels(P, T, D, bits, Bk, Gv, n_out, _p(K), _p(V), _p(out["k_codes"]),
+                                  _p(out["k_meta"]), _p(out["k_tail"]), _p(out["k_outl"]),
+                                  _p(out["v_codes"]), _p(out["v_meta"]), _p(out["v_outl"]),
+                                  None if lv is None else _p(lv), nthreads or default_threads())
     if rc:
         raise ValueError("oracle encode: bad shape")
     return out
 
 
-def dequant(enc, T, D, bits, Bk, Gv, n_out, nthreads=None):
+def _levels(levels, bits):
+    lv = np.ascontiguousarray(levels, dtype=np.float32)
+    if lv.shape != (1 << bits,) or np.any(np.diff(lv) <= 0):
+        raise ValueError(f"levels: {1 << bits} increasing binary32 values expected")
+    return lv
+
+
+def dequant(enc, T, D, bits, Bk, Gv, n_out, nthreads=None, levels=None):
     P = enc["v_codes"].shape[0]
     Kh = np.zeros((P, T, D), np.float64)
     Vh = np.zeros((P, T, D), np.float64)
     e = {k: np.ascontiguousarray(v) for k, v in enc.items()}
-    rc = lib().kvqo_dequant(P, T, D, bits, Bk, Gv, n_out, _p(e["k_codes"]), _p(e["k_meta"]),
-                            _p(e["k_tail"]), _p(e["k_outl"]), _p(e["v_codes"]), _p(e["v_meta"]),
-                            _p(e["v_outl"]), _p(Kh), _p(Vh), nthreads or default_threads())
+    lv = None if levels is None else _levels(levels, bits)
+    rc = lib().kvqo_dequant_levels(P, T, D, bits, Bk, Gv, n_out, _p(e["k_codes"]), _p(e["k_meta"]),
+                                   _p(e["k_tail"]), _p(e["k_outl"]), _p(e["v_codes"]), _p(e["v_meta"]),
+                                   _p(e["v_outl"]), _p(Kh), _p(Vh), None if lv is None else _p(lv),
+                                   nthreads or default_threads())
     if rc:
         raise ValueError("oracle dequant: bad shape")
     return Kh, Vh
@@ -161,3 +178,31 @@ def rope(x, pos, theta):
     y = np.zeros_like(x)
     lib().kvqo_rope(x.size, _p(x), float(pos), float(theta), _p(y))
     return y
+
+
+def group_params_levels(x, excluded=None):
+    """Range r (fp16, rounded up) and zero z of one group, for a level table."""
+    x = np.ascontiguousarray(x, dtype=np.float16)
+    ex = None if excluded is None else np.ascontiguousarray(excluded, dtype=np.uint8)
+    r = np.zeros(1, np.uint16)
+    z = np.zeros(1, np.uint16)
+    lib().kvqo_group_params_levels(x.size, _p(x), None if ex is None else _p(ex), _p(r), _p(z))
+    return r.view(np.float16)[0], z.view(np.float16)[0]
+
+
+def quantize_levels(x, r, z, bits, levels):
+    x = np.ascontiguousarray(x, dtype=np.float16)
+    codes = np.zeros(x.size, np.int32)
+    lv = _levels(levels, bits)
+    lib().kvqo_quantize_levels(x.size, _p(x), int(np.float16(r).view(np.uint16)),
+                               int(np.float16(z).view(np.uint16)), bits, _p(lv), _p(codes))
+    return codes
+
+
+def fit_levels(u, bits, iters=100):
+    """Level table of 2^bits values fitted to samples u in [0, 1] (1-D k-means)."""
+    u = np.ascontiguousarray(u, dtype=np.float64)
+    lv = np.zeros(1 << bits, np.float32)
+    if lib().kvqo_fit_levels(u.size, _p(u), bits, int(iters), _p(lv)):
+        raise ValueError("bad bits or iters")
+    return lv

@@ -15,10 +15,17 @@ Definitions (KV Cache量化技术介绍, developer.horizon.auto/blog/13163):
     left out of the dense statistics.
   * Quanto, steps 1-2: block-wise quantization; every block keeps a scale and a
     zero_point to restore its values (the formula image is lost on the page).
+  * KVQuant, "Non-Uniform KV Cache Quantization": codes index a calibrated
+    table of levels instead of a uniform grid.
 Readings taken where the page is silent (they match the C++ oracle):
   q = clamp(rint_half_even(fp32(fp32(x - z) / s)), 0, 2^b - 1), z = block min
   (fp16, -0 stored as +0), s = fp16_round_up(fp32(fp32(max - min) / (2^b - 1))),
   x_hat = q*s + z; s = 0 gives codes 0; an all-outlier group has s = z = 0.
+  With a level table 0 = l_0 < ... < l_L = 1: r = fp16_round_up(fp32(max) -
+  fp32(min)) in the scale's slot, u = fp32(fp32(x - z) / r), q = the number of
+  binary32 midpoints fp32(0.5 (l_k + l_k+1)) below u (nearest level, ties to
+  the lower), x_hat = z + r * l_q. Tables come from 1-D k-means (Lloyd) on
+  normalized calibration values, end levels held at 0 and 1.
 """
 from __future__ import annotations
 
@@ -27,6 +34,7 @@ import numpy as np
 __all__ = [
     "half_up", "select_outliers", "group_params", "quantize", "pack_rows",
     "unpack_rows", "encode", "dequant", "rope", "attention",
+    "group_params_levels", "quantize_levels", "fit_levels",
 ]
 
 
@@ -86,6 +94,54 @@ def quantize(x, s, z, bits):
     return q.astype(np.uint8)
 
 
+def group_params_levels(x, excluded, axis):
+    """Range r = fp16_round_up(fp32(max - min)) and zero z of the groups of
+    ``x`` along ``axis``, for a level table (fp16 in/out)."""
+    xf = x.astype(np.float32)
+    big = np.float32(np.inf)
+    mn = np.where(excluded, big, xf).min(axis=axis)
+    mx = np.where(excluded, -big, xf).max(axis=axis)
+    empty = np.all(excluded, axis=axis)
+    with np.errstate(invalid="ignore"):
+        r = half_up(np.where(empty, np.float32(0), (mx - mn).astype(np.float32)))
+    z = np.where(empty, np.float32(0), mn).astype(np.float16)
+    z = np.where(z == 0, np.float16(0), z)
+    return r, z
+
+
+def quantize_levels(x, r, z, levels):
+    """Nearest level of u = fp32(fp32(x - z) / r): the count of binary32
+    midpoints below u; r == 0 -> 0."""
+    lv = np.asarray(levels, dtype=np.float32)
+    mids = ((lv[:-1] + lv[1:]) * np.float32(0.5)).astype(np.float32)
+    xf = np.asarray(x, dtype=np.float16).astype(np.float32)
+    rf = np.asarray(r, dtype=np.float16).astype(np.float32)
+    zf = np.asarray(z, dtype=np.float16).astype(np.float32)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        u = ((xf - zf).astype(np.float32) / rf).astype(np.float32)
+    q = (u[..., None] > mids).sum(axis=-1)
+    return np.where(rf == 0, 0, q).astype(np.uint8)
+
+
+def fit_levels(u, bits, iters=100):
+    """1-D k-means of samples u in [0, 1] into 2^bits levels: start at k / L,
+    hold l_0 = 0 and l_L = 1, move each interior level to the mean of the
+    samples nearest to it (ties to the lower level; a level without samples
+    stays); binary64, returned as binary32."""
+    u = np.asarray(u, dtype=np.float64).ravel()
+    L = (1 << bits) - 1
+    lv = np.arange(L + 1, dtype=np.float64) / L
+    for _ in range(iters):
+        mids = 0.5 * (lv[:-1] + lv[1:])
+        cell = np.searchsorted(mids, u, side="left")          # number of midpoints strictly below u
+        cnt = np.bincount(cell, minlength=L + 1)
+        tot = np.bincount(cell, weights=u, minlength=L + 1)
+        inner = np.arange(1, L)
+        has = cnt[inner] > 0
+        lv[inner[has]] = tot[inner[has]] / cnt[inner[has]]
+    return lv.astype(np.float32)
+
+
 def pack_rows(codes, bits):
     """LSB-first bitstream per row: element d at bits [b*d, b*d + b)."""
     codes = np.asarray(codes, dtype=np.uint8)
@@ -108,9 +164,10 @@ def _outlier_mask(idx, D):
     return mask
 
 
-def encode(K, V, bits, Bk, Gv, n_out):
+def encode(K, V, bits, Bk, Gv, n_out, levels=None):
     """Encode streams K, V of shape [P, T, D] (fp16). Returns a dict of arrays
-    laid out like the C++ oracle's outputs."""
+    laid out like the C++ oracle's outputs. ``levels``: a level table
+    (non-uniform codes) or None (uniform grid)."""
     K = np.asarray(K, dtype=np.float16)
     V = np.asarray(V, dtype=np.float16)
     P, T, D = K.shape
@@ -121,15 +178,23 @@ def encode(K, V, bits, Bk, Gv, n_out):
     vi, vv = select_outliers(V, n_out)
     vmask = _outlier_mask(vi, D)
     Vg = V.reshape(P, T, ng, Gv)
-    vs, vz = group_params(Vg, vmask.reshape(P, T, ng, Gv), bits, axis=-1)
-    vq = quantize(Vg, vs[..., None], vz[..., None], bits).reshape(P, T, D)
+    if levels is None:
+        vs, vz = group_params(Vg, vmask.reshape(P, T, ng, Gv), bits, axis=-1)
+        vq = quantize(Vg, vs[..., None], vz[..., None], bits).reshape(P, T, D)
+    else:
+        vs, vz = group_params_levels(Vg, vmask.reshape(P, T, ng, Gv), axis=-1)
+        vq = quantize_levels(Vg, vs[..., None], vz[..., None], levels).reshape(P, T, D)
 
     # Keys: completed blocks only; one (s, z) per block and channel.
     Kb = K[:, : nb * Bk].reshape(P, nb, Bk, D)
     ki, kv = select_outliers(Kb, n_out)
     kmask = _outlier_mask(ki, D)
-    ks, kz = group_params(Kb, kmask, bits, axis=2)                  # [P, nb, D]
-    kq = quantize(Kb, ks[:, :, None, :], kz[:, :, None, :], bits).reshape(P, nb * Bk, D)
+    if levels is None:
+        ks, kz = group_params(Kb, kmask, bits, axis=2)              # [P, nb, D]
+        kq = quantize(Kb, ks[:, :, None, :], kz[:, :, None, :], bits).reshape(P, nb * Bk, D)
+    else:
+        ks, kz = group_params_levels(Kb, kmask, axis=2)
+        kq = quantize_levels(Kb, ks[:, :, None, :], kz[:, :, None, :], levels).reshape(P, nb * Bk, D)
 
     rb = D * bits // 8
     k_codes = np.zeros((P, T, rb), dtype=np.uint8)
@@ -151,16 +216,19 @@ def encode(K, V, bits, Bk, Gv, n_out):
     }
 
 
-def dequant(enc, T, D, bits, Bk, Gv, n_out):
-    """x_hat = q*s + z in float64, outliers restored, tail keys as fp16."""
+def dequant(enc, T, D, bits, Bk, Gv, n_out, levels=None):
+    """x_hat = q*s + z (with a level table: z + r * l_q) in float64, outliers
+    restored, tail keys as fp16."""
     P = enc["v_codes"].shape[0]
     ng = D // Gv
     nb = T // Bk
-    vq = unpack_rows(enc["v_codes"], D, bits).astype(np.float64).reshape(P, T, ng, Gv)
+    step = (lambda q: q.astype(np.float64)) if levels is None else (
+        lambda q: np.asarray(levels, dtype=np.float32).astype(np.float64)[q])
+    vq = step(unpack_rows(enc["v_codes"], D, bits)).reshape(P, T, ng, Gv)
     vmeta = enc["v_meta"].view(np.float16).astype(np.float64)
     Vh = (vq * vmeta[..., 0:1] + vmeta[..., 1:2]).reshape(P, T, D)
     Kh = np.empty((P, T, D), dtype=np.float64)
-    kq = unpack_rows(enc["k_codes"][:, : nb * Bk], D, bits).astype(np.float64).reshape(P, nb, Bk, D)
+    kq = step(unpack_rows(enc["k_codes"][:, : nb * Bk], D, bits)).reshape(P, nb, Bk, D)
     kmeta = enc["k_meta"].view(np.float16).astype(np.float64)          # [P, nb, D, 2]
     Kh[:, : nb * Bk] = (kq * kmeta[:, :, None, :, 0] + kmeta[:, :, None, :, 1]).reshape(P, nb * Bk, D)
     Kh[:, nb * Bk:] = enc["k_tail"][:, : T - nb * Bk].astype(np.float64)
