@@ -604,6 +604,77 @@ def run_paged(args, w, rank, world, device):
     }
 
 
+def run_levels(args, w, rank, world, device):
+    """Non-uniform codes: a level table fitted (kvq_fit_levels) to the
+    normalized values of another layer's groups; the cache is filled with
+    kvq_append_levels (whole key blocks) and each step times one
+    kvq_decode_attn_levels call over T tokens (the CUDA-core kernels)."""
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import bit_quantized_kv_append_gb300 as kvq
+
+    T = w.T
+    Kc, Vc = ki.streams_np(w, [(0, 0)], 1024, layer=9)
+    x = np.concatenate([Kc.reshape(-1, w.value_group), Vc.reshape(-1, w.value_group)]).astype(np.float64)
+    span = x.max(axis=1, keepdims=True) - x.min(axis=1, keepdims=True)
+    levels = kvq.fit_levels(((x - x.min(axis=1, keepdims=True)) / np.where(span > 0, span, 1.0)).ravel(), w.bits, 60)
+    cache = kvq.QuantizedKVCache(w.B, w.H_kv, w.D, T + w.key_block, w.bits, w.key_block, w.value_group,
+                                 w.outlier_frac, H_q=w.H_q, rope_theta=w.rope_theta, device=device)
+    stream = torch.cuda.current_stream()
+    chunk = 1 << 15
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for t0 in range(0, T, chunk):
+        K, V = ki.kv_torch(w, 0, t0, min(chunk, T - t0), device)
+        cache.append_levels(K, V, levels)
+    a1.record(stream)
+    q = ki.queries_torch(w, 0, 1, device)
+    out = torch.empty_like(q)
+    for _ in range(args.warmup):
+        cache.decode_levels(q, levels, out=out)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = ClockSampler(physical_gpu(torch.cuda.current_device()))
+    clocks.start()
+    time.sleep(0.3)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        cache.decode_levels(q, levels, out=out)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_end)
+    (ms,) = max_over_ranks([ms], device)
+    dec_ms = ms / args.steps
+    alg = decode_alg_bytes(w, T)
+    peak, peak_kind = measured_peaks()
+    achieved = alg / (dec_ms * 1e-3) / 1e9
+    return {
+        "metric": "decode-attn tokens/s (one layer; B query tokens per step), non-uniform codes",
+        "value": replica_throughput(w.B * args.steps, world, ms), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dec_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": f"u{w.bits}/f16/f32", "data": "synthetic",
+        "config": {
+            "workload": (f"{w.name} with a {1 << w.bits}-level table: B={w.B} H_q={w.H_q} H_kv={w.H_kv} D={w.D} "
+                         f"T={T} INT{w.bits} key_block={w.key_block} value_group={w.value_group} "
+                         f"outliers={w.outlier_frac} rope_theta={w.rope_theta}"),
+            "step": "kvq_decode_attn_levels over T tokens",
+            "append_ms_whole_context_with_input_generation": a0.elapsed_time(a1),
+            "l2": f"inputs larger than L2 (cache {cache.layout.cache_bytes / 1e9:.2f} GB > 129 MB); no flush",
+            "parallelism": f"replicas x{world}",
+        },
+        "gpu_launches": 2 * args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": peak_kind, "kernel": "decode_levels_kernel + combine (CUDA cores)",
+                     "alg_bytes_per_launch": alg, "traffic": None},
+        "clocks": clk,
+    }
+
+
 def run_reference(args, w):
     """The CPU oracle as the reference arm: each step a bounded sample of the
     workload's decode step, extrapolated to the full step."""
@@ -644,7 +715,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--workload", default="mha7b", choices=list(ki.WORKLOADS))
-    ap.add_argument("--mode", default="decode", choices=["decode", "prefill", "paged"])
+    ap.add_argument("--mode", default="decode", choices=["decode", "prefill", "paged", "levels"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -670,7 +741,8 @@ def main():
         dist.barrier()
     device = torch.device("cuda", local_rank if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(device)
-    line = {"prefill": run_prefill, "paged": run_paged, "decode": run_decode}[args.mode](args, w, rank, world, device)
+    line = {"prefill": run_prefill, "paged": run_paged, "decode": run_decode,
+            "levels": run_levels}[args.mode](args, w, rank, world, device)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()

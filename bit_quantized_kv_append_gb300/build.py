@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libkvq.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["kvq_api.cu", "kvq_rope.cu", "kvq_append.cu", "kvq_decode.cu",
+SOURCES = ["kvq_api.cu", "kvq_rope.cu", "kvq_append.cu", "kvq_decode.cu", "kvq_levels.cu",
            "kvq_decode_b2.cu", "kvq_decode_b3.cu", "kvq_decode_b4.cu", "kvq_decode_b8.cu",
            "kvq_decode_tc_b2.cu", "kvq_decode_tc_b3.cu", "kvq_decode_tc_b4.cu",
            "kvq_decode_tc_b2o.cu", "kvq_decode_tc_b3o.cu", "kvq_decode_tc_b4o.cu",

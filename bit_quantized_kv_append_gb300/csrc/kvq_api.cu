@@ -4,9 +4,12 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "kvq_common.cuh"
+#include "kvq_levels.cuh"
 
 namespace kvq {
 namespace {
@@ -141,6 +144,21 @@ int noalloc_scratch(float** out) {
   }
   *out = addr[dev];
   return KVQ_OK;
+}
+
+// A level table from the caller's 2^bits levels: 0 first, 1 last, strictly
+// increasing and finite; the midpoints are formed here in binary32.
+bool make_levels(const float* levels, int bits, LevelTable* t) {
+  if (!levels) return false;
+  const int L = (1 << bits) - 1;
+  if (!(levels[0] == 0.0f) || !(levels[L] == 1.0f)) return false;
+  for (int k = 0; k < L; ++k)
+    if (!(levels[k] < levels[k + 1])) return false;
+  memset(t, 0, sizeof(*t));
+  t->L = L;
+  for (int k = 0; k <= L; ++k) t->lv[k] = levels[k];
+  for (int k = 0; k < L; ++k) t->mid[k] = (levels[k] + levels[k + 1]) * 0.5f;
+  return true;
 }
 
 }  // namespace
@@ -338,6 +356,73 @@ int kvq_paged_decode_attn(const kvq_config* cfg, const kvq_paged_cache* cache, c
   return cuda_status(launch_decode(d, pool_view(*cache), static_cast<const __half*>(q), H_q, 0,
                                    static_cast<const float2*>(rope_tab), sm_scale, static_cast<__half*>(out),
                                    static_cast<float*>(workspace), static_cast<cudaStream_t>(stream), 0, &pg));
+}
+
+int kvq_fit_levels(const double* u, size_t n, int32_t bits, int32_t iters, float* levels) {
+  if (!u || !levels || iters < 0) return KVQ_ERR_ARG;
+  if (bits != 2 && bits != 3 && bits != 4 && bits != 8) return KVQ_ERR_UNSUPPORTED;
+  const int L = (1 << bits) - 1;
+  // Lloyd iterations on the sorted samples: a cell is a run of the sorted
+  // values, found by binary search; its mean comes from prefix sums.
+  std::vector<double> x(u, u + n);
+  for (double v : x)
+    if (!(v >= 0.0 && v <= 1.0)) return KVQ_ERR_ARG;
+  std::sort(x.begin(), x.end());
+  std::vector<double> pre(n + 1, 0.0);
+  for (size_t i = 0; i < n; ++i) pre[i + 1] = pre[i] + x[i];
+  std::vector<double> lv(L + 1), edge(L + 1);
+  for (int k = 0; k <= L; ++k) lv[k] = (double)k / L;
+  for (int it = 0; it < iters; ++it) {
+    // cell k holds the samples in (mid_{k-1}, mid_k]: ties go to the lower level
+    edge[0] = 0;
+    for (int k = 0; k < L; ++k) {
+      const double mid = 0.5 * (lv[k] + lv[k + 1]);
+      edge[k + 1] = (double)(std::upper_bound(x.begin(), x.end(), mid) - x.begin());
+    }
+    for (int k = 1; k < L; ++k) {
+      const size_t lo = (size_t)edge[k], hi = (size_t)edge[k + 1];
+      if (hi > lo) lv[k] = (pre[hi] - pre[lo]) / (double)(hi - lo);
+    }
+  }
+  for (int k = 0; k <= L; ++k) levels[k] = (float)lv[k];
+  return KVQ_OK;
+}
+
+int kvq_append_levels(const kvq_config* cfg, kvq_cache* cache, const void* k_new, const void* v_new,
+                      int32_t n_new, const float* levels, void* stream) {
+  Dims d;
+  int rc = make_dims(cfg, &d);
+  if (rc) return rc;
+  if (!cache || n_new < 0 || !cache_ptrs_ok(d, *cache)) return KVQ_ERR_ARG;
+  LevelTable t;
+  if (!make_levels(levels, d.bits, &t)) return KVQ_ERR_ARG;
+  if (n_new == 0) return KVQ_OK;
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_ARG;
+  if (cache->T_cur % d.Bk || n_new % d.Bk) return KVQ_ERR_UNSUPPORTED;   // whole key blocks only
+  if ((int64_t)cache->T_cur + n_new > d.T_max) return KVQ_ERR_CAPACITY;
+  rc = cuda_status(launch_append_levels(d, *cache, static_cast<const __half*>(k_new),
+                                        static_cast<const __half*>(v_new), n_new, t,
+                                        static_cast<cudaStream_t>(stream)));
+  if (rc == KVQ_OK) cache->T_cur += n_new;
+  return rc;
+}
+
+int kvq_decode_attn_levels(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t H_q,
+                           int32_t q_pos, const void* rope_tab, float sm_scale, void* out, void* workspace,
+                           size_t workspace_bytes, const float* levels, void* stream) {
+  Dims d;
+  int rc = make_dims(cfg, &d);
+  if (rc) return rc;
+  rc = decode_checks(cfg, d, cache, cache ? cache->T_cur : 0, q, H_q, q_pos, rope_tab, sm_scale, out,
+                     workspace, workspace_bytes);
+  if (rc) return rc;
+  LevelTable t;
+  if (!make_levels(levels, d.bits, &t)) return KVQ_ERR_ARG;
+  if (cache->T_cur % d.Bk) return KVQ_ERR_UNSUPPORTED;                     // whole key blocks only
+  return cuda_status(launch_decode_levels(d, *cache, static_cast<const __half*>(q), H_q, q_pos,
+                                          static_cast<const float2*>(rope_tab), sm_scale,
+                                          static_cast<__half*>(out), static_cast<float*>(workspace), t,
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 const char* kvq_status_string(int status) {

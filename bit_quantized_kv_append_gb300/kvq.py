@@ -6,7 +6,8 @@ library is missing, the calls raise.
 
 Entry points mirror include/kvq.h: ``layout``, ``rope_init``, ``append``,
 ``decode_attn``, ``decode_step``, ``decode_attn_noalloc``, ``paged_layout``,
-``paged_append``, ``paged_decode_attn``. ``QuantizedKVCache`` owns one layer's
+``paged_append``, ``paged_decode_attn``, ``fit_levels``, ``append_levels``,
+``decode_attn_levels``. ``QuantizedKVCache`` owns one layer's
 buffers; ``PagedKVCache`` owns the pools, block table and lengths of a paged,
 ragged batch.
 """
@@ -25,6 +26,7 @@ STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "KVQ_ERR_C
           4: "KVQ_ERR_WORKSPACE", 5: "KVQ_ERR_CUDA"}
 EXPORTS = ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_decode_attn", "kvq_decode_step",
            "kvq_paged_layout", "kvq_paged_append", "kvq_paged_decode_attn",
+           "kvq_fit_levels", "kvq_append_levels", "kvq_decode_attn_levels",
            "kvq_decode_attn_noalloc", "kvq_status_string", "kvq_version")
 
 
@@ -82,13 +84,18 @@ def lib():
         L.kvq_paged_append.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(PagedCacheRef), vp, vp, i32, vp]
         L.kvq_paged_decode_attn.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(PagedCacheRef), vp, i32, vp,
                                             ctypes.c_float, vp, vp, ctypes.c_size_t, vp]
+        L.kvq_fit_levels.argtypes = [vp, ctypes.c_size_t, i32, i32, vp]
+        L.kvq_append_levels.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp, vp, i32, vp, vp]
+        L.kvq_decode_attn_levels.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp, i32, i32, vp,
+                                             ctypes.c_float, vp, vp, ctypes.c_size_t, vp, vp]
         L.kvq_decode_attn_noalloc.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp,
                                               i32, i32, vp, ctypes.c_float, vp, vp]
         L.kvq_status_string.argtypes = [ctypes.c_int]
         L.kvq_status_string.restype = ctypes.c_char_p
         L.kvq_version.restype = ctypes.c_char_p
         for fn in ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_decode_attn", "kvq_decode_step",
-                   "kvq_paged_layout", "kvq_paged_append", "kvq_paged_decode_attn", "kvq_decode_attn_noalloc"):
+                   "kvq_paged_layout", "kvq_paged_append", "kvq_paged_decode_attn", "kvq_fit_levels",
+                   "kvq_append_levels", "kvq_decode_attn_levels", "kvq_decode_attn_noalloc"):
             getattr(L, fn).restype = ctypes.c_int
         _LIB = L
     return _LIB
@@ -153,6 +160,41 @@ def decode_step(cfg: Config, ref: CacheRef, k_new: torch.Tensor, v_new: torch.Te
     _check(lib().kvq_decode_step(ctypes.byref(cfg), ctypes.byref(ref), _ptr(k_new), _ptr(v_new), _ptr(q),
                                  int(H_q), _ptr(rope), float(sm_scale), _ptr(out), _ptr(workspace),
                                  workspace.numel(), _stream(stream)), "kvq_decode_step")
+
+
+def _host_levels(levels, bits):
+    import numpy as np
+    lv = np.ascontiguousarray(levels, dtype=np.float32)
+    if lv.shape != (1 << bits,):
+        raise ValueError(f"expected {1 << bits} levels, got {lv.shape}")
+    return lv
+
+
+def fit_levels(u, bits: int, iters: int = 100):
+    """kvq_fit_levels: 2^bits levels (numpy float32) fitted to samples u in [0, 1]."""
+    import numpy as np
+    x = np.ascontiguousarray(u, dtype=np.float64).ravel()
+    lv = np.zeros(1 << bits, np.float32)
+    _check(lib().kvq_fit_levels(x.ctypes.data_as(ctypes.c_void_p), x.size, int(bits), int(iters),
+                                lv.ctypes.data_as(ctypes.c_void_p)), "kvq_fit_levels")
+    return lv
+
+
+def append_levels(cfg: Config, ref: CacheRef, k_new: torch.Tensor, v_new: torch.Tensor, n_new: int, levels,
+                  stream=None):
+    lv = _host_levels(levels, cfg.bits)
+    _check(lib().kvq_append_levels(ctypes.byref(cfg), ctypes.byref(ref), _ptr(k_new), _ptr(v_new), int(n_new),
+                                   lv.ctypes.data_as(ctypes.c_void_p), _stream(stream)), "kvq_append_levels")
+
+
+def decode_attn_levels(cfg: Config, ref: CacheRef, q: torch.Tensor, H_q: int, q_pos: int,
+                       rope: Optional[torch.Tensor], sm_scale: float, out: torch.Tensor,
+                       workspace: torch.Tensor, levels, stream=None):
+    lv = _host_levels(levels, cfg.bits)
+    _check(lib().kvq_decode_attn_levels(ctypes.byref(cfg), ctypes.byref(ref), _ptr(q), int(H_q), int(q_pos),
+                                        _ptr(rope), float(sm_scale), _ptr(out), _ptr(workspace),
+                                        workspace.numel(), lv.ctypes.data_as(ctypes.c_void_p), _stream(stream)),
+           "kvq_decode_attn_levels")
 
 
 def decode_attn_noalloc(cfg: Config, ref: CacheRef, q: torch.Tensor, H_q: int, q_pos: int,
@@ -246,6 +288,36 @@ class QuantizedKVCache:
         sm_scale = 1.0 / math.sqrt(c.D) if sm_scale is None else sm_scale
         decode_attn(self.cfg, self.ref(), q, self.H_q, q_pos, self.rope, sm_scale, out,
                     self.workspace, stream)
+        return out
+
+    def append_levels(self, k_new: torch.Tensor, v_new: torch.Tensor, levels, stream=None):
+        """Non-uniform codes against the level table ``levels`` (2^bits values,
+        0 first, 1 last, increasing); whole key blocks only."""
+        c = self.cfg
+        for t in (k_new, v_new):
+            if t.dtype != torch.float16 or not t.is_contiguous() or t.device != self.device:
+                raise ValueError("k_new/v_new must be contiguous fp16 tensors on the cache device")
+            if t.dim() != 4 or t.shape[0] != c.B or t.shape[1] != c.H_kv or t.shape[3] != c.D:
+                raise ValueError(f"expected [B={c.B}, H_kv={c.H_kv}, n, D={c.D}], got {tuple(t.shape)}")
+        ref = self.ref()
+        append_levels(self.cfg, ref, k_new, v_new, k_new.shape[2], levels, stream)
+        self.T_cur = ref.T_cur
+
+    def decode_levels(self, q: torch.Tensor, levels, q_pos: Optional[int] = None,
+                      sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                      stream=None) -> torch.Tensor:
+        """Decode attention over a cache filled by append_levels with the same table."""
+        c = self.cfg
+        if q.dtype != torch.float16 or not q.is_contiguous() or q.device != self.device:
+            raise ValueError("q must be a contiguous fp16 tensor on the cache device")
+        if tuple(q.shape) != (c.B, self.H_q, c.D):
+            raise ValueError(f"expected q [B={c.B}, H_q={self.H_q}, D={c.D}], got {tuple(q.shape)}")
+        if out is None:
+            out = torch.empty_like(q)
+        q_pos = self.T_cur - 1 if q_pos is None else q_pos
+        sm_scale = 1.0 / math.sqrt(c.D) if sm_scale is None else sm_scale
+        decode_attn_levels(self.cfg, self.ref(), q, self.H_q, q_pos, self.rope, sm_scale, out, self.workspace,
+                           levels, stream)
         return out
 
     def decode_step(self, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor,

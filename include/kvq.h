@@ -278,6 +278,41 @@ KVQ_API int kvq_paged_decode_attn(const kvq_config* cfg, const kvq_paged_cache* 
                                   int32_t H_q, const void* rope_tab, float sm_scale, void* out,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---- Non-uniform codes (page 3, KVQuant "Non-Uniform KV Cache Quantization":
+ * a calibrated format instead of the uniform grid). A level table holds
+ * 2^bits binary32 levels 0 = l_0 < l_1 < ... < l_L = 1 on a group's
+ * normalized range. Groups, outliers, buffers and packing are those of
+ * kvq_append; per group the scale's slot holds the range
+ * r = fp16_round_up(fp32(max) - fp32(min)) of the dense elements, the code of
+ * x is the nearest level of u = fp32(fp32(x - z) / r) (the number of binary32
+ * midpoints fp32(0.5 (l_k + l_k+1)) below u, ties to the lower level; r = 0
+ * gives 0), and x_hat = z + r * l_code. These calls run CUDA-core kernels for
+ * caches filled in whole key blocks (no fp16 tail). */
+
+/* Level table of 2^bits levels fitted to calibration samples u[0..n) in
+ * [0, 1] (normalized dense values, e.g. (x - min) / (max - min) of groups of
+ * representative keys or values): one-dimensional k-means (Lloyd) started
+ * from the uniform grid k / L, with the end levels held at 0 and 1; a level
+ * whose cell is empty stays. Host memory only; touches no device.
+ * Errors: KVQ_ERR_ARG (NULL, iters < 0, a sample outside [0, 1]),
+ * KVQ_ERR_UNSUPPORTED (bits not in {2, 3, 4, 8}). */
+KVQ_API int kvq_fit_levels(const double* u, size_t n, int32_t bits, int32_t iters, float* levels);
+
+/* kvq_append with non-uniform codes. levels: host pointer to the 2^bits
+ * levels of the table (copied into the launch). T_cur and n_new must be
+ * multiples of key_block. Errors: those of kvq_append; KVQ_ERR_ARG for a
+ * table that does not start at 0, end at 1 and increase; KVQ_ERR_UNSUPPORTED
+ * for a partial key block. */
+KVQ_API int kvq_append_levels(const kvq_config* cfg, kvq_cache* cache, const void* k_new, const void* v_new,
+                              int32_t n_new, const float* levels, void* stream);
+
+/* kvq_decode_attn over a cache appended with kvq_append_levels and the same
+ * table (T_cur a multiple of key_block). Errors: those of kvq_decode_attn;
+ * KVQ_ERR_ARG for a bad table; KVQ_ERR_UNSUPPORTED for a partial key block. */
+KVQ_API int kvq_decode_attn_levels(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t H_q,
+                                   int32_t q_pos, const void* rope_tab, float sm_scale, void* out,
+                                   void* workspace, size_t workspace_bytes, const float* levels, void* stream);
+
 /* Static, human-readable name of a status code. */
 KVQ_API const char* kvq_status_string(int status);
 

@@ -250,3 +250,44 @@ def test_paged_host_errors(lib):
     assert dec(rope=ctypes.c_void_p(FAKE + 8)) == 1
     assert dec(scale=float("inf")) == 1
     assert dec(c=_fake_paged(10, n_blocks=-3)) == 1
+
+
+def test_fit_levels_matches_the_oracle_fit(lib):
+    import numpy as np
+    from oracle import oracle_cpp as oc
+    rng = np.random.default_rng(31)
+    for bits in (2, 3, 4, 8):
+        u = rng.beta(2.0, 4.0, 5000)
+        got = kvq.fit_levels(u, bits, 60)
+        want = oc.fit_levels(u, bits, 60)
+        assert got[0] == 0 and got[-1] == 1 and np.all(np.diff(got) > 0)
+        # the two sum a cell's samples in different orders: within a binary32 ulp
+        assert np.all(np.abs(got.astype(np.float64) - want.astype(np.float64)) <= np.spacing(want))
+    bad = np.array([0.5, 1.2])
+    with pytest.raises(kvq.KvqError):
+        kvq.fit_levels(bad, 2)
+
+
+def test_levels_host_errors(lib):
+    import numpy as np
+    cfg = _cfg()                                    # bits 4, Bk 64, T_max 256, n_out 1
+    p = ctypes.c_void_p(FAKE)
+    good = np.linspace(0, 1, 16).astype(np.float32)
+    lv = lambda a: np.ascontiguousarray(a, dtype=np.float32).ctypes.data_as(ctypes.c_void_p)
+    r = _fake_cache(64)
+    app = lambda levels, n=64, c=r: lib.kvq_append_levels(ctypes.byref(cfg), ctypes.byref(c), p, p, n, levels, None)
+    assert app(lv(good), n=32) == 2                     # a partial key block
+    assert app(lv(good), c=_fake_cache(10)) == 2         # cache not at a block edge
+    assert app(lv(good), n=256) == 3                     # capacity
+    not_zero = good.copy(); not_zero[0] = 0.01
+    not_one = good.copy(); not_one[-1] = 0.99
+    flat = good.copy(); flat[5] = flat[4]
+    for bad in (not_zero, not_one, flat):
+        assert app(lv(bad)) == 1
+    assert app(None) == 1
+    assert r.T_cur == 64
+    lay = kvq.layout(cfg, 8)
+    dec = lambda levels, c=r: lib.kvq_decode_attn_levels(ctypes.byref(cfg), ctypes.byref(c), p, 8, 63, None, 0.1, p,
+                                                         p, lay.workspace_bytes, levels, None)
+    assert dec(lv(flat)) == 1
+    assert dec(lv(good), c=_fake_cache(70)) == 2        # not whole blocks
