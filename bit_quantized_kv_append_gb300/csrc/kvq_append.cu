@@ -96,9 +96,12 @@ __device__ __forceinline__ float rcp_or_zero(float s) {
 // rounding of y is that of Q. Near
 // a half-integer h the exact residual rho = (x - z) - h*s (one fma, exact) and
 // half an ulp of h, times s (exact), tell whether Q rounds to h (then ties go
-// to the even integer) or to a neighbour. Beyond [-0.75, L + 0.75] the clamp
-// decides.
-__device__ __forceinline__ uint32_t exact_code(float x, float z, float s, float r, int L) {
+// to the even integer) or to a neighbour; "near" is the width's tie guard,
+// which exceeds the distance between y and Q. Beyond [-0.75, L + 0.75] the
+// clamp decides.
+template <int BITS>
+__device__ __forceinline__ uint32_t exact_code(float x, float z, float s, float r) {
+  constexpr int L = (1 << BITS) - 1;
   if (!(s > 0.0f)) return 0u;
   const float d = __fsub_rn(x, z);
   const float y = __fmul_rn(d, r);
@@ -106,7 +109,7 @@ __device__ __forceinline__ uint32_t exact_code(float x, float z, float s, float 
   if (!(y > -0.75f)) return 0u;
   const float fl = floorf(y), h = fl + 0.5f;
   float q;
-  if (fabsf(y - h) > 1e-5f) {
+  if (fabsf(y - h) > tie_guard<BITS>()) {
     q = rintf(y);
   } else {
     const float rho = __fmaf_rn(-h, s, d);
@@ -200,7 +203,6 @@ template <int BITS, bool KEYS>
 __device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv, const float4* sPk,
                                            const float* sS, const uint32_t* sO, const uint8_t* sQ, int D,
                                            int Bk, int r, int ch, int grp, int n_out, uint32_t (&w)[BITS]) {
-  constexpr int L = (1 << BITS) - 1;
   const float2 magic2 = make_float2(kMagic, kMagic), nmagic2 = make_float2(-kMagic, -kMagic);
   const float2 neg1 = make_float2(-1.0f, -1.0f);
   float4 vp = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -252,7 +254,7 @@ __device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv,
       rc = vp.y;
       sc = vp.z;
     }
-    set_code<BITS>(w, e, exact_code(x, z, sc, rc, L));
+    set_code<BITS>(w, e, exact_code<BITS>(x, z, sc, rc));
   }
   for (int o = 0; o < n_out; ++o) {
     const int c = (int)(sO[o * Bk + r] & 0xFFFFu);
@@ -503,7 +505,6 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   // ---- C'. codes of the outlier positions, from their stored values
   if (n_out > 0) {
     const int bk_sh = __ffs(Bk) - 1, gv_sh = __ffs(d.Gv) - 1;
-    constexpr int L = (1 << BITS) - 1;
     for (int it = tid; it < (n_out << bk_sh); it += kThreads) {
       const int o = it >> bk_sh, r = it & (Bk - 1);
       if (r >= rows) continue;
@@ -520,7 +521,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
         rc = vp.y;
         sc = vp.z;
       }
-      sQ[o * Bk + r] = (uint8_t)exact_code(__half2float(__ushort_as_half((uint16_t)(ev >> 16))), z, sc, rc, L);
+      sQ[o * Bk + r] = (uint8_t)exact_code<BITS>(__half2float(__ushort_as_half((uint16_t)(ev >> 16))), z, sc, rc);
     }
     __syncthreads();
   }

@@ -10,9 +10,14 @@ half-gap error bound; and the C++ and NumPy oracles against each other.
 import numpy as np
 import pytest
 
+from fractions import Fraction
+
 from oracle import oracle_cpp as oc
 from oracle import oracle_np as on
 import kvq_inputs as ki
+
+ALL_HALF = np.arange(0, 0x7C00, dtype=np.uint16).view(np.float16)   # every finite fp16 >= 0
+ALL_HALF_F64 = ALL_HALF.astype(np.float64)
 
 
 def _nearest_level(u, levels):
@@ -20,6 +25,43 @@ def _nearest_level(u, levels):
     lv = np.asarray(levels, dtype=np.float64)
     d = np.abs(np.asarray(u, dtype=np.float64)[..., None] - lv)
     return np.argmin(d, axis=-1)       # argmin returns the first (lower) index on ties
+
+
+def _range_pin_holds(x, r, z):
+    """The stored range of a level-table group: r is the smallest binary16
+    value at or above fp32(max) - fp32(min) (found in the table of all fp16
+    values), and the levels span the group: z + r >= max, exactly."""
+    d32 = np.float32(np.float32(x.max()) - np.float32(x.min()))
+    want = ALL_HALF[np.searchsorted(ALL_HALF_F64, float(d32), side="left")]
+    if r.view(np.uint16) != want.view(np.uint16):
+        return False
+    return Fraction(float(z)) + Fraction(float(r)) >= Fraction(float(x.max()))
+
+
+def test_range_rounds_up_against_value_table():
+    """Range r of a level-table group (KVQuant "Non-Uniform KV Cache
+    Quantization": the levels sit on the group's normalized range, so the top
+    level must reach the maximum)."""
+    rng = np.random.default_rng(31)
+    rn_would_fail = 0
+    for trial in range(400):
+        n = int(rng.integers(2, 80))
+        x = (rng.standard_normal(n) * np.exp(rng.uniform(-8, 6))).astype(np.float16)
+        if trial % 4 == 0:                       # a spread that is not an fp16 value
+            x[0] = np.float16(np.float16(1.0) + np.float16(2.0 ** -10) * rng.integers(1, 9))
+            x[1] = np.float16(-np.float16(2.0 ** -rng.integers(3, 12)))
+        r, z = oc.group_params_levels(x)
+        r2, z2 = on.group_params_levels(x[None], np.zeros((1, n), bool), axis=-1)
+        assert r.view(np.uint16) == r2[0].view(np.uint16) and z.view(np.uint16) == z2[0].view(np.uint16)
+        assert z.view(np.uint16) == (x.min() if x.min() != 0 else np.float16(0)).view(np.uint16)
+        assert _range_pin_holds(x, r, z), (x, r, z)
+        # the same pin rejects a range rounded to nearest wherever that rounds down
+        d32 = np.float32(np.float32(x.max()) - np.float32(x.min()))
+        r_rn = d32.astype(np.float16)
+        if float(r_rn) < float(d32):
+            rn_would_fail += 1
+            assert not _range_pin_holds(x, r_rn, z)
+    assert rn_would_fail > 50
 
 
 @pytest.mark.parametrize("bits", [2, 3, 4])
