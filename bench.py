@@ -4,16 +4,24 @@
 A step is one decode step of one layer: append one new token for every
 (batch, kv-head) stream (kvq_append), then decode attention for every query
 head over the whole cache (kvq_decode_attn: split-T partial kernel + combine).
-The default workload is the 7B-style MHA cache (B=8, H=32/32, D=128, T=32768,
-INT4, RoPE theta 1e4). Prints one JSON line (rank 0).
+The default workload is the long-context cache: B=1, H=32/8, D=128,
+T=2^20, INT4 with 1% outliers, RoPE theta 5e5, 32 layers resident in HBM
+(about 41 GB), one layer per step in rotation. After the headline the same
+run measures the other workloads (7B MHA, 8B GQA, INT3, INT2 decode and the
+INT3 / INT2 / INT4 prefill appends) and reports them under "configs" in the
+same JSON line. Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--mode decode|prefill] [--impl kvq|reference]
+                  [--mode decode|prefill|paged|levels] [--impl kvq|reference]
+                  [--configs all|none]
 
 --impl reference times the CPU oracle (the plain C++ reference) on the host
-cores, on a bounded sample of the same workload per step, extrapolated to the
-full step. --mode prefill times one kvq_append of the workload's whole
-context (the aggressive-bits prefill run) instead of decode steps.
+cores: each step is one oracle decode step on a bounded sample of the same
+workload (all streams when there are few, a slice of the cached tokens),
+sized so the whole run ends within a few minutes; ms_per_step is that
+sample step, value the metric of the full step by linear extrapolation.
+--mode prefill times one kvq_append of the workload's whole context (the
+aggressive-bits prefill run) instead of decode steps.
 """
 from __future__ import annotations
 
@@ -58,6 +66,13 @@ def dist_env():
 
 def n_out_of(w):
     return 0 if w.outlier_frac == 0 else max(1, int(math.floor(w.outlier_frac * w.D)))
+
+
+def workload_string(w):
+    """The workload as both arms name it in config.workload."""
+    return (f"{w.name}: B={w.B} H_q={w.H_q} H_kv={w.H_kv} D={w.D} T={w.T} INT{w.bits} "
+            f"key_block={w.key_block} value_group={w.value_group} outliers={w.outlier_frac} "
+            f"rope_theta={w.rope_theta} layers_resident={w.layers}")
 
 
 def decode_alg_bytes(w, T):
@@ -283,6 +298,9 @@ def cpu_baseline(w, budget_s=15.0):
     est = t_probe * (n_tok / min(n_tok, 4096)) * math.ceil(n_streams / threads)
     if est > budget_s:
         n_tok = max(w.key_block, int(n_tok * budget_s / est) // w.key_block * w.key_block)
+    # the sample is generated and encoded once (host numpy + oracle): keep it
+    # to about 2^21 cached token-heads so the setup stays a few seconds
+    n_tok = max(w.key_block, min(n_tok, (1 << 21) // n_streams // w.key_block * w.key_block))
     t, threads = oracle_step_seconds(w, n_streams, n_tok)
     # repeat a short sample until it holds about budget_s of host work; median per repetition
     reps = max(1, min(64, int(budget_s / max(t, 1e-3))))
@@ -403,9 +421,7 @@ def run_decode(args, w, rank, world, device):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": f"u{w.bits}/f16/f32", "data": "synthetic",
         "config": {
-            "workload": (f"{w.name}: B={w.B} H_q={w.H_q} H_kv={w.H_kv} D={w.D} T={T} INT{w.bits} "
-                         f"key_block={w.key_block} value_group={w.value_group} outliers={w.outlier_frac} "
-                         f"rope_theta={w.rope_theta} layers_resident={n_layers}"),
+            "workload": workload_string(w),
             "step": "kvq_append of 1 token per stream + kvq_decode_attn over T+1 tokens",
             "l2": f"inputs larger than L2 (cache {caches[0].layout.cache_bytes / 1e9:.2f} GB per layer > 129 MB); no flush",
             "parallelism": f"replicas x{world}",
@@ -675,37 +691,87 @@ def run_levels(args, w, rank, world, device):
     }
 
 
+def reference_sample_size(w, n_steps, budget_s=80.0):
+    """Streams and cached tokens of the reference arm's per-step sample: every
+    stream when they fit twice the host threads (else one per thread), and
+    the largest whole number of key blocks for which n_steps oracle steps
+    plus the sample's one-time generation and encoding (measured at about
+    seven steps) stay within budget_s of host time."""
+    from oracle import oracle_cpp as oc
+    threads = oc.default_threads()
+    streams = w.B * w.H_kv
+    n_streams = streams if streams <= 2 * threads else threads
+    probe_tok = min(w.T, 4096)
+    t_probe, _ = oracle_step_seconds(w, n_streams, probe_tok, reps=2)
+    per_tok = t_probe / probe_tok
+    n_tok = int(budget_s / ((n_steps + 8) * max(per_tok, 1e-12)))
+    n_tok = max(w.key_block, min(w.T, n_tok // w.key_block * w.key_block))
+    return n_streams, n_tok
+
+
 def run_reference(args, w):
-    """The CPU oracle as the reference arm: each step a bounded sample of the
-    workload's decode step, extrapolated to the full step."""
+    """The CPU oracle as the reference arm. Each step is one oracle decode step
+    (encode the new token, dequantize, float64 attention) on a bounded sample of
+    the workload; ms_per_step is that step's wall time, value the metric of the
+    full step (all streams, all T tokens) by linear extrapolation."""
     from oracle import oracle_cpp as oc
     oc.build()
-    threads = oc.default_threads()
-    n_streams = min(threads, w.B * w.H_kv)
-    # the whole run (warm-up + steps) holds about 150 s of timed host work; the
-    # sample is generated and encoded once, then every step reruns it
-    budget = max(0.002, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
-    t_probe, _ = oracle_step_seconds(w, n_streams, min(w.T, 1024), reps=3)
-    n_tok = min(w.T, max(w.key_block, int(1024 * budget / max(t_probe, 1e-6)) // w.key_block * w.key_block))
+    n_streams, n_tok = reference_sample_size(w, args.steps + args.warmup)
     step, threads = oracle_sample(w, n_streams, n_tok)
-    full = []
+    times = []
     for i in range(args.warmup + args.steps):
         t = step()
         if i >= args.warmup:
-            full.append(t * (w.T / n_tok) * (w.B * w.H_kv / n_streams))
-    step_s = statistics.mean(full)
-    value = w.B / step_s
-    sample = (f"per step {n_streams} of {w.B * w.H_kv} (b,h_kv) streams x {n_tok} of {w.T} tokens "
-              f"(encode new token, dequantize, float64 attention), extrapolated; host {host_cpu()}")
+            times.append(t)
+    step_s = statistics.mean(times)
+    factor = (w.T / n_tok) * (w.B * w.H_kv / n_streams)
+    value = w.B / (step_s * factor)
+    sample = (f"per step {n_streams} of {w.B * w.H_kv} (b,h_kv) streams x {n_tok} of {w.T} cached tokens "
+              f"(encode new token, dequantize, float64 attention) on {threads} host threads; value "
+              f"extrapolated linearly to the full step (x{factor:.3g}); host {host_cpu()}")
     return {
         "impl": "reference", "metric": "decode-attn tokens/s (one layer; B query tokens per step)",
         "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{w.name}: B={w.B} H_q={w.H_q} H_kv={w.H_kv} D={w.D} T={w.T} INT{w.bits}"},
+        "config": {"workload": workload_string(w),
+                   "step": "one oracle decode step on the bounded sample below (ms_per_step); "
+                           "value = B / (ms_per_step x extrapolation factor)",
+                   "full_step_ms_extrapolated": step_s * factor * 1e3},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+
+
+SUITE = [("decode", "mha7b"), ("decode", "gqa8b"), ("decode", "int3"), ("decode", "int2"),
+         ("prefill", "int3"), ("prefill", "int2"), ("prefill", "gqa8b")]
+
+
+def run_config_suite(args, rank, world, device):
+    """The other workloads, measured after the headline in the same run (up to
+    20 timed steps each, at least 3 warm-up steps); their figures go into the
+    headline's JSON line under "configs"."""
+    import argparse as _ap
+    import torch
+    sub = _ap.Namespace(**vars(args))
+    sub.steps = max(1, min(args.steps, 20))
+    sub.warmup = max(3, min(args.warmup, 5))
+    out = {}
+    for mode, name in SUITE:
+        w = ki.WORKLOADS[name]
+        line = (run_decode if mode == "decode" else run_prefill)(sub, w, rank, world, device)
+        torch.cuda.empty_cache()
+        rf = line["roofline"]
+        entry = {"metric": line["metric"], "value": line["value"], "unit": line["unit"],
+                 "ms_per_step": line["ms_per_step"], "steps": sub.steps, "warmup": sub.warmup,
+                 "workload": line["config"]["workload"],
+                 "roofline": {k: rf[k] for k in ("bound", "achieved", "peak", "unit", "frac", "kernel",
+                                                 "alg_bytes_per_launch", "traffic")},
+                 "e2e": line["e2e"]["value"], "clocks": line["clocks"]}
+        if "decode_call_ms" in line["config"]:
+            entry["decode_call_ms"] = line["config"]["decode_call_ms"]
+        out[f"{mode}:{name}"] = entry
+    return out
 
 
 def main():
@@ -714,7 +780,9 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
-    ap.add_argument("--workload", default="mha7b", choices=list(ki.WORKLOADS))
+    ap.add_argument("--workload", default="long1m", choices=list(ki.WORKLOADS))
+    ap.add_argument("--configs", default="all", choices=["all", "none"],
+                    help="after a default decode run, also measure the other workloads")
     ap.add_argument("--mode", default="decode", choices=["decode", "prefill", "paged", "levels"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -743,6 +811,9 @@ def main():
     torch.cuda.set_device(device)
     line = {"prefill": run_prefill, "paged": run_paged, "decode": run_decode,
             "levels": run_levels}[args.mode](args, w, rank, world, device)
+    torch.cuda.empty_cache()
+    if args.configs == "all" and args.mode == "decode" and args.workload == "long1m":
+        line["configs"] = run_config_suite(args, rank, world, device)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()

@@ -8,6 +8,8 @@
 #include <mutex>
 #include <vector>
 
+#include <cuda.h>
+
 #include "kvq_common.cuh"
 #include "kvq_levels.cuh"
 
@@ -128,22 +130,55 @@ int decode_checks(const kvq_config* cfg, const Dims& d, const kvq_cache* cache, 
 constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
 
+// The driver's cuCtxGetCurrent, looked up once (thread-safe static init).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current() {
+  static const CtxGetCurrentFn fn = []() -> CtxGetCurrentFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<CtxGetCurrentFn>(p);
+    return nullptr;
+  }();
+  return fn;
+}
+
 // Device address of g_noalloc_scratch on the current device. In host code
 // the array's name is only a stand-in symbol, so the address is looked up
-// once per device (with that device current) and remembered.
+// with the device current and remembered per device together with the
+// context it belongs to; a new context on the device (after cudaDeviceReset,
+// say) reloads the module, so the address is looked up again.
 int noalloc_scratch(float** out) {
+  struct Entry {
+    CUcontext ctx;
+    float* addr;
+  };
   static std::mutex mu;
-  static float* addr[64] = {};
+  static Entry known[kMaxDevices] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ERR_CUDA;
+  int rc = current_device(&dev);
+  if (rc) return rc;
+  const CtxGetCurrentFn get = ctx_get_current();
+  if (!get) return KVQ_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) return KVQ_ERR_CUDA;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
+  if (!ctx || known[dev].ctx != ctx || !known[dev].addr) {
+    void* p = nullptr;   // the lookup also creates the device's context if there is none yet
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return KVQ_ERR_CUDA;
-    addr[dev] = static_cast<float*>(p);
+    if (get(&ctx) != CUDA_SUCCESS || !ctx) return KVQ_ERR_CUDA;
+    known[dev].ctx = ctx;
+    known[dev].addr = static_cast<float*>(p);
   }
-  *out = addr[dev];
+  *out = known[dev].addr;
   return KVQ_OK;
+}
+
+// The calling thread's device, if the library's per-device tables cover it.
+int device_ok() {
+  int dev = 0;
+  return current_device(&dev);
 }
 
 // A level table from the caller's 2^bits levels: 0 first, 1 last, strictly
@@ -203,6 +238,8 @@ int kvq_rope_init(const kvq_config* cfg, double rope_theta, void* rope_tab, size
   if (!rope_tab || !aligned16(rope_tab) || !(rope_theta > 0.0) || !isfinite(rope_theta))
     return KVQ_ERR_ARG;
   if (rope_bytes < rope_entries(d) * sizeof(float2)) return KVQ_ERR_WORKSPACE;
+  rc = device_ok();
+  if (rc) return rc;
   return cuda_status(launch_rope_init(d, rope_theta, static_cast<float2*>(rope_tab),
                                       static_cast<cudaStream_t>(stream)));
 }
@@ -216,6 +253,8 @@ int kvq_append(const kvq_config* cfg, kvq_cache* cache, const void* k_new, const
   if (n_new == 0) return KVQ_OK;
   if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_ARG;
   if ((int64_t)cache->T_cur + n_new > d.T_max) return KVQ_ERR_CAPACITY;
+  rc = device_ok();
+  if (rc) return rc;
   rc = cuda_status(launch_append(d, *cache, static_cast<const __half*>(k_new),
                                  static_cast<const __half*>(v_new), n_new,
                                  static_cast<cudaStream_t>(stream)));
@@ -231,6 +270,8 @@ int kvq_decode_attn(const kvq_config* cfg, const kvq_cache* cache, const void* q
   if (rc) return rc;
   rc = decode_checks(cfg, d, cache, cache ? cache->T_cur : 0, q, H_q, q_pos, rope_tab, sm_scale, out,
                      workspace, workspace_bytes);
+  if (rc) return rc;
+  rc = device_ok();
   if (rc) return rc;
   return cuda_status(launch_decode(d, *cache, static_cast<const __half*>(q), H_q, q_pos,
                                    static_cast<const float2*>(rope_tab), sm_scale,
@@ -252,6 +293,8 @@ int kvq_decode_step(const kvq_config* cfg, kvq_cache* cache, const void* k_new, 
                      workspace_bytes);
   if (rc) return rc;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  rc = device_ok();
+  if (rc) return rc;
   rc = cuda_status(launch_append(d, *cache, static_cast<const __half*>(k_new),
                                  static_cast<const __half*>(v_new), 1, st));
   if (rc) return rc;
@@ -328,6 +371,8 @@ int kvq_paged_append(const kvq_config* cfg, kvq_paged_cache* cache, const void* 
   if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_ARG;
   if ((int64_t)cache->max_len + n_new > d.T_max) return KVQ_ERR_CAPACITY;
   const Paged pg = paging(d, *cache);
+  rc = device_ok();
+  if (rc) return rc;
   rc = cuda_status(launch_append(d, pool_view(*cache), static_cast<const __half*>(k_new),
                                  static_cast<const __half*>(v_new), n_new, static_cast<cudaStream_t>(stream), &pg));
   if (rc == KVQ_OK) cache->max_len += n_new;
@@ -353,6 +398,8 @@ int kvq_paged_decode_attn(const kvq_config* cfg, const kvq_paged_cache* cache, c
   if (rc) return rc;
   if (workspace_bytes < lay.workspace_bytes) return KVQ_ERR_WORKSPACE;
   const Paged pg = paging(d, *cache);
+  rc = device_ok();
+  if (rc) return rc;
   return cuda_status(launch_decode(d, pool_view(*cache), static_cast<const __half*>(q), H_q, 0,
                                    static_cast<const float2*>(rope_tab), sm_scale, static_cast<__half*>(out),
                                    static_cast<float*>(workspace), static_cast<cudaStream_t>(stream), 0, &pg));
@@ -400,6 +447,8 @@ int kvq_append_levels(const kvq_config* cfg, kvq_cache* cache, const void* k_new
   if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_ARG;
   if (cache->T_cur % d.Bk || n_new % d.Bk) return KVQ_ERR_UNSUPPORTED;   // whole key blocks only
   if ((int64_t)cache->T_cur + n_new > d.T_max) return KVQ_ERR_CAPACITY;
+  rc = device_ok();
+  if (rc) return rc;
   rc = cuda_status(launch_append_levels(d, *cache, static_cast<const __half*>(k_new),
                                         static_cast<const __half*>(v_new), n_new, t,
                                         static_cast<cudaStream_t>(stream)));
@@ -419,6 +468,8 @@ int kvq_decode_attn_levels(const kvq_config* cfg, const kvq_cache* cache, const 
   LevelTable t;
   if (!make_levels(levels, d.bits, &t)) return KVQ_ERR_ARG;
   if (cache->T_cur % d.Bk) return KVQ_ERR_UNSUPPORTED;                     // whole key blocks only
+  rc = device_ok();
+  if (rc) return rc;
   return cuda_status(launch_decode_levels(d, *cache, static_cast<const __half*>(q), H_q, q_pos,
                                           static_cast<const float2*>(rope_tab), sm_scale,
                                           static_cast<__half*>(out), static_cast<float*>(workspace), t,

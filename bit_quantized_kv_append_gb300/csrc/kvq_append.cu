@@ -587,14 +587,14 @@ size_t append_smem(const Dims& d) {
 template <int BITS, int D>
 cudaError_t launch_bd(const AppendArgs& a, dim3 grid, size_t smem, cudaStream_t st) {
   // the shared-memory limit is a per-device function attribute: set it once on each device
-  static std::atomic<bool> attr_set[64];
+  static std::atomic<bool> attr_set[kMaxDevices];
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (!attr_set[dev & 63].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(append_kernel<BITS, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+  if (current_device(&dev) != KVQ_OK) return cudaErrorInvalidDevice;   // the API checked it first
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(append_kernel<BITS, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
     if (e != cudaSuccess) return e;
-    attr_set[dev & 63].store(true, std::memory_order_release);
+    attr_set[dev].store(true, std::memory_order_release);
   }
   append_kernel<BITS, D><<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();

@@ -55,6 +55,15 @@ __host__ __device__ inline int max_splits(const Dims& d) {
   return d.n_blk + 1 < kMaxSplits ? d.n_blk + 1 : kMaxSplits;
 }
 
+// Devices the library's per-device tables cover (function attributes,
+// occupancies, the allocation-free scratch address): ordinals 0 .. 63. A
+// call on a device beyond them is refused with KVQ_ERR_UNSUPPORTED.
+constexpr int kMaxDevices = 64;
+inline int current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  return (*dev >= 0 && *dev < kMaxDevices) ? KVQ_OK : KVQ_ERR_UNSUPPORTED;
+}
+
 __device__ __forceinline__ float h2f(uint16_t h) { return __half2float(__ushort_as_half(h)); }
 
 // cos/sin of the composed rotation R(a) R(b) = R(a + b).

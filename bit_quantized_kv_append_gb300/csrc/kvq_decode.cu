@@ -47,10 +47,10 @@ void pick_g(int G, LaunchFn* f, OccFn* o) {
 // Occupancy (CTAs per SM) of each kernel variant, per device, computed once.
 int cached_occupancy(int dev, int bits, int D, int G, OccFn fn) {
   static std::mutex mu;
-  static int cache[16][4][2][4];
+  static int cache[kMaxDevices][4][2][4];
   const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
   std::lock_guard<std::mutex> lock(mu);
-  int& slot = cache[dev & 15][bits == 8 ? 3 : bits - 2][D == 128][gi];
+  int& slot = cache[dev][bits == 8 ? 3 : bits - 2][D == 128][gi];
   if (slot == 0) slot = fn();
   return slot;
 }
@@ -172,10 +172,10 @@ void pick_tc(int Bk, int G, bool outl, bool paged, TcLaunchFn* f, TcOccFn* o) {
 int cached_tc_occupancy(int dev, int bits, int Bk, int G, bool outl, bool paged, size_t smem, TcOccFn fn) {
   struct Slot { size_t smem; int occ; };
   static std::mutex mu;
-  static Slot cache[16][4][2][4][2][2];
+  static Slot cache[kMaxDevices][4][2][4][2][2];
   const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
   std::lock_guard<std::mutex> lock(mu);
-  Slot& s = cache[dev & 15][bits == 8 ? 3 : bits - 2][Bk == 128][gi][outl ? 1 : 0][paged ? 1 : 0];
+  Slot& s = cache[dev][bits == 8 ? 3 : bits - 2][Bk == 128][gi][outl ? 1 : 0][paged ? 1 : 0];
   if (s.occ == 0 || s.smem != smem) {
     s.occ = fn(smem);
     s.smem = smem;
@@ -215,9 +215,8 @@ cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, in
   const int G = H_q / d.H_kv;
 
   int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (current_device(&dev) != KVQ_OK) return cudaErrorInvalidDevice;   // the API checked it first
+  cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int units = a.n_full + (a.tail_len > 0 ? 1 : 0);
 

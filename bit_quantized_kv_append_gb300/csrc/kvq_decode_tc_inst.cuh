@@ -13,15 +13,14 @@ cudaError_t launch_tc(const DecodeArgs& a, const tc::StageLayout& L, const CUten
                       const CUtensorMap& tv, size_t smem, cudaStream_t st) {
   auto kern = tc::decode_tc_kernel<BITS, G, SL, OUTL, PAGED>;
   // largest dynamic shared memory requested so far, per device (a function attribute per device)
-  static std::atomic<size_t> smem_set[64];
+  static std::atomic<size_t> smem_set[kMaxDevices];
   int dev = 0;
-  cudaError_t e0 = cudaGetDevice(&dev);
-  if (e0 != cudaSuccess) return e0;
-  if (smem_set[dev & 63].load(std::memory_order_acquire) < smem) {
+  if (current_device(&dev) != KVQ_OK) return cudaErrorInvalidDevice;
+  if (smem_set[dev].load(std::memory_order_acquire) < smem) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    size_t cur = smem_set[dev & 63].load(std::memory_order_relaxed);
-    while (cur < smem && !smem_set[dev & 63].compare_exchange_weak(cur, smem, std::memory_order_acq_rel)) {
+    size_t cur = smem_set[dev].load(std::memory_order_relaxed);
+    while (cur < smem && !smem_set[dev].compare_exchange_weak(cur, smem, std::memory_order_acq_rel)) {
     }
   }
   const dim3 grid(a.n_split, a.d.B * a.d.H_kv);

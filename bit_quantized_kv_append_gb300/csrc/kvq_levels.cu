@@ -378,9 +378,8 @@ cudaError_t launch_decode_levels(const Dims& d, const kvq_cache& c, const __half
   a.S = max_splits(d);
   a.sm_scale = sm_scale;
   int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (current_device(&dev) != KVQ_OK) return cudaErrorInvalidDevice;   // the API checked it first
+  cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int units = a.T / d.Bk, streams = d.B * d.H_kv;
   int n = (4 * sms + streams - 1) / streams;               // about four CTAs per SM

@@ -33,7 +33,9 @@
  *     and no output or cache field changes. KVQ_ERR_CUDA reports a launch
  *     error (cudaGetLastError after the launch; no synchronization).
  *   - Devices: calls run on the calling thread's current CUDA device; the
- *     buffers must belong to that device.
+ *     buffers must belong to that device. Device ordinals 0 .. 63 are
+ *     supported; a launching call on a higher ordinal returns
+ *     KVQ_ERR_UNSUPPORTED before anything is launched.
  */
 #ifndef KVQ_H
 #define KVQ_H
@@ -123,11 +125,19 @@ typedef struct kvq_cache {
 } kvq_cache;
 
 /* Sizes of every buffer for `cfg` and for decode with H_q query heads
- * (H_q a positive multiple of H_kv). Host-only and pure: touches no device.
+ * (H_q a positive multiple of H_kv). Passage: the KV-cache memory formula of
+ * the page "TurboQuant ..." (mlqm.cn/news/1002276), §2.1 "KVCache的本质与内存
+ * 开销": fp16 K and V take 2 x layers x batch x tokens x hidden x 2 bytes;
+ * fp16_equiv_bytes is that size for one layer of this cache's capacity, and
+ * cache_bytes what the packed codes, metadata and outliers take instead.
+ * Host-only and pure: touches no device.
  * Errors: KVQ_ERR_ARG (NULL), KVQ_ERR_UNSUPPORTED (cfg or H_q). */
 KVQ_API int kvq_layout(const kvq_config* cfg, int32_t H_q, kvq_layout_t* out);
 
-/* Fill the RoPE table used by kvq_decode_attn for base `rope_theta` (> 0):
+/* Fill the RoPE table used by kvq_decode_attn for base `rope_theta` (> 0).
+ * Passage: page 3, KVQuant "Pre-RoPE Key Quantization" (keys are cached
+ * before the rotary embedding, which is applied to them after
+ * dequantization); the table holds that rotation:
  * cos/sin of pos * theta^(-2i/D) (rotate-half pairs (i, i + D/2)), built in
  * binary64 on the device and stored as binary32, for every position the cache
  * can hold. Its contents are private to the library; build it once per
@@ -154,7 +164,10 @@ KVQ_API int kvq_append(const kvq_config* cfg, kvq_cache* cache, const void* k_ne
 
 /* Decode attention of one query token per sequence over the T_cur cached
  * tokens (GQA: query head h reads kv head h / G, G = H_q / H_kv in
- * {1, 2, 4, 8}).
+ * {1, 2, 4, 8}). Passages: page 3, Quanto "量化原理" step 3 (the cache is
+ * dequantized as it is read) and KVQuant "Pre-RoPE Key Quantization" (RoPE
+ * applied to the dequantized keys); the dense-and-sparse outliers of KVQuant
+ * "Per-Vector Dense-and-Sparse Quantization" are restored on read.
  *   q:   fp16 [B][H_q][D], pre-RoPE, at position q_pos (0 <= q_pos < T_max);
  *   out: fp16 [B][H_q][D].
  * out_h = sum_t softmax_t(sm_scale * <RoPE(q_h, q_pos), RoPE(k_hat_t, t)>) v_hat_t
@@ -197,7 +210,11 @@ KVQ_API int kvq_decode_step(const kvq_config* cfg, kvq_cache* cache, const void*
  * that reserves all device memory at start-up and forbids later cudaMalloc
  * calls, or a plain-C host that owns no device allocator from which to hand
  * over scratch. The pages have no counterpart; it is a convenience of this
- * library. Same arguments, results and errors as kvq_decode_attn.
+ * library. Same arguments and errors as kvq_decode_attn. The results are
+ * bit-identical to kvq_decode_attn's when the split limit below does not
+ * bind; when it does, fewer T splits change the order of the fp32 merge and
+ * the results agree within the decode tolerance (2e-3 max-abs, 1e-2
+ * relative) instead.
  *   - Scratch: the split partials go to one file-scope device array of
  *     8 MiB that every GPU loading the library keeps until the process
  *     exits. No allocation or free happens in this call.
@@ -206,8 +223,9 @@ KVQ_API int kvq_decode_step(const kvq_config* cfg, kvq_cache* cache, const void*
  *     exceeds 8 MiB is rejected with KVQ_ERR_WORKSPACE. Fewer splits can make
  *     it slower than kvq_decode_attn on very wide batches.
  *   - Set-up: the first call on each device looks up the array's device
- *     address with that device current; make that first call before any
- *     stream capture on the device.
+ *     address with that device current (and again after the device gets a
+ *     new context, e.g. after cudaDeviceReset); make that first call before
+ *     any stream capture on the device.
  *   - Sharing: every call uses the same array. Each call writes every entry
  *     it later reads, so nothing has to be cleared between calls, but calls
  *     whose kernels overlap on the GPU (different streams, or different host
@@ -247,7 +265,9 @@ typedef struct kvq_paged_cache {
   int32_t max_len;              /* host: an upper bound of every seq_len[b] (sizes the grids) */
 } kvq_paged_cache;
 
-/* Sizes of the pools for n_blocks physical blocks (bytes[]), per physical
+/* Sizes of a paged cache (passage: the paged serving setting of
+ * mlqm.cn/news/1002276 §5.2-5.3, with the memory formula of its §2.1 giving
+ * fp16_equiv_bytes): the pools for n_blocks physical blocks (bytes[]), per physical
  * block for the pools and per sequence for K_TAIL (stream_bytes[]), and the
  * decode workspace for H_q query heads. fp16_equiv_bytes is the fp16 K and V
  * of the pools' capacity. Host-only and pure.
@@ -289,7 +309,8 @@ KVQ_API int kvq_paged_decode_attn(const kvq_config* cfg, const kvq_paged_cache* 
  * gives 0), and x_hat = z + r * l_code. These calls run CUDA-core kernels for
  * caches filled in whole key blocks (no fp16 tail). */
 
-/* Level table of 2^bits levels fitted to calibration samples u[0..n) in
+/* Level table (page 3, KVQuant "Non-Uniform KV Cache Quantization": the
+ * format is calibrated offline) of 2^bits levels fitted to calibration samples u[0..n) in
  * [0, 1] (normalized dense values, e.g. (x - min) / (max - min) of groups of
  * representative keys or values): one-dimensional k-means (Lloyd) started
  * from the uniform grid k / L, with the end levels held at 0 and 1; a level
@@ -298,7 +319,8 @@ KVQ_API int kvq_paged_decode_attn(const kvq_config* cfg, const kvq_paged_cache* 
  * KVQ_ERR_UNSUPPORTED (bits not in {2, 3, 4, 8}). */
 KVQ_API int kvq_fit_levels(const double* u, size_t n, int32_t bits, int32_t iters, float* levels);
 
-/* kvq_append with non-uniform codes. levels: host pointer to the 2^bits
+/* kvq_append with non-uniform codes (page 3, KVQuant "Non-Uniform KV Cache
+ * Quantization"). levels: host pointer to the 2^bits
  * levels of the table (copied into the launch). T_cur and n_new must be
  * multiples of key_block. Errors: those of kvq_append; KVQ_ERR_ARG for a
  * table that does not start at 0, end at 1 and increase; KVQ_ERR_UNSUPPORTED
@@ -307,16 +329,18 @@ KVQ_API int kvq_append_levels(const kvq_config* cfg, kvq_cache* cache, const voi
                               int32_t n_new, const float* levels, void* stream);
 
 /* kvq_decode_attn over a cache appended with kvq_append_levels and the same
- * table (T_cur a multiple of key_block). Errors: those of kvq_decode_attn;
+ * table (page 3, KVQuant "Non-Uniform KV Cache Quantization": x_hat = z + r *
+ * l_code on read; T_cur a multiple of key_block). Errors: those of kvq_decode_attn;
  * KVQ_ERR_ARG for a bad table; KVQ_ERR_UNSUPPORTED for a partial key block. */
 KVQ_API int kvq_decode_attn_levels(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t H_q,
                                    int32_t q_pos, const void* rope_tab, float sm_scale, void* out,
                                    void* workspace, size_t workspace_bytes, const float* levels, void* stream);
 
-/* Static, human-readable name of a status code. */
+/* Static, human-readable name of a status code (a utility of this library;
+ * no passage). */
 KVQ_API const char* kvq_status_string(int status);
 
-/* Library version, e.g. "kvq 0.1.0 sm_103a". */
+/* Library version, e.g. "kvq 0.1.0 sm_103a" (a utility; no passage). */
 KVQ_API const char* kvq_version(void);
 
 #ifdef __cplusplus

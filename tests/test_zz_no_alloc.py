@@ -31,7 +31,12 @@ CASES = {
     "int3_bk128": W("na_int3", 1, 8, 2, 128, 700, 3, 128, 32, 0.01, 5e5, 32),
     "d64_mha": W("na_d64", 2, 4, 4, 64, 300, 3, 64, 32, 0.0, 1e4, 33),
     "wide_batch": W("na_wide", 8, 32, 32, 128, 2000, 4, 64, 64, 0.0, 1e4, 34),
+    # 8 MiB holds only 7 splits of B * H_q * (D + 2) floats here, against 65
+    # key blocks per stream: the allocation-free call runs with fewer splits
+    # than the workspace call chooses, so the split limit itself is exercised
+    "split_limit_binds": W("na_cap", 32, 64, 8, 128, 4096 + 37, 4, 64, 64, 0.01, 5e5, 35),
 }
+SCRATCH_BYTES = 8 << 20
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -45,6 +50,9 @@ def _lib():
 def test_noalloc_matches_workspace_entry(name):
     w = CASES[name]
     T = w.T
+    if name == "split_limit_binds":
+        fit = SCRATCH_BYTES // (w.B * w.H_q * (w.D + 2) * 4)
+        assert fit < (T + w.key_block - 1) // w.key_block // 8
     cache = tl.make_cache(w, (T // w.key_block + 1) * w.key_block)
     K, V = ki.kv_torch(w, 0, 0, T, "cuda")
     cache.append(K, V)
