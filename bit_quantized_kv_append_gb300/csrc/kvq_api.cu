@@ -262,6 +262,26 @@ int kvq_append(const kvq_config* cfg, kvq_cache* cache, const void* k_new, const
   return rc;
 }
 
+int kvq_append_window(const kvq_config* cfg, kvq_cache* cache, const void* k_new, const void* v_new,
+                      int32_t n_new, int32_t window, void* k_bstat, void* stream) {
+  Dims d;
+  int rc = make_dims(cfg, &d);
+  if (rc) return rc;
+  if (window < d.Bk || window % d.Bk) return KVQ_ERR_UNSUPPORTED;
+  if (!cache || n_new < 0 || !cache_ptrs_ok(d, *cache)) return KVQ_ERR_ARG;
+  if (!k_bstat || !aligned16(k_bstat)) return KVQ_ERR_ARG;
+  if (n_new == 0) return KVQ_OK;
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_ARG;
+  if ((int64_t)cache->T_cur + n_new > d.T_max) return KVQ_ERR_CAPACITY;
+  rc = device_ok();
+  if (rc) return rc;
+  rc = cuda_status(launch_append(d, *cache, static_cast<const __half*>(k_new), static_cast<const __half*>(v_new),
+                                 n_new, static_cast<cudaStream_t>(stream), nullptr, window / d.Bk,
+                                 static_cast<uint32_t*>(k_bstat)));
+  if (rc == KVQ_OK) cache->T_cur += n_new;
+  return rc;
+}
+
 int kvq_decode_attn(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t H_q,
                     int32_t q_pos, const void* rope_tab, float sm_scale, void* out,
                     void* workspace, size_t workspace_bytes, void* stream) {

@@ -57,6 +57,14 @@ struct AppendArgs {
   const int32_t* block_table;  // paged cache (NULL: contiguous streams); then the
   const int32_t* seq_len;      // position, first block and tail rule are per sequence
   int max_blocks, n_blocks;
+  // Sliding-window key statistics (0: the block's own statistics). Phase 1
+  // quantizes the values, selects the key outliers and stores each finished
+  // key block's dense {min, max} per channel in k_bstat; phase 2 (key CTAs
+  // only, a later launch) takes (s, z) from the last window_blocks blocks'
+  // {min, max} and writes the key codes and metadata.
+  int phase;
+  int window_blocks;
+  uint32_t* k_bstat;
 };
 
 // Paged append: position of sequence b (its length, kept inside the capacity).
@@ -270,7 +278,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   const int tid = threadIdx.x;
   const int bh = blockIdx.y;
   const int b = bh / d.H_kv, h = bh - b * d.H_kv;
-  const bool isK = blockIdx.z != 0;
+  const bool isK = a.phase == 2 || blockIdx.z != 0;
   int T_cur = a.T_cur, first_blk = a.first_blk, tail_in_kernel = a.tail_in_kernel;
   if (a.block_table) {
     T_cur = paged_pos(a, b);
@@ -294,7 +302,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
 
   if (isK && !complete) {
     // unfinished block: keep the new keys as fp16 rows t % Bk of the tail
-    if (tail_in_kernel) {
+    if (tail_in_kernel && a.phase != 2) {
       for (int i = tid; i < nv * vpr; i += kThreads) {
         const int r = i / vpr, c = i % vpr;
         const int t = t_lo + r;
@@ -360,7 +368,14 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   // ---- B. dense-and-sparse split: per row, the n_out largest |x|
   uint32_t* gout_base = (isK ? a.k_outl : a.v_outl) + (size_t)(row_base + t_row0) * n_out;
   const __half nanh = __ushort_as_half((uint16_t)0x7E00u);   // marks outliers for step C
-  if (n_out == 1 && D == 128) {
+  if (a.phase == 2) {
+    // window keys, phase 2: the outliers phase 1 selected (their codes are
+    // patched in step C'; the statistics come from the window)
+    for (int it = tid; it < n_out * Bk; it += kThreads) {
+      const int k = it / Bk, r = it % Bk;
+      sO[k * Bk + r] = gout_base[(size_t)r * n_out + k];
+    }
+  } else if (n_out == 1 && D == 128) {
     // four threads per row, 32 channels (four 16-byte chunks) each. The fp16
     // magnitude bits (x & 0x7FFF) order like |x|, so the largest |x| is an
     // unsigned 16-bit maximum; then the lowest channel holding it.
@@ -469,6 +484,29 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
       a.v_meta[(size_t)(row_base + t_row0 + r) * ng + g] = packed;
       sPv[g * Bk + r] = make_float4(-sz.y, rcp_or_zero(sz.x), sz.x, 0.0f);
     }
+  } else if (a.phase == 2) {
+    // window keys: min and max of the dense elements of the last
+    // window_blocks blocks (this block and the ones before it), from the
+    // {min, max} pairs phase 1 stored; +inf / -inf mark a block without dense
+    // elements in the channel
+    if (tid < D) {
+      const int c = tid, cp = c >> 1, hc = c & 1;
+      float mn = INFINITY, mx = -INFINITY;
+      const int u_lo = blk - a.window_blocks + 1 > 0 ? blk - a.window_blocks + 1 : 0;
+      for (int u = u_lo; u <= blk; ++u) {
+        const size_t ub = unit_block(d, a.block_table, a.max_blocks, a.n_blocks, b, h, u);
+        const uint32_t e = a.k_bstat[ub * D + c];
+        mn = fminf(mn, h2f((uint16_t)(e & 0xFFFFu)));
+        mx = fmaxf(mx, h2f((uint16_t)(e >> 16)));
+      }
+      float2 sz;
+      const uint32_t packed = group_params(mn, mx, mn <= mx, Lf, &sz);
+      a.k_meta[kblk * D + c] = packed;
+      float* pk = reinterpret_cast<float*>(&sPk[cp]);
+      pk[hc] = -sz.y;
+      pk[2 + hc] = rcp_or_zero(sz.x);
+      sS[c] = sz.x;
+    }
   } else {
     // channel pairs p < D/2, row slices q < S: partial fp16 min/max, then combined
     const int P = D / 2, S = kThreads / P;
@@ -491,16 +529,25 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
         mn = fminf(mn, hc ? __high2float(a2) : __low2float(a2));
         mx = fmaxf(mx, hc ? __high2float(b2) : __low2float(b2));
       }
-      float2 sz;
-      const uint32_t packed = group_params(mn, mx, !isnan(mn), Lf, &sz);
-      a.k_meta[kblk * D + c] = packed;
-      float* pk = reinterpret_cast<float*>(&sPk[cp]);
-      pk[hc] = -sz.y;
-      pk[2 + hc] = rcp_or_zero(sz.x);
-      sS[c] = sz.x;
+      if (a.phase == 1) {
+        // window keys, phase 1: the block's dense {min, max} (fp16 values;
+        // +inf / -inf when every element of the channel is an outlier)
+        const uint16_t lo = isnan(mn) ? (uint16_t)0x7C00u : hbits(__float2half_rn(mn));
+        const uint16_t hi = isnan(mn) ? (uint16_t)0xFC00u : hbits(__float2half_rn(mx));
+        a.k_bstat[kblk * D + c] = (uint32_t)lo | ((uint32_t)hi << 16);
+      } else {
+        float2 sz;
+        const uint32_t packed = group_params(mn, mx, !isnan(mn), Lf, &sz);
+        a.k_meta[kblk * D + c] = packed;
+        float* pk = reinterpret_cast<float*>(&sPk[cp]);
+        pk[hc] = -sz.y;
+        pk[2 + hc] = rcp_or_zero(sz.x);
+        sS[c] = sz.x;
+      }
     }
   }
   __syncthreads();
+  if (isK && a.phase == 1) return;   // window keys: codes in phase 2
 
   // ---- C'. codes of the outlier positions, from their stored values
   if (n_out > 0) {
@@ -615,9 +662,13 @@ __global__ void seq_len_advance_kernel(int32_t* seq_len, int B, int n_new, int T
 }
 
 cudaError_t launch_append(const Dims& d, const kvq_cache& c, const __half* k_new,
-                          const __half* v_new, int n_new, cudaStream_t st, const Paged* pg) {
+                          const __half* v_new, int n_new, cudaStream_t st, const Paged* pg,
+                          int window_blocks, uint32_t* k_bstat) {
   AppendArgs a;
   a.d = d;
+  a.phase = window_blocks > 0 ? 1 : 0;
+  a.window_blocks = window_blocks;
+  a.k_bstat = k_bstat;
   a.k_codes = static_cast<uint8_t*>(c.k_codes);
   a.k_meta = static_cast<uint32_t*>(c.k_meta);
   a.k_tail = static_cast<__half*>(c.k_tail);
@@ -666,6 +717,18 @@ cudaError_t launch_append(const Dims& d, const kvq_cache& c, const __half* k_new
     default: e = launch_bits<4>(a, grid, smem, st); break;
   }
   if (e != cudaSuccess) return e;
+  if (window_blocks > 0) {
+    // window keys, phase 2: every block statistic of phase 1 is stored now
+    a.phase = 2;
+    const dim3 grid2(blocks_x, d.B * d.H_kv, 1);
+    switch (d.bits) {
+      case 2: e = launch_bits<2>(a, grid2, smem, st); break;
+      case 3: e = launch_bits<3>(a, grid2, smem, st); break;
+      case 8: e = launch_bits<8>(a, grid2, smem, st); break;
+      default: e = launch_bits<4>(a, grid2, smem, st); break;
+    }
+    if (e != cudaSuccess) return e;
+  }
   if (defer_tail) {
     const int rows = pg ? d.Bk - 1 : t_end - t_from;   // paged: at most Bk - 1 unfinished rows
     const int blocks = (rows * (d.D / 8) + 255) / 256;

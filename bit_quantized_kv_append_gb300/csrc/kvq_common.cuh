@@ -101,8 +101,12 @@ __device__ __forceinline__ size_t unit_block(const Dims& d, const int32_t* table
 // Launch helpers (defined in the kernel translation units).
 cudaError_t launch_rope_init(const Dims& d, double theta, float2* tab, cudaStream_t st);
 // pg: a paged cache (positions from pg->seq_len, advanced by n_new after the append).
+// window_blocks > 0: key statistics over the last window_blocks key blocks,
+// with every finished block's dense {min, max} per channel kept in k_bstat
+// (the size of K_META).
 cudaError_t launch_append(const Dims& d, const kvq_cache& c, const __half* k_new,
-                          const __half* v_new, int n_new, cudaStream_t st, const Paged* pg = nullptr);
+                          const __half* v_new, int n_new, cudaStream_t st, const Paged* pg = nullptr,
+                          int window_blocks = 0, uint32_t* k_bstat = nullptr);
 // split_cap > 0 bounds the T splits (and the workspace stride) below max_splits().
 // pg: a paged cache (per-sequence lengths; q of sequence b at seq_len[b] - 1).
 cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, int H_q, int q_pos,

@@ -24,7 +24,7 @@ import torch
 BUFFERS = ("k_codes", "k_meta", "k_tail", "k_outl", "v_codes", "v_meta", "v_outl")
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "KVQ_ERR_CAPACITY",
           4: "KVQ_ERR_WORKSPACE", 5: "KVQ_ERR_CUDA"}
-EXPORTS = ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_decode_attn", "kvq_decode_step",
+EXPORTS = ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_append_window", "kvq_decode_attn", "kvq_decode_step",
            "kvq_paged_layout", "kvq_paged_append", "kvq_paged_decode_attn",
            "kvq_fit_levels", "kvq_append_levels", "kvq_decode_attn_levels",
            "kvq_decode_attn_noalloc", "kvq_status_string", "kvq_version")
@@ -76,6 +76,7 @@ def lib():
         L.kvq_layout.argtypes = [ctypes.POINTER(Config), i32, ctypes.POINTER(Layout)]
         L.kvq_rope_init.argtypes = [ctypes.POINTER(Config), ctypes.c_double, vp, ctypes.c_size_t, vp]
         L.kvq_append.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp, vp, i32, vp]
+        L.kvq_append_window.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp, vp, i32, i32, vp, vp]
         L.kvq_decode_attn.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp, i32, i32,
                                       vp, ctypes.c_float, vp, vp, ctypes.c_size_t, vp]
         L.kvq_decode_step.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp, vp, vp, i32,
@@ -93,7 +94,7 @@ def lib():
         L.kvq_status_string.argtypes = [ctypes.c_int]
         L.kvq_status_string.restype = ctypes.c_char_p
         L.kvq_version.restype = ctypes.c_char_p
-        for fn in ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_decode_attn", "kvq_decode_step",
+        for fn in ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_append_window", "kvq_decode_attn", "kvq_decode_step",
                    "kvq_paged_layout", "kvq_paged_append", "kvq_paged_decode_attn", "kvq_fit_levels",
                    "kvq_append_levels", "kvq_decode_attn_levels", "kvq_decode_attn_noalloc"):
             getattr(L, fn).restype = ctypes.c_int
@@ -141,6 +142,12 @@ def rope_init(cfg: Config, theta: float, table: torch.Tensor, stream=None):
 def append(cfg: Config, ref: CacheRef, k_new: torch.Tensor, v_new: torch.Tensor, n_new: int, stream=None):
     _check(lib().kvq_append(ctypes.byref(cfg), ctypes.byref(ref), _ptr(k_new), _ptr(v_new), int(n_new),
                             _stream(stream)), "kvq_append")
+
+
+def append_window(cfg: Config, ref: CacheRef, k_new: torch.Tensor, v_new: torch.Tensor, n_new: int,
+                  window: int, k_bstat: torch.Tensor, stream=None):
+    _check(lib().kvq_append_window(ctypes.byref(cfg), ctypes.byref(ref), _ptr(k_new), _ptr(v_new), int(n_new),
+                                   int(window), _ptr(k_bstat), _stream(stream)), "kvq_append_window")
 
 
 def decode_attn(cfg: Config, ref: CacheRef, q: torch.Tensor, H_q: int, q_pos: int,
@@ -260,8 +267,7 @@ class QuantizedKVCache:
         self.T_cur = int(T_cur)
 
     # -- the two paths
-    def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
-        """k_new, v_new: fp16 [B, H_kv, n, D] on the cache's device (pre-RoPE keys)."""
+    def _check_kv(self, k_new, v_new):
         c = self.cfg
         for t in (k_new, v_new):
             if t.dtype != torch.float16 or not t.is_contiguous() or t.device != self.device:
@@ -270,8 +276,24 @@ class QuantizedKVCache:
                 raise ValueError(f"expected [B={c.B}, H_kv={c.H_kv}, n, D={c.D}], got {tuple(t.shape)}")
         if k_new.shape != v_new.shape:
             raise ValueError("k_new and v_new shapes differ")
+
+    def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
+        """k_new, v_new: fp16 [B, H_kv, n, D] on the cache's device (pre-RoPE keys)."""
+        self._check_kv(k_new, v_new)
         ref = self.ref()
         append(self.cfg, ref, k_new, v_new, k_new.shape[2], stream)
+        self.T_cur = ref.T_cur
+
+    def append_window(self, k_new: torch.Tensor, v_new: torch.Tensor, window: int, stream=None):
+        """kvq_append with key statistics over the last `window` tokens; the
+        block statistics buffer (the size of K_META) is allocated on first use
+        and kept with the cache."""
+        self._check_kv(k_new, v_new)
+        if getattr(self, "k_bstat", None) is None:
+            self.k_bstat = torch.empty(self.layout.bytes[BUFFERS.index("k_meta")], dtype=torch.uint8,
+                                       device=self.device)
+        ref = self.ref()
+        append_window(self.cfg, ref, k_new, v_new, k_new.shape[2], window, self.k_bstat, stream)
         self.T_cur = ref.T_cur
 
     def decode(self, q: torch.Tensor, q_pos: Optional[int] = None, sm_scale: Optional[float] = None,

@@ -162,6 +162,29 @@ KVQ_API int kvq_rope_init(const kvq_config* cfg, double rope_theta, void* rope_t
 KVQ_API int kvq_append(const kvq_config* cfg, kvq_cache* cache, const void* k_new, const void* v_new,
                int32_t n_new, void* stream);
 
+/* kvq_append with sliding-window key statistics (page mlqm.cn/news/1064729
+ * ("UltraQuant ..."), §3.2 "时空自适应量化", sliding-window statistics: the
+ * scale and zero follow the most recent `window` tokens instead of the whole
+ * sequence). Values are quantized exactly as kvq_append quantizes them. When
+ * a key block completes, its (s, z) per channel are the group parameters of
+ * the channel's dense elements (outliers excluded) in the last `window`
+ * tokens up to the block's end, tokens [max(0, t_end - window), t_end); the
+ * block's codes, outliers and K_META entry are then those of kvq_append with
+ * these (s, z). window = key_block gives exactly kvq_append's cache.
+ *   window:  tokens, a positive multiple of key_block (1024 in the passage);
+ *   k_bstat: device buffer of the size of K_META (layout bytes[KVQ_K_META]),
+ *            caller-owned and kept with the cache: every finished key block's
+ *            dense {min, max} per channel (fp16 pair; +inf / -inf when all of
+ *            the channel's elements in the block are outliers), laid out like
+ *            K_META. Every append to the cache must go through this call with
+ *            the same window and buffer; decode reads the cache unchanged
+ *            (kvq_decode_attn).
+ * Two launches (statistics, then key codes), plus the deferred tail copy of
+ * kvq_append when it applies. Errors: those of kvq_append; KVQ_ERR_ARG for a
+ * NULL or misaligned k_bstat; KVQ_ERR_UNSUPPORTED for a bad window. */
+KVQ_API int kvq_append_window(const kvq_config* cfg, kvq_cache* cache, const void* k_new, const void* v_new,
+                              int32_t n_new, int32_t window, void* k_bstat, void* stream);
+
 /* Decode attention of one query token per sequence over the T_cur cached
  * tokens (GQA: query head h reads kv head h / G, G = H_q / H_kv in
  * {1, 2, 4, 8}). Passages: page 3, Quanto "量化原理" step 3 (the cache is

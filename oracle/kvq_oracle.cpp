@@ -24,6 +24,15 @@
 //   |x| then ascending index; a group with max == min has s = 0 and codes 0; a
 //   group whose every element is an outlier has s = 0, z = 0.
 //
+//   Page mlqm.cn/news/1064729 ("UltraQuant ..."), §3.2, sliding-window
+//     statistics: the scale and zero of a key block may come from the most
+//     recent W tokens (W a multiple of the block, e.g. 1024) instead of the
+//     block alone. Reading: for key block b and channel c, (s, z) are the
+//     group parameters of the dense elements of channel c in tokens
+//     [max(0, (b + 1) Bk - W), (b + 1) Bk); the block's codes use them (the
+//     clamp of the code rule never binds for the block's own elements, which
+//     lie inside the window). W = Bk is the per-block rule.
+//
 //   Same page, KVQuant "Non-Uniform KV Cache Quantization": codes may instead
 //     index a calibrated table of levels (a non-uniform grid). Reading: 2^b
 //     sorted levels 0 = l_0 < ... < l_L = 1 on the group's normalized range;
@@ -272,9 +281,12 @@ bool is_outlier(const uint16_t* idx, int n_out, int c) {
 
 // Encode one (batch, kv-head) stream of T tokens.
 // levels: a level table (non-uniform codes) or nullptr (uniform grid).
+// window: tokens of the key statistics window (a multiple of Bk; Bk or 0:
+// the block alone).
 void encode_stream(const Shape& sh, const uint16_t* K, const uint16_t* V,
                    uint8_t* k_codes, uint16_t* k_meta, uint16_t* k_tail, uint16_t* k_outl,
-                   uint8_t* v_codes, uint16_t* v_meta, uint16_t* v_outl, const float* levels) {
+                   uint8_t* v_codes, uint16_t* v_meta, uint16_t* v_outl, const float* levels,
+                   int window) {
   const int D = sh.D, T = sh.T, n_out = sh.n_out, bits = sh.bits;
   const std::vector<float> mids = levels ? level_mids(levels, (1 << bits) - 1) : std::vector<float>();
   auto params = [&](const std::vector<uint16_t>& dense, uint16_t* s, uint16_t* z) {
@@ -312,7 +324,8 @@ void encode_stream(const Shape& sh, const uint16_t* K, const uint16_t* V,
 
   // Keys: per channel over each completed block of Bk tokens.
   const int nb = sh.n_full();
-  std::vector<uint16_t> blk_idx(static_cast<size_t>(sh.Bk) * std::max(n_out, 1));
+  // outlier channels of every key vector of the finished blocks
+  std::vector<uint16_t> win_idx(static_cast<size_t>(nb) * sh.Bk * std::max(n_out, 1));
   for (int b = 0; b < nb; ++b) {
     const int t0 = b * sh.Bk;
     for (int j = 0; j < sh.Bk; ++j) {
@@ -320,17 +333,19 @@ void encode_stream(const Shape& sh, const uint16_t* K, const uint16_t* V,
       const uint16_t* x = K + static_cast<size_t>(t) * D;
       select_outliers(x, D, n_out, oi.data(), ov.data());
       for (int k = 0; k < n_out; ++k) {
-        blk_idx[static_cast<size_t>(j) * n_out + k] = oi[k];
+        win_idx[static_cast<size_t>(t) * n_out + k] = oi[k];
         k_outl[(static_cast<size_t>(t) * n_out + k) * 2 + 0] = oi[k];
         k_outl[(static_cast<size_t>(t) * n_out + k) * 2 + 1] = ov[k];
       }
     }
     std::vector<uint16_t> s_c(D), z_c(D);
+    // the statistics window: this block, or the last `window` tokens up to its end
+    const int w0 = (window > sh.Bk) ? std::max(0, t0 + sh.Bk - window) : t0;
     for (int c = 0; c < D; ++c) {
       std::vector<uint16_t> dense;
-      for (int j = 0; j < sh.Bk; ++j)
-        if (!is_outlier(&blk_idx[static_cast<size_t>(j) * n_out], n_out, c))
-          dense.push_back(K[static_cast<size_t>(t0 + j) * D + c]);
+      for (int t = w0; t < t0 + sh.Bk; ++t)
+        if (!is_outlier(&win_idx[static_cast<size_t>(t) * n_out], n_out, c))
+          dense.push_back(K[static_cast<size_t>(t) * D + c]);
       params(dense, &s_c[c], &z_c[c]);
       k_meta[(static_cast<size_t>(b) * D + c) * 2 + 0] = s_c[c];
       k_meta[(static_cast<size_t>(b) * D + c) * 2 + 1] = z_c[c];
@@ -486,12 +501,28 @@ int kvqo_encode(int P, int T, int D, int bits, int Bk, int Gv, int n_out, const 
                             v_meta, v_outl, nullptr, nthreads);
 }
 
+int kvqo_encode_window(int P, int T, int D, int bits, int Bk, int Gv, int n_out, int window,
+                       const uint16_t* K, const uint16_t* V, uint8_t* k_codes, uint16_t* k_meta,
+                       uint16_t* k_tail, uint16_t* k_outl, uint8_t* v_codes, uint16_t* v_meta,
+                       uint16_t* v_outl, const float* levels, int nthreads);
+
 // levels: 2^bits sorted binary32 levels (non-uniform codes) or NULL (uniform).
 int kvqo_encode_levels(int P, int T, int D, int bits, int Bk, int Gv, int n_out, const uint16_t* K,
                        const uint16_t* V, uint8_t* k_codes, uint16_t* k_meta, uint16_t* k_tail,
                        uint16_t* k_outl, uint8_t* v_codes, uint16_t* v_meta, uint16_t* v_outl,
                        const float* levels, int nthreads) {
+  return kvqo_encode_window(P, T, D, bits, Bk, Gv, n_out, Bk, K, V, k_codes, k_meta, k_tail, k_outl, v_codes,
+                            v_meta, v_outl, levels, nthreads);
+}
+
+// window: key statistics over the last `window` tokens (a positive multiple
+// of Bk; Bk is the per-block rule); uniform grid only when window > Bk.
+int kvqo_encode_window(int P, int T, int D, int bits, int Bk, int Gv, int n_out, int window,
+                       const uint16_t* K, const uint16_t* V, uint8_t* k_codes, uint16_t* k_meta,
+                       uint16_t* k_tail, uint16_t* k_outl, uint8_t* v_codes, uint16_t* v_meta,
+                       uint16_t* v_outl, const float* levels, int nthreads) {
   if (!shape_ok(T, D, bits, Bk, Gv, n_out) || P < 0) return 1;
+  if (window < Bk || window % Bk || (levels && window != Bk)) return 1;
   const Shape sh{T, D, bits, Bk, Gv, n_out};
   const size_t td = static_cast<size_t>(T) * D;
   const size_t rows = static_cast<size_t>(T) * sh.row_bytes();
@@ -504,7 +535,7 @@ int kvqo_encode_levels(int P, int T, int D, int bits, int Bk, int Gv, int n_out,
     std::memset(k_outl + p * ol, 0, ol * sizeof(uint16_t));
     std::memset(k_tail + p * kt, 0, kt * sizeof(uint16_t));
     encode_stream(sh, K + p * td, V + p * td, k_codes + p * rows, k_meta + p * km, k_tail + p * kt,
-                  k_outl + p * ol, v_codes + p * rows, v_meta + p * vm, v_outl + p * ol, levels);
+                  k_outl + p * ol, v_codes + p * rows, v_meta + p * vm, v_outl + p * ol, levels, window);
   });
   return 0;
 }

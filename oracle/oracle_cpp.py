@@ -51,6 +51,7 @@ def lib():
         L.kvqo_pack_row.argtypes = [i, P, i, P]
         L.kvqo_rope.argtypes = [i, P, d, d, P]
         L.kvqo_encode_levels.argtypes = [i] * 7 + [P] * 10 + [i]
+        L.kvqo_encode_window.argtypes = [i] * 8 + [P] * 10 + [i]
         L.kvqo_dequant_levels.argtypes = [i] * 7 + [P] * 10 + [i]
         L.kvqo_group_params_levels.argtypes = [i, P, P, P, P]
         L.kvqo_quantize_levels.argtypes = [i, P, ctypes.c_uint16, ctypes.c_uint16, i, P, P]
@@ -67,10 +68,12 @@ def default_threads() -> int:
     return max(1, os.cpu_count() or 1)
 
 
-def encode(K, V, bits, Bk, Gv, n_out, nthreads=None, levels=None):
+def encode(K, V, bits, Bk, Gv, n_out, nthreads=None, levels=None, window=None):
     """Encode streams K, V [P, T, D] fp16; same dict layout as ``oracle_np.encode``.
     ``levels``: a table of 2^bits sorted levels in [0, 1] (non-uniform codes;
-    the scale slot then holds the group's range), or None (uniform grid)."""
+    the scale slot then holds the group's range), or None (uniform grid).
+    ``window``: key statistics over the most recent `window` tokens (a
+    multiple of Bk; None: the block alone)."""
     K = np.ascontiguousarray(K, dtype=np.float16)
     V = np.ascontiguousarray(V, dtype=np.float16)
     P, T, D = K.shape
@@ -86,9 +89,9 @@ def encode(K, V, bits, Bk, Gv, n_out, nthreads=None, levels=None):
         "v_outl": np.zeros((P, T, n_out, 2), np.uint16),
     }
     lv = None if levels is None else _levels(levels, bits)
-    rc = lib().kvqo_encode_levels(P, T, D, bits, Bk, Gv, n_out, _p(K), _p(V), _p(out["k_codes"]),
-                                  _p(out["k_meta"]), _p(out["k_tail"]), _p(out["k_outl"]),
-                                  _p(out["v_codes"]), _p(out["v_meta"]), _p(out["v_outl"]),
+    rc = lib().kvqo_encode_window(P, T, D, bits, Bk, Gv, n_out, Bk if window is None else int(window), _p(K),
+                                  _p(V), _p(out["k_codes"]), _p(out["k_meta"]), _p(out["k_tail"]),
+                                  _p(out["k_outl"]), _p(out["v_codes"]), _p(out["v_meta"]), _p(out["v_outl"]),
                                   None if lv is None else _p(lv), nthreads or default_threads())
     if rc:
         raise ValueError("oracle encode: bad shape")

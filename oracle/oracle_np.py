@@ -164,10 +164,15 @@ def _outlier_mask(idx, D):
     return mask
 
 
-def encode(K, V, bits, Bk, Gv, n_out, levels=None):
+def encode(K, V, bits, Bk, Gv, n_out, levels=None, window=None):
     """Encode streams K, V of shape [P, T, D] (fp16). Returns a dict of arrays
     laid out like the C++ oracle's outputs. ``levels``: a level table
-    (non-uniform codes) or None (uniform grid)."""
+    (non-uniform codes) or None (uniform grid). ``window``: sliding-window
+    key statistics (page mlqm.cn/news/1064729 §3.2, "滑动窗口统计": the scale
+    and zero come from the most recent `window` tokens only): the (s, z) of
+    key block b and channel c are those of the dense elements of channel c in
+    tokens [max(0, (b + 1) Bk - window), (b + 1) Bk); the block's codes use
+    them. None (or window = Bk) is the per-block statistics."""
     K = np.asarray(K, dtype=np.float16)
     V = np.asarray(V, dtype=np.float16)
     P, T, D = K.shape
@@ -189,7 +194,20 @@ def encode(K, V, bits, Bk, Gv, n_out, levels=None):
     Kb = K[:, : nb * Bk].reshape(P, nb, Bk, D)
     ki, kv = select_outliers(Kb, n_out)
     kmask = _outlier_mask(ki, D)
-    if levels is None:
+    if levels is not None and window is not None and window != Bk:
+        raise ValueError("window statistics are defined for the uniform grid")
+    if levels is None and window is not None and window != Bk:
+        if window % Bk or window < Bk:
+            raise ValueError("window: a positive multiple of the key block")
+        Kt = K[:, : nb * Bk]
+        tmask = kmask.reshape(P, nb * Bk, D)
+        ks = np.zeros((P, nb, D), np.float16)
+        kz = np.zeros((P, nb, D), np.float16)
+        for b in range(nb):                                          # the window ending with block b
+            lo = max(0, (b + 1) * Bk - window)
+            ks[:, b], kz[:, b] = group_params(Kt[:, lo:(b + 1) * Bk], tmask[:, lo:(b + 1) * Bk], bits, axis=1)
+        kq = quantize(Kb, ks[:, :, None, :], kz[:, :, None, :], bits).reshape(P, nb * Bk, D)
+    elif levels is None:
         ks, kz = group_params(Kb, kmask, bits, axis=2)              # [P, nb, D]
         kq = quantize(Kb, ks[:, :, None, :], kz[:, :, None, :], bits).reshape(P, nb * Bk, D)
     else:
