@@ -317,11 +317,11 @@ def cpu_baseline(w, budget_s=15.0):
 
 
 # ----------------------------------------------------------------------------- GPU runs
-def build_cache(w, T, T_max, device, layer=0, rope_table=None):
+def build_cache(w, T, T_max, device, layer=0, rope_table=None, precise=False):
     import bit_quantized_kv_append_gb300 as kvq
     cache = kvq.QuantizedKVCache(w.B, w.H_kv, w.D, T_max, w.bits, w.key_block, w.value_group,
                                  w.outlier_frac, H_q=w.H_q, rope_theta=w.rope_theta, device=device,
-                                 rope_table=rope_table)
+                                 rope_table=rope_table, precise=precise)
     chunk = max(w.key_block, (1 << 26) // max(1, w.B * w.H_kv * w.D) // w.key_block * w.key_block)
     t = 0
     while t < T:
@@ -339,8 +339,9 @@ def run_decode(args, w, rank, world, device):
     T = w.T
     T_max = T + w.key_block
     n_layers = w.layers
-    cache0 = build_cache(w, T, T_max, device)
-    caches = [cache0] + [build_cache(w, T, T_max, device, layer=l, rope_table=cache0.rope)
+    precise = getattr(args, "precise", False)
+    cache0 = build_cache(w, T, T_max, device, precise=precise)
+    caches = [cache0] + [build_cache(w, T, T_max, device, layer=l, rope_table=cache0.rope, precise=precise)
                          for l in range(1, n_layers)]
     k1, v1 = ki.kv_torch(w, 0, T, 1, device)
     q = ki.queries_torch(w, 0, 1, device)
@@ -422,7 +423,8 @@ def run_decode(args, w, rank, world, device):
         "dtype": f"u{w.bits}/f16/f32", "data": "synthetic",
         "config": {
             "workload": workload_string(w),
-            "step": "kvq_append of 1 token per stream + kvq_decode_attn over T+1 tokens",
+            "step": "kvq_append of 1 token per stream + kvq_decode_attn over T+1 tokens"
+                    + (" (KVQ_FLAG_PRECISE_SCORES)" if precise else ""),
             "l2": f"inputs larger than L2 (cache {caches[0].layout.cache_bytes / 1e9:.2f} GB per layer > 129 MB); no flush",
             "parallelism": f"replicas x{world}",
             "kv_tokens_per_s": replica_throughput(w.B * (T + 1) * args.steps, world, ms),
@@ -785,6 +787,8 @@ def main():
                     help="after a default decode run, also measure the other workloads")
     ap.add_argument("--mode", default="decode", choices=["decode", "prefill", "paged", "levels"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--precise", action="store_true",
+                    help="decode with KVQ_FLAG_PRECISE_SCORES (fp32 keys, hi + lo operands)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

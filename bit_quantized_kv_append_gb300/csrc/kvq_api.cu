@@ -39,6 +39,7 @@ int make_dims(const kvq_config* cfg, Dims* d) {
   const int n_out = n_outliers(c);
   if (n_out > KVQ_MAX_OUTLIERS) return KVQ_ERR_UNSUPPORTED;
   if ((int64_t)c.B * c.H_kv > 65535) return KVQ_ERR_UNSUPPORTED;  // grid.y
+  if (c.flags & ~KVQ_FLAG_PRECISE_SCORES) return KVQ_ERR_UNSUPPORTED;
   d->B = c.B;
   d->H_kv = c.H_kv;
   d->D = c.D;
@@ -51,6 +52,7 @@ int make_dims(const kvq_config* cfg, Dims* d) {
   d->ng = c.D / c.value_group;
   d->n_blk = c.T_max / c.key_block;
   d->rope_n_hi = rope_n_hi(d->n_blk);
+  d->flags = c.flags;
   return KVQ_OK;
 }
 
@@ -224,7 +226,7 @@ int kvq_layout(const kvq_config* cfg, int32_t H_q, kvq_layout_t* out) {
   }
   out->fp16_equiv_bytes = 2 * streams * (size_t)d.T_max * d.D * 2;
   out->rope_bytes = rope_entries(d) * sizeof(float2);
-  out->workspace_bytes = (size_t)d.B * H_q * max_splits(d) * (d.D + 2) * sizeof(float);
+  out->workspace_bytes = kWsHeaderBytes + (size_t)d.B * H_q * max_splits(d) * (d.D + 2) * sizeof(float);
   out->n_out = d.n_out;
   out->code_row_bytes = d.cb;
   return KVQ_OK;
@@ -299,6 +301,24 @@ int kvq_decode_attn(const kvq_config* cfg, const kvq_cache* cache, const void* q
                                    static_cast<cudaStream_t>(stream)));
 }
 
+int kvq_decode_attn_diag(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t H_q,
+                         int32_t q_pos, const void* rope_tab, float sm_scale, void* out, void* workspace,
+                         size_t workspace_bytes, uint32_t tx_pad, void* stream) {
+  Dims d;
+  int rc = make_dims(cfg, &d);
+  if (rc) return rc;
+  rc = decode_checks(cfg, d, cache, cache ? cache->T_cur : 0, q, H_q, q_pos, rope_tab, sm_scale, out,
+                     workspace, workspace_bytes);
+  if (rc) return rc;
+  if (d.D != 128 || (tx_pad & 15u)) return KVQ_ERR_UNSUPPORTED;
+  rc = device_ok();
+  if (rc) return rc;
+  return cuda_status(launch_decode(d, *cache, static_cast<const __half*>(q), H_q, q_pos,
+                                   static_cast<const float2*>(rope_tab), sm_scale,
+                                   static_cast<__half*>(out), static_cast<float*>(workspace),
+                                   static_cast<cudaStream_t>(stream), 0, nullptr, tx_pad));
+}
+
 int kvq_decode_step(const kvq_config* cfg, kvq_cache* cache, const void* k_new, const void* v_new,
                     const void* q, int32_t H_q, const void* rope_tab, float sm_scale, void* out,
                     void* workspace, size_t workspace_bytes, void* stream) {
@@ -339,7 +359,7 @@ int kvq_decode_attn_noalloc(const kvq_config* cfg, const kvq_cache* cache, const
   if (rope_tab && !aligned16(rope_tab)) return KVQ_ERR_ARG;
   // one T split needs (D + 2) floats per (sequence, query head)
   const size_t split_bytes = (size_t)d.B * H_q * (d.D + 2) * sizeof(float);
-  const size_t fit = kNoAllocScratchBytes / split_bytes;
+  const size_t fit = (kNoAllocScratchBytes - kWsHeaderBytes) / split_bytes;
   if (fit < 1) return KVQ_ERR_WORKSPACE;
   float* scratch = nullptr;
   rc = noalloc_scratch(&scratch);
@@ -504,10 +524,11 @@ const char* kvq_status_string(int status) {
     case KVQ_ERR_CAPACITY: return "KVQ_ERR_CAPACITY: T_cur + n_new exceeds T_max";
     case KVQ_ERR_WORKSPACE: return "KVQ_ERR_WORKSPACE: workspace or table smaller than kvq_layout() requires";
     case KVQ_ERR_CUDA: return "KVQ_ERR_CUDA: CUDA launch error";
+    case KVQ_ERR_TIMEOUT: return "KVQ_ERR_TIMEOUT: a bounded wait of a kernel expired (status word)";
     default: return "KVQ_ERR_UNKNOWN";
   }
 }
 
-const char* kvq_version(void) { return "kvq 0.1.0 sm_103a"; }
+const char* kvq_version(void) { return "kvq 0.2.0 sm_103a"; }
 
 }  // extern "C"

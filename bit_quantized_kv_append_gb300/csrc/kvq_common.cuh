@@ -17,6 +17,7 @@ struct Dims {
   int ng;         // value groups per token = D/Gv
   int n_blk;      // key blocks per stream = T_max/Bk
   int rope_n_hi;  // rows of the coarse RoPE table
+  int flags;      // kvq_config.flags (KVQ_FLAG_*)
 };
 
 // Strides (elements of the buffer's own unit) of one (b, h_kv) stream.
@@ -50,7 +51,10 @@ __host__ __device__ inline size_t rope_entries(const Dims& d) {
 }
 
 // Decode split-T scratch: per (b, h_q, split) the partial output o[D], then m, l.
+// The workspace starts with the device status word (kWsHeaderBytes, of which
+// the first 4 bytes are used); the partials follow.
 constexpr int kMaxSplits = 256;
+constexpr size_t kWsHeaderBytes = 256;
 __host__ __device__ inline int max_splits(const Dims& d) {
   return d.n_blk + 1 < kMaxSplits ? d.n_blk + 1 : kMaxSplits;
 }
@@ -109,8 +113,11 @@ cudaError_t launch_append(const Dims& d, const kvq_cache& c, const __half* k_new
                           int window_blocks = 0, uint32_t* k_bstat = nullptr);
 // split_cap > 0 bounds the T splits (and the workspace stride) below max_splits().
 // pg: a paged cache (per-sequence lengths; q of sequence b at seq_len[b] - 1).
+// ws: the workspace, status word first (kWsHeaderBytes), partials after it.
+// tx_pad: diagnostics of the bounded waits (0: none).
 cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, int H_q, int q_pos,
                           const float2* rope, float sm_scale, __half* out, float* ws,
-                          cudaStream_t st, int split_cap = 0, const Paged* pg = nullptr);
+                          cudaStream_t st, int split_cap = 0, const Paged* pg = nullptr,
+                          uint32_t tx_pad = 0);
 
 }  // namespace kvq

@@ -28,7 +28,9 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restri
     L = fmaf(w, ps[D + 1], L);
     acc = fmaf(w, ps[c], acc);
   }
-  out[(size_t)bhq * D + c] = __float2half_rn(L > 0.0f ? acc / L : 0.0f);   // a sequence without tokens: 0
+  // a sequence without tokens: 0; partials of a split whose waits expired are
+  // NaN and stay NaN here
+  out[(size_t)bhq * D + c] = __float2half_rn(L == 0.0f ? 0.0f : acc / L);
 }
 
 using LaunchFn = cudaError_t (*)(const DecodeArgs&, cudaStream_t);
@@ -149,33 +151,37 @@ using TcLaunchFn = cudaError_t (*)(const DecodeArgs&, const tc::StageLayout&, co
                                    const CUtensorMap&, size_t, cudaStream_t);
 using TcOccFn = int (*)(size_t);
 
-template <int BITS, int SL, bool OUTL, bool PAGED>
+template <int BITS, int SL, bool OUTL, bool PAGED, bool PREC>
 void pick_tc_g(int G, TcLaunchFn* f, TcOccFn* o) {
   switch (G) {
-    case 1: *f = launch_tc<BITS, 1, SL, OUTL, PAGED>; *o = tc_occupancy<BITS, 1, SL, OUTL, PAGED>; break;
-    case 2: *f = launch_tc<BITS, 2, SL, OUTL, PAGED>; *o = tc_occupancy<BITS, 2, SL, OUTL, PAGED>; break;
-    case 4: *f = launch_tc<BITS, 4, SL, OUTL, PAGED>; *o = tc_occupancy<BITS, 4, SL, OUTL, PAGED>; break;
-    default: *f = launch_tc<BITS, 8, SL, OUTL, PAGED>; *o = tc_occupancy<BITS, 8, SL, OUTL, PAGED>; break;
+    case 1: *f = launch_tc<BITS, 1, SL, OUTL, PAGED, PREC>; *o = tc_occupancy<BITS, 1, SL, OUTL, PAGED, PREC>; break;
+    case 2: *f = launch_tc<BITS, 2, SL, OUTL, PAGED, PREC>; *o = tc_occupancy<BITS, 2, SL, OUTL, PAGED, PREC>; break;
+    case 4: *f = launch_tc<BITS, 4, SL, OUTL, PAGED, PREC>; *o = tc_occupancy<BITS, 4, SL, OUTL, PAGED, PREC>; break;
+    default: *f = launch_tc<BITS, 8, SL, OUTL, PAGED, PREC>; *o = tc_occupancy<BITS, 8, SL, OUTL, PAGED, PREC>; break;
   }
 }
 
-template <int BITS, bool PAGED>
+template <int BITS, bool PAGED, bool PREC>
 void pick_tc_p(int Bk, int G, bool outl, TcLaunchFn* f, TcOccFn* o) {
-  if (Bk == 64) outl ? pick_tc_g<BITS, 1, true, PAGED>(G, f, o) : pick_tc_g<BITS, 1, false, PAGED>(G, f, o);
-  else outl ? pick_tc_g<BITS, 2, true, PAGED>(G, f, o) : pick_tc_g<BITS, 2, false, PAGED>(G, f, o);
+  if (Bk == 64)
+    outl ? pick_tc_g<BITS, 1, true, PAGED, PREC>(G, f, o) : pick_tc_g<BITS, 1, false, PAGED, PREC>(G, f, o);
+  else
+    outl ? pick_tc_g<BITS, 2, true, PAGED, PREC>(G, f, o) : pick_tc_g<BITS, 2, false, PAGED, PREC>(G, f, o);
 }
 template <int BITS>
-void pick_tc(int Bk, int G, bool outl, bool paged, TcLaunchFn* f, TcOccFn* o) {
-  paged ? pick_tc_p<BITS, true>(Bk, G, outl, f, o) : pick_tc_p<BITS, false>(Bk, G, outl, f, o);
+void pick_tc(int Bk, int G, bool outl, bool paged, bool prec, TcLaunchFn* f, TcOccFn* o) {
+  if (prec) paged ? pick_tc_p<BITS, true, true>(Bk, G, outl, f, o) : pick_tc_p<BITS, false, true>(Bk, G, outl, f, o);
+  else paged ? pick_tc_p<BITS, true, false>(Bk, G, outl, f, o) : pick_tc_p<BITS, false, false>(Bk, G, outl, f, o);
 }
 
-int cached_tc_occupancy(int dev, int bits, int Bk, int G, bool outl, bool paged, size_t smem, TcOccFn fn) {
+int cached_tc_occupancy(int dev, int bits, int Bk, int G, bool outl, bool paged, bool prec, size_t smem,
+                        TcOccFn fn) {
   struct Slot { size_t smem; int occ; };
   static std::mutex mu;
-  static Slot cache[kMaxDevices][4][2][4][2][2];
+  static Slot cache[kMaxDevices][4][2][4][2][2][2];
   const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
   std::lock_guard<std::mutex> lock(mu);
-  Slot& s = cache[dev][bits == 8 ? 3 : bits - 2][Bk == 128][gi][outl ? 1 : 0][paged ? 1 : 0];
+  Slot& s = cache[dev][bits == 8 ? 3 : bits - 2][Bk == 128][gi][outl ? 1 : 0][paged ? 1 : 0][prec ? 1 : 0];
   if (s.occ == 0 || s.smem != smem) {
     s.occ = fn(smem);
     s.smem = smem;
@@ -186,8 +192,9 @@ int cached_tc_occupancy(int dev, int bits, int Bk, int G, bool outl, bool paged,
 }  // namespace
 
 cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, int H_q, int q_pos,
-                          const float2* rope, float sm_scale, __half* out, float* ws,
-                          cudaStream_t st, int split_cap, const Paged* pg) {
+                          const float2* rope, float sm_scale, __half* out, float* ws_all,
+                          cudaStream_t st, int split_cap, const Paged* pg, uint32_t tx_pad) {
+  float* ws = ws_all + kWsHeaderBytes / sizeof(float);   // the partials follow the status word
   DecodeArgs a;
   a.d = d;
   a.k_codes = static_cast<const uint8_t*>(c.k_codes);
@@ -200,6 +207,8 @@ cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, in
   a.q = q;
   a.rope = rope;
   a.ws = ws;
+  a.status = reinterpret_cast<uint32_t*>(ws_all);
+  a.tx_pad = tx_pad;
   // paged: the grid is sized for the longest sequence; each CTA reads its own length
   a.T = pg ? pg->max_len : c.T_cur;
   a.n_full = a.T / d.Bk;
@@ -230,13 +239,14 @@ cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, in
     TcLaunchFn fn = nullptr;
     TcOccFn occ_fn = nullptr;
     const bool paged = pg != nullptr;
+    const bool prec = (d.flags & KVQ_FLAG_PRECISE_SCORES) != 0;
     switch (d.bits) {
-      case 2: pick_tc<2>(d.Bk, G, d.n_out > 0, paged, &fn, &occ_fn); break;
-      case 3: pick_tc<3>(d.Bk, G, d.n_out > 0, paged, &fn, &occ_fn); break;
-      case 8: pick_tc<8>(d.Bk, G, d.n_out > 0, paged, &fn, &occ_fn); break;
-      default: pick_tc<4>(d.Bk, G, d.n_out > 0, paged, &fn, &occ_fn); break;
+      case 2: pick_tc<2>(d.Bk, G, d.n_out > 0, paged, prec, &fn, &occ_fn); break;
+      case 3: pick_tc<3>(d.Bk, G, d.n_out > 0, paged, prec, &fn, &occ_fn); break;
+      case 8: pick_tc<8>(d.Bk, G, d.n_out > 0, paged, prec, &fn, &occ_fn); break;
+      default: pick_tc<4>(d.Bk, G, d.n_out > 0, paged, prec, &fn, &occ_fn); break;
     }
-    const int occ = cached_tc_occupancy(dev, d.bits, d.Bk, G, d.n_out > 0, paged, smem, occ_fn);
+    const int occ = cached_tc_occupancy(dev, d.bits, d.Bk, G, d.n_out > 0, paged, prec, smem, occ_fn);
     a.n_split = paged ? paged_splits(d, units, sms * occ, a.S) : choose_splits(d.B * d.H_kv, units, sms * occ, a.S);
     e = fn(a, L, tk, tv, smem, st);
   } else {

@@ -45,6 +45,8 @@ struct DecodeArgs {
   const int32_t* block_table;  // paged cache (NULL: contiguous streams)
   const int32_t* seq_len;      // paged: tokens of each sequence
   int max_blocks, n_blocks;
+  uint32_t* status;            // device status word: KVQ_STATUS_* bits are ORed in
+  uint32_t tx_pad;             // diagnostics: bytes each ring stage expects beyond its copies (0)
 };
 
 // Tokens, full key blocks, tail length and query position of sequence b.

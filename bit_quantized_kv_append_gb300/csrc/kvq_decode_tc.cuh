@@ -26,6 +26,11 @@
 //  * P . V, transposed (rows = channels, columns = heads): A = value codes as
 //    exact fp16 subnormals (q * 2^-24, power-of-two rescale at the flush),
 //    B = p*s split into fp16 hi + lo; zero points as sum_t p*z per group.
+//  * precise scores (PREC, the caller's KVQ_FLAG_PRECISE_SCORES): the keys are
+//    dequantized and rotated in fp32 (the rotation from the fp32 in-block
+//    table), and both operands of q . k are split into fp16 hi + lo parts with
+//    three mma per product (hi.hi + lo.hi + hi.lo), so the scores carry about
+//    22 bits instead of 11; P . V takes p*s as hi + lo as well.
 //  * accumulation: the tensor-core accumulators move every kFlush blocks into
 //    fp32 shared sums (long accumulations on the tensor core drift low). The
 //    shared sums and the value-outlier corrections p*(x_out - x_dense) live
@@ -51,7 +56,6 @@ namespace tc {
 #define KVQ_TC_MINB 4        // CTAs per SM the register allocation is held to
 #endif
 
-constexpr uint32_t kWaitLimit = 1u << 20;  // mbarrier polls before giving up (~1 s)
 constexpr int kFlush = 8;                   // blocks between P.V accumulator flushes
 constexpr float kFrameGap = 64.0f;          // renormalise the shared sums past 2^64
 
@@ -87,10 +91,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return done != 0;
 }
-// Bounded wait: false if the phase did not complete within kWaitLimit polls.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait: false if the phase did not complete within kWaitNs of the
+// GPU's global timer (time rather than a poll count, so the bound does not
+// depend on how long one try_wait suspends the thread); a poll count of 2^26
+// caps it as well.
+constexpr uint64_t kWaitNs = 1000000000ull;   // one second
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0; i < (1u << 26); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitNs) return false;
+  }
   return false;
 }
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -364,6 +381,45 @@ __device__ __forceinline__ float value_scale(int e) {
   else return (e & 1) ? 2097152.0f : 16777216.0f;                             // 2^21 : 2^24
 }
 
+// PREC: (a, b) as an fp16 pair hi plus the fp16 pair of the remainders lo.
+__device__ __forceinline__ void split_hilo(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 hf = __half22float2(h);
+  hi = as_u32(h);
+  lo = as_u32(__floats2half2_rn(a - hf.x, b - hf.y));
+}
+
+// PREC: one token's keys of k-step kq in fp32: x = code * s + z (the halved
+// fp16 s, z of the slots), rotated by R(j) from the fp32 in-block table
+// (`fine`: [pair][Bk] {cos, sin}; NULL: no RoPE), then split into fp16 hi +
+// lo B operands. f*/p*: exact half2 codes of the first-half slots (0, 1),
+// (2, 3) and of their partners; kf*/kp*: {b0, b1} of the rotated first-half
+// and partner keys.
+template <int BITS>
+__device__ __forceinline__ void prec_keys(const uint32_t (&f)[2], const uint32_t (&p)[2], const uint4& zf,
+                                          const uint4& zp, const float2* fine, int Bk, int j, int r, int kq,
+                                          uint32_t (&kf_hi)[2], uint32_t (&kf_lo)[2], uint32_t (&kp_hi)[2],
+                                          uint32_t (&kp_lo)[2]) {
+  const uint32_t sf[2] = {zf.x, zf.y}, zff[2] = {zf.z, zf.w}, sp[2] = {zp.x, zp.y}, zpp[2] = {zp.z, zp.w};
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const float2 cf = __half22float2(as_h2(f[hh])), cp = __half22float2(as_h2(p[hh]));
+    const float2 s1 = __half22float2(as_h2(sf[hh])), z1 = __half22float2(as_h2(zff[hh]));
+    const float2 s2 = __half22float2(as_h2(sp[hh])), z2 = __half22float2(as_h2(zpp[hh]));
+    const float xf[2] = {fmaf(cf.x, s1.x, z1.x), fmaf(cf.y, s1.y, z1.y)};
+    const float xp[2] = {fmaf(cp.x, s2.x, z2.x), fmaf(cp.y, s2.y, z2.y)};
+    float kf[2], kp[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float2 cs = fine ? __ldg(fine + (size_t)kchan<BITS>(r, kq, 2 * hh + e) * Bk + j) : make_float2(1.0f, 0.0f);
+      kf[e] = fmaf(xf[e], cs.x, -xp[e] * cs.y);
+      kp[e] = fmaf(xp[e], cs.x, xf[e] * cs.y);
+    }
+    split_hilo(kf[0], kf[1], kf_hi[hh], kf_lo[hh]);
+    split_hilo(kp[0], kp[1], kp_hi[hh], kp_lo[hh]);
+  }
+}
+
 // Float offset in s_acc[w][mt][g][r'] (a float4 per lane) of channel c, head h.
 template <int RQ>
 __device__ __forceinline__ int acc_index(int w, int c, int h) {
@@ -378,7 +434,7 @@ __device__ __forceinline__ int acc_index(int w, int c, int h) {
 // OUTL: the cache keeps outliers (n_out > 0); without them the outlier code
 // is not compiled in. PAGED: a paged, ragged batch (block table, per-sequence
 // lengths); the contiguous instantiation holds none of that code.
-template <int BITS, int G, int SL, bool OUTL, bool PAGED>
+template <int BITS, int G, int SL, bool OUTL, bool PAGED, bool PREC>
 __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const DecodeArgs a, const StageLayout L,
                                                              const __grid_constant__ CUtensorMap tm_k,
                                                              const __grid_constant__ CUtensorMap tm_v) {
@@ -393,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
   __shared__ float s_qp[G][kD];                               // q at q_pos, times 2*sm_scale*log2(e)
   __shared__ const void* s_src[4];                            // this stream's k_meta, v_meta, k_outl, v_outl
   __shared__ __align__(16) uint4 s_qa[2][SL][8][32];          // A quads {a0, 0, a2, 0} of 2 q_block, fp16
+  __shared__ __align__(16) uint4 s_ql[PREC ? 2 : 1][PREC ? SL : 1][PREC ? 8 : 1][32];   // PREC: the lo parts
   __shared__ __align__(16) uint4 s_kz[2][4][4][2];            // key {s01, s23, z01, z23} / 2 [k-step][quarter][half]
   __shared__ __align__(16) float4 s_acc[kWarps][8][8][RQ];    // P.V sums in the frame m_frame, fragment order
   __shared__ __align__(16) float4 s_tok[kWarps][16];          // key-outlier staging of one warp
@@ -446,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
     const uint32_t bar = smem_addr(&s_bar[stage]);
     const uint32_t base = ring_s + stage * L.stage_bytes;
     const int y = PAGED ? 0 : u * BK, z = PAGED ? (int)kblk : bh;
-    mbar_arrive_expect_tx(bar, L.tx_bytes);
+    mbar_arrive_expect_tx(bar, L.tx_bytes + a.tx_pad);
     tma_load_3d(base + L.kc, &tm_k, 0, y, z, bar);
     tma_load_3d(base + L.vc, &tm_v, 0, y, z, bar);
     bulk_load(base + L.km, static_cast<const uint8_t*>(s_src[0]) + kblk * L.km_bytes, L.km_bytes, bar);
@@ -461,7 +518,9 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
     return mbar_wait(smem_addr(&s_bar[k % NST]), (uint32_t)((k / NST) & 1));
   };
   auto abort_split = [&](int u) {
-    // drain every copy still in flight, then report NaN for this split
+    // report the expired wait in the status word, drain every copy still in
+    // flight (bounded waits again), then write NaN partials for this split
+    if (tid == 0) atomicOr(a.status, (unsigned int)KVQ_STATUS_TIMEOUT);
     for (int x = u; x < u1 && x < u + NST; ++x) wait_unit(x);
     for (int e = tid; e < G * (kD + 2); e += kThreads)
       ws_base[(size_t)(e / (kD + 2)) * a.S * (kD + 2) + e % (kD + 2)] = __int_as_float(0x7fffffff);
@@ -509,18 +568,25 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
       for (int sl = 0; sl < SL; ++sl) {
         const float2 rs = sl ? rot_compose(rr, r64) : rr;
         uint8_t* qa = reinterpret_cast<uint8_t*>(&s_qa[buf][sl][0][0]) + q_off;
+        uint8_t* ql = reinterpret_cast<uint8_t*>(&s_ql[PREC ? buf : 0][PREC ? sl : 0][0][0]) + q_off;
+        // fp16 value of v (PREC: hi, and the lo part v - hi)
+        auto put = [&](int off, float v) {
+          const __half hi = __float2half_rn(v);
+          *reinterpret_cast<__half*>(qa + off) = hi;
+          if constexpr (PREC) *reinterpret_cast<__half*>(ql + off) = __float2half_rn(v - __half2float(hi));
+        };
         if constexpr (G == 1) {
           const float x = s_qp[0][qi], y = s_qp[0][qi + HALF];
           const bool part = tid >= HALF;
           const float v = part ? fmaf(y, rs.x, -x * rs.y) : fmaf(x, rs.x, y * rs.y);   // apply R(-t)
-          *reinterpret_cast<__half*>(qa + (part ? 2048 : 0)) = __float2half_rn(v);
+          put(part ? 2048 : 0, v);
         } else {
 #pragma unroll
           for (int gg = tid >> 6; gg < G; gg += 2) {
             const float x = s_qp[gg][qi], y = s_qp[gg][qi + HALF];
             const float x2 = fmaf(x, rs.x, y * rs.y), y2 = fmaf(y, rs.x, -x * rs.y);   // apply R(-t)
-            *reinterpret_cast<__half*>(qa + 64 * gg) = __float2half_rn(x2);
-            *reinterpret_cast<__half*>(qa + 64 * gg + 2048) = __float2half_rn(y2);
+            put(64 * gg, x2);
+            put(64 * gg + 2048, y2);
           }
         }
       }
@@ -575,6 +641,8 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
   {
     uint32_t* z = reinterpret_cast<uint32_t*>(&s_qa[0][0][0][0]);
     for (int e = tid; e < (int)(sizeof(s_qa) / 4); e += kThreads) z[e] = 0u;
+    uint32_t* zl = reinterpret_cast<uint32_t*>(&s_ql[0][0][0][0]);
+    for (int e = tid; e < (int)(sizeof(s_ql) / 4); e += kThreads) zl[e] = 0u;
     float* f = reinterpret_cast<float*>(&s_acc[0][0][0][0]);
     for (int e = tid; e < (int)(sizeof(s_acc) / 4); e += kThreads) f[e] = 0.0f;
   }
@@ -675,18 +743,32 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
               key_codes<BITS>(kw[nt].f, lo.ksh, kq, f0, f1);
               key_codes<BITS>(kw[nt].p, lo.ksh, kq, p0, p1);
             }
-            const __half2 xf0 = __hfma2(as_h2(f0), as_h2(zf.x), as_h2(zf.z));
-            const __half2 xf1 = __hfma2(as_h2(f1), as_h2(zf.y), as_h2(zf.w));
-            const __half2 xp0 = __hfma2(as_h2(p0), as_h2(zp.x), as_h2(zp.z));
-            const __half2 xp1 = __hfma2(as_h2(p1), as_h2(zp.y), as_h2(zp.w));
-            const uint4 rt = __ldg(rot + (nt * 4 + kq) * 32);
-            const __half2 c01 = as_h2(rt.x), c23 = as_h2(rt.y), s01 = as_h2(rt.z), s23 = as_h2(rt.w);
-            const __half2 kf0 = __hfma2(xf0, c01, __hneg2(__hmul2(xp0, s01)));
-            const __half2 kp0 = __hfma2(xp0, c01, __hmul2(xf0, s01));
-            const __half2 kf1 = __hfma2(xf1, c23, __hneg2(__hmul2(xp1, s23)));
-            const __half2 kp1 = __hfma2(xp1, c23, __hmul2(xf1, s23));
-            mma16816(acc[nt][0], qf, as_u32(kf0), as_u32(kf1));
-            mma16816(acc[nt][KVQ_TC_QK_CHAINS - 1], qp, as_u32(kp0), as_u32(kp1));
+            if constexpr (PREC) {
+              const uint4 qfl = s_ql[PREC ? buf : 0][PREC ? sl : 0][PREC ? kq : 0][lane];
+              const uint4 qpl = s_ql[PREC ? buf : 0][PREC ? sl : 0][PREC ? kq + 4 : 0][lane];
+              const uint32_t fw[2] = {f0, f1}, pw[2] = {p0, p1};
+              uint32_t kfh[2], kfl[2], kph[2], kpl[2];
+              prec_keys<BITS>(fw, pw, zf, zp, a.rope, d.Bk, 16 * w + 8 * nt + tperm(g), r, kq, kfh, kfl, kph, kpl);
+              mma16816(acc[nt][0], qf, kfh[0], kfh[1]);
+              mma16816(acc[nt][0], qfl, kfh[0], kfh[1]);
+              mma16816(acc[nt][0], qf, kfl[0], kfl[1]);
+              mma16816(acc[nt][KVQ_TC_QK_CHAINS - 1], qp, kph[0], kph[1]);
+              mma16816(acc[nt][KVQ_TC_QK_CHAINS - 1], qpl, kph[0], kph[1]);
+              mma16816(acc[nt][KVQ_TC_QK_CHAINS - 1], qp, kpl[0], kpl[1]);
+            } else {
+              const __half2 xf0 = __hfma2(as_h2(f0), as_h2(zf.x), as_h2(zf.z));
+              const __half2 xf1 = __hfma2(as_h2(f1), as_h2(zf.y), as_h2(zf.w));
+              const __half2 xp0 = __hfma2(as_h2(p0), as_h2(zp.x), as_h2(zp.z));
+              const __half2 xp1 = __hfma2(as_h2(p1), as_h2(zp.y), as_h2(zp.w));
+              const uint4 rt = __ldg(rot + (nt * 4 + kq) * 32);
+              const __half2 c01 = as_h2(rt.x), c23 = as_h2(rt.y), s01 = as_h2(rt.z), s23 = as_h2(rt.w);
+              const __half2 kf0 = __hfma2(xf0, c01, __hneg2(__hmul2(xp0, s01)));
+              const __half2 kp0 = __hfma2(xp0, c01, __hmul2(xf0, s01));
+              const __half2 kf1 = __hfma2(xf1, c23, __hneg2(__hmul2(xp1, s23)));
+              const __half2 kp1 = __hfma2(xp1, c23, __hmul2(xf1, s23));
+              mma16816(acc[nt][0], qf, as_u32(kf0), as_u32(kf1));
+              mma16816(acc[nt][KVQ_TC_QK_CHAINS - 1], qp, as_u32(kp0), as_u32(kp1));
+            }
           }
         }
       } else {
@@ -707,6 +789,23 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
                 xs[s] = __hmul(k_tail[(size_t)j * kD + c], __float2half_rn(0.5f));
                 xs[4 + s] = __hmul(k_tail[(size_t)j * kD + c + HALF], __float2half_rn(0.5f));
               }
+            }
+            if constexpr (PREC) {
+              // fp16 keys are exact codes of themselves: s = 1, z = 0 in the fp32 path
+              const uint4 qfl = s_ql[PREC ? buf : 0][PREC ? sl : 0][PREC ? kq : 0][lane];
+              const uint4 qpl = s_ql[PREC ? buf : 0][PREC ? sl : 0][PREC ? kq + 4 : 0][lane];
+              const uint32_t fw[2] = {as_u32(__halves2half2(xs[0], xs[1])), as_u32(__halves2half2(xs[2], xs[3]))};
+              const uint32_t pw[2] = {as_u32(__halves2half2(xs[4], xs[5])), as_u32(__halves2half2(xs[6], xs[7]))};
+              const uint4 one = make_uint4(0x3C003C00u, 0x3C003C00u, 0u, 0u);
+              uint32_t kfh[2], kfl[2], kph[2], kpl[2];
+              prec_keys<BITS>(fw, pw, one, one, a.rope, d.Bk, 16 * w + 8 * nt + tperm(g), r, kq, kfh, kfl, kph, kpl);
+              mma16816(acc[nt][0], qf, kfh[0], kfh[1]);
+              mma16816(acc[nt][0], qfl, kfh[0], kfh[1]);
+              mma16816(acc[nt][0], qf, kfl[0], kfl[1]);
+              mma16816(acc[nt][KVQ_TC_QK_CHAINS - 1], qp, kph[0], kph[1]);
+              mma16816(acc[nt][KVQ_TC_QK_CHAINS - 1], qpl, kph[0], kph[1]);
+              mma16816(acc[nt][KVQ_TC_QK_CHAINS - 1], qp, kpl[0], kpl[1]);
+              continue;
             }
             const __half2 xf0 = __halves2half2(xs[0], xs[1]), xf1 = __halves2half2(xs[2], xs[3]);
             const __half2 xp0 = __halves2half2(xs[4], xs[5]), xp1 = __halves2half2(xs[6], xs[7]);
@@ -752,13 +851,19 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
           __syncwarp();
           if (g < G) {
             const uint8_t* qa = reinterpret_cast<const uint8_t*>(&s_qa[buf][sl][0][0]) + 64 * g;
+            const uint8_t* ql = reinterpret_cast<const uint8_t*>(&s_ql[PREC ? buf : 0][PREC ? sl : 0][0][0]) + 64 * g;
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
                 const float4 T = s_tok[w][8 * nt + 2 * r + e];
                 const int qa_off = __float_as_int(T.w);
-                const float wgt = fmaf(ld_h(qa + qa_off), T.y, ld_h(qa + qa_off + 2048) * T.z);
+                float q0 = ld_h(qa + qa_off), q1 = ld_h(qa + qa_off + 2048);
+                if constexpr (PREC) {
+                  q0 += ld_h(ql + qa_off);
+                  q1 += ld_h(ql + qa_off + 2048);
+                }
+                const float wgt = fmaf(q0, T.y, q1 * T.z);
                 sc[nt][e] = fmaf(T.x, wgt, sc[nt][e]);
               }
           }
@@ -895,7 +1000,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
           const __half2 h0 = __floats2half2_rn(A[0], A[1]), h1 = __floats2half2_rn(A[2], A[3]);
           bh0 = (g < G) ? as_u32(h0) : 0u;
           bh1 = (g < G) ? as_u32(h1) : 0u;
-          if (KVQ_TC_PV_LO) {
+          if (KVQ_TC_PV_LO || PREC) {
             const __half2 l0 = __floats2half2_rn(A[0] - __low2float(h0), A[1] - __high2float(h0));
             const __half2 l1 = __floats2half2_rn(A[2] - __low2float(h1), A[3] - __high2float(h1));
             bl0 = (g < G) ? as_u32(l0) : 0u;
@@ -912,7 +1017,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
         for (int mi = 0; mi < 2; ++mi) {
           const uint4 av = make_uint4(x0[2 * mi], x0[2 * mi + 1], x1[2 * mi], x1[2 * mi + 1]);
           mma16816(o[2 * c4 + mi], av, bh0, bh1);
-          if (KVQ_TC_PV_LO) mma16816(o[2 * c4 + mi], av, bl0, bl1);
+          if (KVQ_TC_PV_LO || PREC) mma16816(o[2 * c4 + mi], av, bl0, bl1);
         }
       }
     }
@@ -992,10 +1097,10 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
 
 }  // namespace tc
 
-template <int BITS, int G, int SL, bool OUTL, bool PAGED>
+template <int BITS, int G, int SL, bool OUTL, bool PAGED, bool PREC>
 cudaError_t launch_tc(const DecodeArgs& a, const tc::StageLayout& L, const CUtensorMap& tk,
                       const CUtensorMap& tv, size_t smem, cudaStream_t st);
-template <int BITS, int G, int SL, bool OUTL, bool PAGED>
+template <int BITS, int G, int SL, bool OUTL, bool PAGED, bool PREC>
 int tc_occupancy(size_t smem);
 
 }  // namespace kvq

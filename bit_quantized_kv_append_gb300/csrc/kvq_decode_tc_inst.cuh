@@ -8,10 +8,10 @@
 
 namespace kvq {
 
-template <int BITS, int G, int SL, bool OUTL, bool PAGED>
+template <int BITS, int G, int SL, bool OUTL, bool PAGED, bool PREC>
 cudaError_t launch_tc(const DecodeArgs& a, const tc::StageLayout& L, const CUtensorMap& tk,
                       const CUtensorMap& tv, size_t smem, cudaStream_t st) {
-  auto kern = tc::decode_tc_kernel<BITS, G, SL, OUTL, PAGED>;
+  auto kern = tc::decode_tc_kernel<BITS, G, SL, OUTL, PAGED, PREC>;
   // largest dynamic shared memory requested so far, per device (a function attribute per device)
   static std::atomic<size_t> smem_set[kMaxDevices];
   int dev = 0;
@@ -28,9 +28,9 @@ cudaError_t launch_tc(const DecodeArgs& a, const tc::StageLayout& L, const CUten
   return cudaGetLastError();
 }
 
-template <int BITS, int G, int SL, bool OUTL, bool PAGED>
+template <int BITS, int G, int SL, bool OUTL, bool PAGED, bool PREC>
 int tc_occupancy(size_t smem) {
-  auto kern = tc::decode_tc_kernel<BITS, G, SL, OUTL, PAGED>;
+  auto kern = tc::decode_tc_kernel<BITS, G, SL, OUTL, PAGED, PREC>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return 1;
   int n = 0;
@@ -38,11 +38,14 @@ int tc_occupancy(size_t smem) {
   return n < 1 ? 1 : n;
 }
 
-#define KVQ_TC_ONE(BITS, G, SL, OUTL, PAGED)                                                          \
-  template cudaError_t launch_tc<BITS, G, SL, OUTL, PAGED>(const DecodeArgs&, const tc::StageLayout&,     \
-                                                           const CUtensorMap&, const CUtensorMap&, size_t, \
-                                                           cudaStream_t);                                  \
-  template int tc_occupancy<BITS, G, SL, OUTL, PAGED>(size_t);
+#define KVQ_TC_ONE_P(BITS, G, SL, OUTL, PAGED, PREC)                                                         \
+  template cudaError_t launch_tc<BITS, G, SL, OUTL, PAGED, PREC>(const DecodeArgs&, const tc::StageLayout&,     \
+                                                                 const CUtensorMap&, const CUtensorMap&, size_t, \
+                                                                 cudaStream_t);                                  \
+  template int tc_occupancy<BITS, G, SL, OUTL, PAGED, PREC>(size_t);
+#define KVQ_TC_ONE(BITS, G, SL, OUTL, PAGED) \
+  KVQ_TC_ONE_P(BITS, G, SL, OUTL, PAGED, false) \
+  KVQ_TC_ONE_P(BITS, G, SL, OUTL, PAGED, true)
 #define KVQ_INSTANTIATE_TC(BITS, OUTL, PAGED) \
   KVQ_TC_ONE(BITS, 1, 1, OUTL, PAGED)         \
   KVQ_TC_ONE(BITS, 2, 1, OUTL, PAGED)         \

@@ -371,6 +371,7 @@ cudaError_t launch_decode_levels(const Dims& d, const kvq_cache& c, const __half
   a.v_outl = static_cast<const uint32_t*>(c.v_outl);
   a.q = q;
   a.rope = rope;
+  ws += kWsHeaderBytes / sizeof(float);   // the partials follow the status word
   a.ws = ws;
   a.T = c.T_cur;
   a.H_q = H_q;

@@ -23,11 +23,13 @@ import torch
 
 BUFFERS = ("k_codes", "k_meta", "k_tail", "k_outl", "v_codes", "v_meta", "v_outl")
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "KVQ_ERR_CAPACITY",
-          4: "KVQ_ERR_WORKSPACE", 5: "KVQ_ERR_CUDA"}
+          4: "KVQ_ERR_WORKSPACE", 5: "KVQ_ERR_CUDA", 6: "KVQ_ERR_TIMEOUT"}
+STATUS_TIMEOUT = 1          # bit of the device status word (first 4 bytes of a decode workspace)
+WS_HEADER_BYTES = 256
 EXPORTS = ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_append_window", "kvq_decode_attn", "kvq_decode_step",
            "kvq_paged_layout", "kvq_paged_append", "kvq_paged_decode_attn",
            "kvq_fit_levels", "kvq_append_levels", "kvq_decode_attn_levels",
-           "kvq_decode_attn_noalloc", "kvq_status_string", "kvq_version")
+           "kvq_decode_attn_noalloc", "kvq_decode_attn_diag", "kvq_status_string", "kvq_version")
 
 
 class KvqError(RuntimeError):
@@ -40,7 +42,10 @@ class Config(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("H_kv", ctypes.c_int32), ("D", ctypes.c_int32),
                 ("T_max", ctypes.c_int32), ("bits", ctypes.c_int32),
                 ("key_block", ctypes.c_int32), ("value_group", ctypes.c_int32),
-                ("outlier_frac", ctypes.c_float)]
+                ("outlier_frac", ctypes.c_float), ("flags", ctypes.c_int32)]
+
+
+FLAG_PRECISE_SCORES = 1
 
 
 class Layout(ctypes.Structure):
@@ -91,12 +96,15 @@ def lib():
                                              ctypes.c_float, vp, vp, ctypes.c_size_t, vp, vp]
         L.kvq_decode_attn_noalloc.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp,
                                               i32, i32, vp, ctypes.c_float, vp, vp]
+        L.kvq_decode_attn_diag.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp, i32, i32, vp,
+                                           ctypes.c_float, vp, vp, ctypes.c_size_t, ctypes.c_uint32, vp]
         L.kvq_status_string.argtypes = [ctypes.c_int]
         L.kvq_status_string.restype = ctypes.c_char_p
         L.kvq_version.restype = ctypes.c_char_p
         for fn in ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_append_window", "kvq_decode_attn", "kvq_decode_step",
                    "kvq_paged_layout", "kvq_paged_append", "kvq_paged_decode_attn", "kvq_fit_levels",
-                   "kvq_append_levels", "kvq_decode_attn_levels", "kvq_decode_attn_noalloc"):
+                   "kvq_append_levels", "kvq_decode_attn_levels", "kvq_decode_attn_noalloc",
+                   "kvq_decode_attn_diag"):
             getattr(L, fn).restype = ctypes.c_int
         _LIB = L
     return _LIB
@@ -124,8 +132,9 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def make_config(B, H_kv, D, T_max, bits=4, key_block=64, value_group=64, outlier_frac=0.0) -> Config:
-    return Config(B, H_kv, D, T_max, bits, key_block, value_group, float(outlier_frac))
+def make_config(B, H_kv, D, T_max, bits=4, key_block=64, value_group=64, outlier_frac=0.0,
+                flags=0) -> Config:
+    return Config(B, H_kv, D, T_max, bits, key_block, value_group, float(outlier_frac), int(flags))
 
 
 def layout(cfg: Config, H_q: int) -> Layout:
@@ -156,6 +165,14 @@ def decode_attn(cfg: Config, ref: CacheRef, q: torch.Tensor, H_q: int, q_pos: in
     _check(lib().kvq_decode_attn(ctypes.byref(cfg), ctypes.byref(ref), _ptr(q), int(H_q), int(q_pos),
                                  _ptr(rope), float(sm_scale), _ptr(out), _ptr(workspace),
                                  workspace.numel(), _stream(stream)), "kvq_decode_attn")
+
+
+def decode_attn_diag(cfg: Config, ref: CacheRef, q: torch.Tensor, H_q: int, q_pos: int,
+                     rope: Optional[torch.Tensor], sm_scale: float, out: torch.Tensor,
+                     workspace: torch.Tensor, tx_pad: int, stream=None):
+    _check(lib().kvq_decode_attn_diag(ctypes.byref(cfg), ctypes.byref(ref), _ptr(q), int(H_q), int(q_pos),
+                                      _ptr(rope), float(sm_scale), _ptr(out), _ptr(workspace), workspace.numel(),
+                                      int(tx_pad), _stream(stream)), "kvq_decode_attn_diag")
 
 
 def decode_step(cfg: Config, ref: CacheRef, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor,
@@ -217,8 +234,10 @@ class QuantizedKVCache:
     """One layer's low-bit KV cache in device memory (buffers sized by kvq_layout)."""
 
     def __init__(self, B, H_kv, D, T_max, bits=4, key_block=64, value_group=64, outlier_frac=0.0,
-                 H_q=None, rope_theta=0.0, device="cuda", rope_table: Optional[torch.Tensor] = None):
-        self.cfg = make_config(B, H_kv, D, T_max, bits, key_block, value_group, outlier_frac)
+                 H_q=None, rope_theta=0.0, device="cuda", rope_table: Optional[torch.Tensor] = None,
+                 precise=False):
+        self.cfg = make_config(B, H_kv, D, T_max, bits, key_block, value_group, outlier_frac,
+                               FLAG_PRECISE_SCORES if precise else 0)
         self.H_q = H_q or H_kv
         self.layout = layout(self.cfg, self.H_q)
         self.device = torch.device(device)
@@ -227,12 +246,21 @@ class QuantizedKVCache:
         self.buffers = {name: torch.empty(self.layout.bytes[i], dtype=torch.uint8, device=self.device)
                         for i, name in enumerate(BUFFERS)}
         self.workspace = torch.empty(self.layout.workspace_bytes, dtype=torch.uint8, device=self.device)
+        self.workspace[:WS_HEADER_BYTES].zero_()      # the device status word starts cleared
         self.rope_theta = float(rope_theta)
         self.rope = rope_table
         if self.rope is None and self.rope_theta > 0:
             self.rope = torch.empty(self.layout.rope_bytes, dtype=torch.uint8, device=self.device)
             rope_init(self.cfg, self.rope_theta, self.rope)
         self.T_cur = 0
+
+    def status(self) -> int:
+        """The device status word of this cache's decode workspace (reads it
+        back, which waits for the work queued so far)."""
+        return int(self.workspace[:4].view(torch.int32).item())
+
+    def clear_status(self):
+        self.workspace[:WS_HEADER_BYTES].zero_()
 
     # -- shape helpers
     @property
@@ -395,8 +423,10 @@ class PagedKVCache:
     sequence's fp16 tail of keys. ``lengths`` mirrors seq_len on the host."""
 
     def __init__(self, B, H_kv, D, T_max, n_blocks, bits=4, key_block=64, value_group=64, outlier_frac=0.0,
-                 H_q=None, rope_theta=0.0, device="cuda", rope_table: Optional[torch.Tensor] = None):
-        self.cfg = make_config(B, H_kv, D, T_max, bits, key_block, value_group, outlier_frac)
+                 H_q=None, rope_theta=0.0, device="cuda", rope_table: Optional[torch.Tensor] = None,
+                 precise=False):
+        self.cfg = make_config(B, H_kv, D, T_max, bits, key_block, value_group, outlier_frac,
+                               FLAG_PRECISE_SCORES if precise else 0)
         self.H_q = H_q or H_kv
         self.n_blocks = int(n_blocks)
         self.layout = paged_layout(self.cfg, self.n_blocks, self.H_q)
@@ -409,6 +439,7 @@ class PagedKVCache:
         self.seq_len = torch.zeros(B, dtype=torch.int32, device=self.device)
         self.lengths = [0] * B
         self.workspace = torch.empty(self.layout.workspace_bytes, dtype=torch.uint8, device=self.device)
+        self.workspace[:WS_HEADER_BYTES].zero_()      # the device status word starts cleared
         self.rope_theta = float(rope_theta)
         self.rope = rope_table
         if self.rope is None and self.rope_theta > 0:
@@ -437,7 +468,7 @@ class PagedKVCache:
 
     def _cfg_one(self) -> Config:
         c = self.cfg
-        return make_config(1, c.H_kv, c.D, c.T_max, c.bits, c.key_block, c.value_group, c.outlier_frac)
+        return make_config(1, c.H_kv, c.D, c.T_max, c.bits, c.key_block, c.value_group, c.outlier_frac, c.flags)
 
     def _check_kv(self, k_new, v_new, B):
         c = self.cfg

@@ -59,10 +59,36 @@ typedef enum kvq_status {
   KVQ_ERR_UNSUPPORTED = 2,  /* a configuration outside the supported set (see kvq_config) */
   KVQ_ERR_CAPACITY = 3,     /* T_cur + n_new > T_max */
   KVQ_ERR_WORKSPACE = 4,    /* workspace or RoPE table smaller than kvq_layout() says */
-  KVQ_ERR_CUDA = 5          /* the CUDA runtime reported an error at launch */
+  KVQ_ERR_CUDA = 5,         /* the CUDA runtime reported an error at launch */
+  KVQ_ERR_TIMEOUT = 6       /* a bounded wait of a kernel expired (read from the status word) */
 } kvq_status;
 
+/* Device status word: the first 4 bytes of every decode workspace (the
+ * layout's workspace_bytes include a 256-byte header for it; the partials
+ * follow). The head_dim-128 decode kernels wait on shared-memory barriers for
+ * their TMA copies; every wait is bounded (one second). When one expires
+ * the kernel ORs KVQ_STATUS_TIMEOUT into the word, waits (bounded) for its own
+ * copies, writes NaN partials for its part of the output and returns, so the
+ * context stays usable. The library never clears the word and never reads it
+ * back: zero the header when the workspace is allocated, and copy the word to
+ * the host (cudaMemcpyAsync, 4 bytes) when a check is wanted; a set bit means
+ * the outputs of the calls since it was cleared are not valid
+ * (KVQ_ERR_TIMEOUT). */
+#define KVQ_STATUS_TIMEOUT 1u
+
 #define KVQ_MAX_OUTLIERS 8  /* largest n_out per vector */
+
+/* kvq_config.flags. KVQ_FLAG_PRECISE_SCORES: decode attention at head_dim
+ * 128 dequantizes and rotates the keys in fp32 and splits both q . k operands
+ * into fp16 hi + lo parts (three tensor-core products each), so the scores
+ * carry about 22 significant bits instead of fp16's 11; P . V takes p * s as
+ * hi + lo as well. Without it the scores come from fp16 operands: their error
+ * is about 2^-11 of sum_c |q_c k_c| per token, which stays far below the
+ * outputs' tolerance while the logits span a few nats but moves the weights
+ * of attention whose competing logits are tens of nats apart from the rest.
+ * The flag costs decode time (see the design notes); head_dim 64 and the
+ * level-table calls compute in fp32 and ignore it. Other bits: reserved (0). */
+#define KVQ_FLAG_PRECISE_SCORES 1
 
 /* One layer's cache shape. Supported: bits in {2, 3, 4, 8} (8: the 8-bit
  * width of Quanto's block-wise scheme, page 3 "Quanto"); D in {64, 128};
@@ -79,6 +105,7 @@ typedef struct kvq_config {
   int32_t key_block;    /* Bk: tokens per key-quantization block */
   int32_t value_group;  /* Gv: channels per value-quantization group */
   float outlier_frac;   /* fraction of each K and V vector kept as fp16 outliers */
+  int32_t flags;        /* KVQ_FLAG_* (0: defaults) */
 } kvq_config;
 
 /* Cache buffers. Every buffer is [B][H_kv][...] with each (b, h_kv) stream
@@ -203,6 +230,20 @@ KVQ_API int kvq_append_window(const kvq_config* cfg, kvq_cache* cache, const voi
 KVQ_API int kvq_decode_attn(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t H_q,
                     int32_t q_pos, const void* rope_tab, float sm_scale, void* out,
                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Diagnostics of the bounded waits: kvq_decode_attn (head_dim 128) with every
+ * ring stage's barrier armed for tx_pad bytes (a multiple of 16) more than its
+ * copies deliver. With tx_pad > 0 no stage ever completes, so every wait
+ * expires (each after one second of the GPU's global timer): the kernel sets
+ * KVQ_STATUS_TIMEOUT in the workspace's status word, drains its copies
+ * (bounded waits again), writes NaN partials and returns; a call takes a few
+ * seconds. It exists to test the failure path without a fault (no page has a
+ * counterpart); tx_pad = 0 gives kvq_decode_attn's results. Errors: those of
+ * kvq_decode_attn; KVQ_ERR_UNSUPPORTED for head_dim 64 or a tx_pad that is
+ * not a multiple of 16. */
+KVQ_API int kvq_decode_attn_diag(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t H_q,
+                                 int32_t q_pos, const void* rope_tab, float sm_scale, void* out,
+                                 void* workspace, size_t workspace_bytes, uint32_t tx_pad, void* stream);
 
 /* One decode step of one layer in a single stream-ordered call: append the
  * new token of every sequence, then attend its query over all cached tokens
