@@ -472,6 +472,14 @@ int kvq_fit_levels(const double* u, size_t n, int32_t bits, int32_t iters, float
     }
   }
   for (int k = 0; k <= L; ++k) levels[k] = (float)lv[k];
+  // Levels distinct in binary64 can round to one binary32 value (tightly
+  // clustered samples); keep the table strictly increasing, as the append and
+  // decode calls require, by moving such a level up by one ulp (a backward
+  // pass keeps every interior level below l_L = 1).
+  for (int k = 1; k < L; ++k)
+    if (!(levels[k] > levels[k - 1])) levels[k] = nextafterf(levels[k - 1], 2.0f);
+  for (int k = L - 1; k >= 1; --k)
+    if (!(levels[k] < levels[k + 1])) levels[k] = nextafterf(levels[k + 1], -1.0f);
   return KVQ_OK;
 }
 

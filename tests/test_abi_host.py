@@ -279,6 +279,25 @@ def test_fit_levels_matches_the_oracle_fit(lib):
         kvq.fit_levels(bad, 2)
 
 
+def test_fit_levels_clustered_samples_stay_increasing(lib):
+    """Two clusters 1e-9 apart across a starting midpoint of the 8-bit grid:
+    the k-means gives them two levels that are distinct in binary64 but round
+    to one binary32 value; the library's table must still increase strictly
+    and be accepted by the level-table calls."""
+    import numpy as np
+    mid = 127.5 / 255
+    u = np.concatenate([np.full(4000, mid - 5e-10), np.full(4000, mid + 5e-10)])
+    got = kvq.fit_levels(u, 8, 40)
+    assert got[0] == 0 and got[-1] == 1 and np.all(np.diff(got.astype(np.float64)) > 0)
+    assert np.any(np.abs(got - np.float32(mid)) <= np.spacing(np.float32(mid)))   # the clusters got their levels
+    cfg = kvq.make_config(1, 2, 128, 256, 8, 64, 64, 0.0)
+    p = ctypes.c_void_p(FAKE)
+    r = _fake_cache(64)
+    # n_new = 0: every check of the table runs, nothing touches a device
+    assert lib.kvq_append_levels(ctypes.byref(cfg), ctypes.byref(r), p, p, 0,
+                                 got.ctypes.data_as(ctypes.c_void_p), None) == 0
+
+
 def test_levels_host_errors(lib):
     import numpy as np
     cfg = _cfg()                                    # bits 4, Bk 64, T_max 256, n_out 1
