@@ -24,7 +24,8 @@ SOURCES = ["kvq_api.cu", "kvq_rope.cu", "kvq_append.cu", "kvq_decode.cu", "kvq_l
            "kvq_decode_tc_b2o.cu", "kvq_decode_tc_b3o.cu", "kvq_decode_tc_b4o.cu",
            "kvq_decode_tc_b2p.cu", "kvq_decode_tc_b3p.cu", "kvq_decode_tc_b4p.cu",
            "kvq_decode_tc_b2op.cu", "kvq_decode_tc_b3op.cu", "kvq_decode_tc_b4op.cu",
-           "kvq_decode_tc_b8.cu", "kvq_decode_tc_b8o.cu", "kvq_decode_tc_b8p.cu", "kvq_decode_tc_b8op.cu"]
+           "kvq_decode_tc_b8.cu", "kvq_decode_tc_b8o.cu", "kvq_decode_tc_b8p.cu", "kvq_decode_tc_b8op.cu",
+           "kvq_decode_tc_b4lv.cu"]
 
 
 def nvcc() -> str:

@@ -518,6 +518,11 @@ int kvq_decode_attn_levels(const kvq_config* cfg, const kvq_cache* cache, const 
   if (cache->T_cur % d.Bk) return KVQ_ERR_UNSUPPORTED;                     // whole key blocks only
   rc = device_ok();
   if (rc) return rc;
+  if (d.D == 128 && d.bits == 4 && !(d.flags & KVQ_FLAG_PRECISE_SCORES))   // the tensor-core kernel
+    return cuda_status(launch_decode(d, *cache, static_cast<const __half*>(q), H_q, q_pos,
+                                     static_cast<const float2*>(rope_tab), sm_scale, static_cast<__half*>(out),
+                                     static_cast<float*>(workspace), static_cast<cudaStream_t>(stream), 0, nullptr,
+                                     0, t.lv));
   return cuda_status(launch_decode_levels(d, *cache, static_cast<const __half*>(q), H_q, q_pos,
                                           static_cast<const float2*>(rope_tab), sm_scale,
                                           static_cast<__half*>(out), static_cast<float*>(workspace), t,

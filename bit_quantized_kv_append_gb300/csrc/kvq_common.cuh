@@ -114,10 +114,11 @@ cudaError_t launch_append(const Dims& d, const kvq_cache& c, const __half* k_new
 // split_cap > 0 bounds the T splits (and the workspace stride) below max_splits().
 // pg: a paged cache (per-sequence lengths; q of sequence b at seq_len[b] - 1).
 // ws: the workspace, status word first (kWsHeaderBytes), partials after it.
-// tx_pad: diagnostics of the bounded waits (0: none).
+// tx_pad: diagnostics of the bounded waits (0: none). levels: the 16 levels
+// of a non-uniform 4-bit cache (head_dim 128; NULL: uniform codes).
 cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, int H_q, int q_pos,
                           const float2* rope, float sm_scale, __half* out, float* ws,
                           cudaStream_t st, int split_cap = 0, const Paged* pg = nullptr,
-                          uint32_t tx_pad = 0);
+                          uint32_t tx_pad = 0, const float* levels = nullptr);
 
 }  // namespace kvq

@@ -151,37 +151,44 @@ using TcLaunchFn = cudaError_t (*)(const DecodeArgs&, const tc::StageLayout&, co
                                    const CUtensorMap&, size_t, cudaStream_t);
 using TcOccFn = int (*)(size_t);
 
-template <int BITS, int SL, bool OUTL, bool PAGED, bool PREC>
+template <int BITS, int SL, bool OUTL, bool PAGED, int MODE>
 void pick_tc_g(int G, TcLaunchFn* f, TcOccFn* o) {
   switch (G) {
-    case 1: *f = launch_tc<BITS, 1, SL, OUTL, PAGED, PREC>; *o = tc_occupancy<BITS, 1, SL, OUTL, PAGED, PREC>; break;
-    case 2: *f = launch_tc<BITS, 2, SL, OUTL, PAGED, PREC>; *o = tc_occupancy<BITS, 2, SL, OUTL, PAGED, PREC>; break;
-    case 4: *f = launch_tc<BITS, 4, SL, OUTL, PAGED, PREC>; *o = tc_occupancy<BITS, 4, SL, OUTL, PAGED, PREC>; break;
-    default: *f = launch_tc<BITS, 8, SL, OUTL, PAGED, PREC>; *o = tc_occupancy<BITS, 8, SL, OUTL, PAGED, PREC>; break;
+    case 1: *f = launch_tc<BITS, 1, SL, OUTL, PAGED, MODE>; *o = tc_occupancy<BITS, 1, SL, OUTL, PAGED, MODE>; break;
+    case 2: *f = launch_tc<BITS, 2, SL, OUTL, PAGED, MODE>; *o = tc_occupancy<BITS, 2, SL, OUTL, PAGED, MODE>; break;
+    case 4: *f = launch_tc<BITS, 4, SL, OUTL, PAGED, MODE>; *o = tc_occupancy<BITS, 4, SL, OUTL, PAGED, MODE>; break;
+    default: *f = launch_tc<BITS, 8, SL, OUTL, PAGED, MODE>; *o = tc_occupancy<BITS, 8, SL, OUTL, PAGED, MODE>; break;
   }
 }
 
-template <int BITS, bool PAGED, bool PREC>
+template <int BITS, bool PAGED, int MODE>
 void pick_tc_p(int Bk, int G, bool outl, TcLaunchFn* f, TcOccFn* o) {
   if (Bk == 64)
-    outl ? pick_tc_g<BITS, 1, true, PAGED, PREC>(G, f, o) : pick_tc_g<BITS, 1, false, PAGED, PREC>(G, f, o);
+    outl ? pick_tc_g<BITS, 1, true, PAGED, MODE>(G, f, o) : pick_tc_g<BITS, 1, false, PAGED, MODE>(G, f, o);
   else
-    outl ? pick_tc_g<BITS, 2, true, PAGED, PREC>(G, f, o) : pick_tc_g<BITS, 2, false, PAGED, PREC>(G, f, o);
+    outl ? pick_tc_g<BITS, 2, true, PAGED, MODE>(G, f, o) : pick_tc_g<BITS, 2, false, PAGED, MODE>(G, f, o);
 }
+// mode 0: fp16-operand scores, 1: precise scores, 2: level tables (4-bit, contiguous only)
 template <int BITS>
-void pick_tc(int Bk, int G, bool outl, bool paged, bool prec, TcLaunchFn* f, TcOccFn* o) {
-  if (prec) paged ? pick_tc_p<BITS, true, true>(Bk, G, outl, f, o) : pick_tc_p<BITS, false, true>(Bk, G, outl, f, o);
-  else paged ? pick_tc_p<BITS, true, false>(Bk, G, outl, f, o) : pick_tc_p<BITS, false, false>(Bk, G, outl, f, o);
+void pick_tc(int Bk, int G, bool outl, bool paged, int mode, TcLaunchFn* f, TcOccFn* o) {
+  if constexpr (BITS == 4) {
+    if (mode == 2) {
+      pick_tc_p<4, false, 2>(Bk, G, outl, f, o);
+      return;
+    }
+  }
+  if (mode == 1) paged ? pick_tc_p<BITS, true, 1>(Bk, G, outl, f, o) : pick_tc_p<BITS, false, 1>(Bk, G, outl, f, o);
+  else paged ? pick_tc_p<BITS, true, 0>(Bk, G, outl, f, o) : pick_tc_p<BITS, false, 0>(Bk, G, outl, f, o);
 }
 
-int cached_tc_occupancy(int dev, int bits, int Bk, int G, bool outl, bool paged, bool prec, size_t smem,
+int cached_tc_occupancy(int dev, int bits, int Bk, int G, bool outl, bool paged, int mode, size_t smem,
                         TcOccFn fn) {
   struct Slot { size_t smem; int occ; };
   static std::mutex mu;
-  static Slot cache[kMaxDevices][4][2][4][2][2][2];
+  static Slot cache[kMaxDevices][4][2][4][2][2][3];
   const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
   std::lock_guard<std::mutex> lock(mu);
-  Slot& s = cache[dev][bits == 8 ? 3 : bits - 2][Bk == 128][gi][outl ? 1 : 0][paged ? 1 : 0][prec ? 1 : 0];
+  Slot& s = cache[dev][bits == 8 ? 3 : bits - 2][Bk == 128][gi][outl ? 1 : 0][paged ? 1 : 0][mode];
   if (s.occ == 0 || s.smem != smem) {
     s.occ = fn(smem);
     s.smem = smem;
@@ -193,7 +200,8 @@ int cached_tc_occupancy(int dev, int bits, int Bk, int G, bool outl, bool paged,
 
 cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, int H_q, int q_pos,
                           const float2* rope, float sm_scale, __half* out, float* ws_all,
-                          cudaStream_t st, int split_cap, const Paged* pg, uint32_t tx_pad) {
+                          cudaStream_t st, int split_cap, const Paged* pg, uint32_t tx_pad,
+                          const float* levels) {
   float* ws = ws_all + kWsHeaderBytes / sizeof(float);   // the partials follow the status word
   DecodeArgs a;
   a.d = d;
@@ -209,6 +217,7 @@ cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, in
   a.ws = ws;
   a.status = reinterpret_cast<uint32_t*>(ws_all);
   a.tx_pad = tx_pad;
+  for (int k = 0; k < 16; ++k) a.lv[k] = levels ? levels[k] : 0.0f;
   // paged: the grid is sized for the longest sequence; each CTA reads its own length
   a.T = pg ? pg->max_len : c.T_cur;
   a.n_full = a.T / d.Bk;
@@ -239,14 +248,15 @@ cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, in
     TcLaunchFn fn = nullptr;
     TcOccFn occ_fn = nullptr;
     const bool paged = pg != nullptr;
-    const bool prec = (d.flags & KVQ_FLAG_PRECISE_SCORES) != 0;
+    const int mode = levels ? 2 : (d.flags & KVQ_FLAG_PRECISE_SCORES) ? 1 : 0;
+    if (mode == 2 && (d.bits != 4 || paged)) return cudaErrorInvalidValue;   // the API only asks for 4-bit caches
     switch (d.bits) {
-      case 2: pick_tc<2>(d.Bk, G, d.n_out > 0, paged, prec, &fn, &occ_fn); break;
-      case 3: pick_tc<3>(d.Bk, G, d.n_out > 0, paged, prec, &fn, &occ_fn); break;
-      case 8: pick_tc<8>(d.Bk, G, d.n_out > 0, paged, prec, &fn, &occ_fn); break;
-      default: pick_tc<4>(d.Bk, G, d.n_out > 0, paged, prec, &fn, &occ_fn); break;
+      case 2: pick_tc<2>(d.Bk, G, d.n_out > 0, paged, mode, &fn, &occ_fn); break;
+      case 3: pick_tc<3>(d.Bk, G, d.n_out > 0, paged, mode, &fn, &occ_fn); break;
+      case 8: pick_tc<8>(d.Bk, G, d.n_out > 0, paged, mode, &fn, &occ_fn); break;
+      default: pick_tc<4>(d.Bk, G, d.n_out > 0, paged, mode, &fn, &occ_fn); break;
     }
-    const int occ = cached_tc_occupancy(dev, d.bits, d.Bk, G, d.n_out > 0, paged, prec, smem, occ_fn);
+    const int occ = cached_tc_occupancy(dev, d.bits, d.Bk, G, d.n_out > 0, paged, mode, smem, occ_fn);
     a.n_split = paged ? paged_splits(d, units, sms * occ, a.S) : choose_splits(d.B * d.H_kv, units, sms * occ, a.S);
     e = fn(a, L, tk, tv, smem, st);
   } else {

@@ -372,10 +372,28 @@ __device__ __forceinline__ void value_pair(const uint8_t* vc, const LaneOff& o, 
     b[3] = x6 & 0x00380038u;
   }
 }
-// Power of two that undoes the subnormal encoding of value code b[e].
-template <int BITS>
+// Level tables, 4-bit codes: the value A operands as fp16 levels. A byte of a
+// code row holds two channels; s_lut[byte] is {l[lo nibble], l[hi nibble]}.
+// b[0] = (l[channel 32 c4 + 4 g] at t, at t + 1), b[1] the next channel,
+// b[2], b[3] the following byte's two channels (the layout value_pair<4> gives).
+__device__ __forceinline__ void value_pair_lv(const uint8_t* vc, const LaneOff& o, int sl, int rp, int c4,
+                                              const uint32_t* s_lut, int bb, uint32_t (&b)[4]) {
+  const uint8_t* p = vc + (o.vb + ((c4 << 4) ^ o.vx)) + 4096 * sl + 512 * rp;
+  const uint32_t A = ld_s32(p), B = ld_s32(p + 64);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t la = s_lut[(A >> (8 * (bb + h))) & 0xFFu], lb = s_lut[(B >> (8 * (bb + h))) & 0xFFu];
+    b[2 * h] = __byte_perm(la, lb, 0x5410u);
+    b[2 * h + 1] = __byte_perm(la, lb, 0x7632u);
+  }
+}
+
+// Power of two that undoes the subnormal encoding of value code b[e] (level
+// tables carry their fp16 levels unscaled: 1).
+template <int BITS, bool LV = false>
 __device__ __forceinline__ float value_scale(int e) {
-  if constexpr (BITS == 8) return 16777216.0f;                                  // 2^24
+  if constexpr (LV) return 1.0f;
+  else if constexpr (BITS == 8) return 16777216.0f;                             // 2^24
   else if constexpr (BITS == 4) return (e & 1) ? 1048576.0f : 16777216.0f;    // 2^20 : 2^24
   else if constexpr (BITS == 2) return 16777216.0f / (float)(1 << (2 * e));    // 2^(24-2e)
   else return (e & 1) ? 2097152.0f : 16777216.0f;                             // 2^21 : 2^24
@@ -434,10 +452,15 @@ __device__ __forceinline__ int acc_index(int w, int c, int h) {
 // OUTL: the cache keeps outliers (n_out > 0); without them the outlier code
 // is not compiled in. PAGED: a paged, ragged batch (block table, per-sequence
 // lengths); the contiguous instantiation holds none of that code.
-template <int BITS, int G, int SL, bool OUTL, bool PAGED, bool PREC>
+// MODE 0: fp16-operand scores; 1: precise scores (PREC); 2: codes index the
+// level table a.lv (LV, non-uniform codes at 4 bits).
+template <int BITS, int G, int SL, bool OUTL, bool PAGED, int MODE>
 __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const DecodeArgs a, const StageLayout L,
                                                              const __grid_constant__ CUtensorMap tm_k,
                                                              const __grid_constant__ CUtensorMap tm_v) {
+  constexpr bool PREC = MODE == 1;
+  constexpr bool LV = MODE == 2;
+  static_assert(!LV || BITS == 4, "level tables run at 4 bits");
   constexpr int HALF = kD / 2;
   constexpr int BK = 64 * SL;
   constexpr int NST = ring_stages(BK);
@@ -448,8 +471,10 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
   __shared__ int s_abort;
   __shared__ float s_qp[G][kD];                               // q at q_pos, times 2*sm_scale*log2(e)
   __shared__ const void* s_src[4];                            // this stream's k_meta, v_meta, k_outl, v_outl
-  __shared__ __align__(16) uint4 s_qa[2][SL][8][32];          // A quads {a0, 0, a2, 0} of 2 q_block, fp16
-  __shared__ __align__(16) uint4 s_ql[PREC ? 2 : 1][PREC ? SL : 1][PREC ? 8 : 1][32];   // PREC: the lo parts
+  // q . k A fragments {a0, a2} of 2 q_block, fp16 (a1 = a3 = 0: rows g + 8 are
+  // padding heads), double-buffered by block parity; PREC: the lo parts
+  __shared__ __align__(16) uint2 s_qa[2][SL][8][32];
+  __shared__ __align__(16) uint2 s_ql[PREC ? 2 : 1][PREC ? SL : 1][PREC ? 8 : 1][PREC ? 32 : 1];
   __shared__ __align__(16) uint4 s_kz[2][4][4][2];            // key {s01, s23, z01, z23} / 2 [k-step][quarter][half]
   __shared__ __align__(16) float4 s_acc[kWarps][8][8][RQ];    // P.V sums in the frame m_frame, fragment order
   __shared__ __align__(16) float4 s_tok[kWarps][16];          // key-outlier staging of one warp
@@ -458,6 +483,8 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
   __shared__ float s_w[OUTL ? HALF : 1];                      // RoPE frequency of every channel pair
   __shared__ float s_wm[kWarps][G], s_wl[kWarps][G], s_wf[kWarps][G];
   __shared__ float s_z[kWarps][G][4];                         // zero-point sums per 32-channel block
+  __shared__ uint32_t s_lut[LV ? 256 : 1];                    // LV: {l[b & 15], l[b >> 4]} fp16 per code byte b
+  __shared__ float s_lvf[LV ? 16 : 1];                        // LV: the levels
 
   const Dims d = a.d;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -535,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
   {
     int rr, kq, s;
     kslot<BITS>(qi, rr, kq, s);
-    q_off = (uint32_t)((kq * 32 + rr) * 16 + aslot_byte(s));   // head 0, first half; + 64 g, + 2048 partner
+    q_off = (uint32_t)((kq * 32 + rr) * 8 + aslot2_byte(s));   // head 0, first half; + 32 g, + 1024 partner
   }
   // key scale/zero: thread owns channel tid
   uint32_t kz_off;
@@ -579,14 +606,14 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
           const float x = s_qp[0][qi], y = s_qp[0][qi + HALF];
           const bool part = tid >= HALF;
           const float v = part ? fmaf(y, rs.x, -x * rs.y) : fmaf(x, rs.x, y * rs.y);   // apply R(-t)
-          put(part ? 2048 : 0, v);
+          put(part ? 1024 : 0, v);
         } else {
 #pragma unroll
           for (int gg = tid >> 6; gg < G; gg += 2) {
             const float x = s_qp[gg][qi], y = s_qp[gg][qi + HALF];
             const float x2 = fmaf(x, rs.x, y * rs.y), y2 = fmaf(y, rs.x, -x * rs.y);   // apply R(-t)
-            put(64 * gg, x2);
-            put(64 * gg + 2048, y2);
+            put(32 * gg, x2);
+            put(32 * gg + 1024, y2);
           }
         }
       }
@@ -643,6 +670,11 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
     for (int e = tid; e < (int)(sizeof(s_qa) / 4); e += kThreads) z[e] = 0u;
     uint32_t* zl = reinterpret_cast<uint32_t*>(&s_ql[0][0][0][0]);
     for (int e = tid; e < (int)(sizeof(s_ql) / 4); e += kThreads) zl[e] = 0u;
+    if constexpr (LV) {
+      for (int e = tid; e < 256; e += kThreads)
+        s_lut[e] = as_u32(__floats2half2_rn(a.lv[e & 15], a.lv[e >> 4]));
+      if (tid < 16) s_lvf[tid] = a.lv[tid];
+    }
     float* f = reinterpret_cast<float*>(&s_acc[0][0][0][0]);
     for (int e = tid; e < (int)(sizeof(s_acc) / 4); e += kThreads) f[e] = 0.0f;
   }
@@ -675,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
     if (r < RQ) {
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        const float v0 = value_scale<BITS>(2 * (mt & 1)), v1 = value_scale<BITS>(2 * (mt & 1) + 1);
+        const float v0 = value_scale<BITS, LV>(2 * (mt & 1)), v1 = value_scale<BITS, LV>(2 * (mt & 1) + 1);
         float4 v = s_acc[w][mt][g][r];
         v.x = fmaf(o[mt][0], v0 * fa, v.x);
         v.y = fmaf(o[mt][1], v0 * fb, v.y);
@@ -729,7 +761,8 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
         }
 #pragma unroll
         for (int kq = 0; kq < 4; ++kq) {
-          const uint4 qf = s_qa[buf][sl][kq][lane], qp = s_qa[buf][sl][kq + 4][lane];
+          const uint2 qf2 = s_qa[buf][sl][kq][lane], qp2 = s_qa[buf][sl][kq + 4][lane];
+          const uint4 qf = make_uint4(qf2.x, 0u, qf2.y, 0u), qp = make_uint4(qp2.x, 0u, qp2.y, 0u);
           const uint4 zf = s_kz[buf][kq][r][0], zp = s_kz[buf][kq][r][1];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
@@ -740,12 +773,25 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
               key_codes8(wf[kq], f0, f1);
               key_codes8(wp[kq], p0, p1);
             } else {
-              key_codes<BITS>(kw[nt].f, lo.ksh, kq, f0, f1);
-              key_codes<BITS>(kw[nt].p, lo.ksh, kq, p0, p1);
+              if constexpr (LV) {
+                // levels of slots (0, 2) from byte kq & 1 of the word, (1, 3) from byte (kq & 1) + 2
+                const uint32_t Wf = kw[nt].f[kq >> 1], Wp = kw[nt].p[kq >> 1];
+                const int sh = 8 * (kq & 1);   // kq is unrolled: a constant shift
+                const uint32_t fa = s_lut[(Wf >> sh) & 0xFFu], fb = s_lut[(Wf >> (sh + 16)) & 0xFFu];
+                const uint32_t pa = s_lut[(Wp >> sh) & 0xFFu], pb = s_lut[(Wp >> (sh + 16)) & 0xFFu];
+                f0 = __byte_perm(fa, fb, 0x5410u);
+                f1 = __byte_perm(fa, fb, 0x7632u);
+                p0 = __byte_perm(pa, pb, 0x5410u);
+                p1 = __byte_perm(pa, pb, 0x7632u);
+              } else {
+                key_codes<BITS>(kw[nt].f, lo.ksh, kq, f0, f1);
+                key_codes<BITS>(kw[nt].p, lo.ksh, kq, p0, p1);
+              }
             }
             if constexpr (PREC) {
-              const uint4 qfl = s_ql[PREC ? buf : 0][PREC ? sl : 0][PREC ? kq : 0][lane];
-              const uint4 qpl = s_ql[PREC ? buf : 0][PREC ? sl : 0][PREC ? kq + 4 : 0][lane];
+              const uint2 qfl2 = s_ql[PREC ? buf : 0][PREC ? sl : 0][PREC ? kq : 0][PREC ? lane : 0];
+              const uint2 qpl2 = s_ql[PREC ? buf : 0][PREC ? sl : 0][PREC ? kq + 4 : 0][PREC ? lane : 0];
+              const uint4 qfl = make_uint4(qfl2.x, 0u, qfl2.y, 0u), qpl = make_uint4(qpl2.x, 0u, qpl2.y, 0u);
               const uint32_t fw[2] = {f0, f1}, pw[2] = {p0, p1};
               uint32_t kfh[2], kfl[2], kph[2], kpl[2];
               prec_keys<BITS>(fw, pw, zf, zp, a.rope, d.Bk, 16 * w + 8 * nt + tperm(g), r, kq, kfh, kfl, kph, kpl);
@@ -776,7 +822,8 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
         const __half* k_tail = a.k_tail + (size_t)bh * k_tail_stream(d);
 #pragma unroll
         for (int kq = 0; kq < 4; ++kq) {
-          const uint4 qf = s_qa[buf][sl][kq][lane], qp = s_qa[buf][sl][kq + 4][lane];
+          const uint2 qf2 = s_qa[buf][sl][kq][lane], qp2 = s_qa[buf][sl][kq + 4][lane];
+          const uint4 qf = make_uint4(qf2.x, 0u, qf2.y, 0u), qp = make_uint4(qp2.x, 0u, qp2.y, 0u);
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
             const int j = 64 * sl + 16 * w + 8 * nt + tperm(g);
@@ -792,8 +839,9 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
             }
             if constexpr (PREC) {
               // fp16 keys are exact codes of themselves: s = 1, z = 0 in the fp32 path
-              const uint4 qfl = s_ql[PREC ? buf : 0][PREC ? sl : 0][PREC ? kq : 0][lane];
-              const uint4 qpl = s_ql[PREC ? buf : 0][PREC ? sl : 0][PREC ? kq + 4 : 0][lane];
+              const uint2 qfl2 = s_ql[PREC ? buf : 0][PREC ? sl : 0][PREC ? kq : 0][PREC ? lane : 0];
+              const uint2 qpl2 = s_ql[PREC ? buf : 0][PREC ? sl : 0][PREC ? kq + 4 : 0][PREC ? lane : 0];
+              const uint4 qfl = make_uint4(qfl2.x, 0u, qfl2.y, 0u), qpl = make_uint4(qpl2.x, 0u, qpl2.y, 0u);
               const uint32_t fw[2] = {as_u32(__halves2half2(xs[0], xs[1])), as_u32(__halves2half2(xs[2], xs[3]))};
               const uint32_t pw[2] = {as_u32(__halves2half2(xs[4], xs[5])), as_u32(__halves2half2(xs[6], xs[7]))};
               const uint4 one = make_uint4(0x3C003C00u, 0x3C003C00u, 0u, 0u);
@@ -838,7 +886,8 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
             const uint32_t e = ko[row * n_out + oi];
             const int c = (int)(e & (kD - 1));
             const uint32_t m = km[c];
-            const float xd = fmaf(small_int_f(tile_code<BITS>(kc, row, c)), h2f((uint16_t)(m & 0xFFFFu)),
+            const uint32_t qc = tile_code<BITS>(kc, row, c);
+            const float xd = fmaf(LV ? s_lvf[LV ? qc : 0] : small_int_f(qc), h2f((uint16_t)(m & 0xFFFFu)),
                                   h2f((uint16_t)(m >> 16)));
             int rr, kq, s;
             kslot<BITS>(c & (HALF - 1), rr, kq, s);
@@ -846,22 +895,22 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
             sincos_small((float)(row & 63) * s_w[c & (HALF - 1)], sn, cs);
             const bool first = c < HALF;
             s_tok[w][lane] = make_float4(0.5f * (h2f((uint16_t)(e >> 16)) - xd), first ? cs : -sn, first ? sn : cs,
-                                         __int_as_float((kq * 32 + rr) * 16 + aslot_byte(s)));
+                                         __int_as_float((kq * 32 + rr) * 8 + aslot2_byte(s)));
           }
           __syncwarp();
           if (g < G) {
-            const uint8_t* qa = reinterpret_cast<const uint8_t*>(&s_qa[buf][sl][0][0]) + 64 * g;
-            const uint8_t* ql = reinterpret_cast<const uint8_t*>(&s_ql[PREC ? buf : 0][PREC ? sl : 0][0][0]) + 64 * g;
+            const uint8_t* qa = reinterpret_cast<const uint8_t*>(&s_qa[buf][sl][0][0]) + 32 * g;
+            const uint8_t* ql = reinterpret_cast<const uint8_t*>(&s_ql[PREC ? buf : 0][PREC ? sl : 0][0][0]) + 32 * g;
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
                 const float4 T = s_tok[w][8 * nt + 2 * r + e];
                 const int qa_off = __float_as_int(T.w);
-                float q0 = ld_h(qa + qa_off), q1 = ld_h(qa + qa_off + 2048);
+                float q0 = ld_h(qa + qa_off), q1 = ld_h(qa + qa_off + 1024);
                 if constexpr (PREC) {
                   q0 += ld_h(ql + qa_off);
-                  q1 += ld_h(ql + qa_off + 2048);
+                  q1 += ld_h(ql + qa_off + 1024);
                 }
                 const float wgt = fmaf(q0, T.y, q1 * T.z);
                 sc[nt][e] = fmaf(T.x, wgt, sc[nt][e]);
@@ -955,7 +1004,8 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
             const uint32_t e = vo[row * n_out + oi];
             c = (int)(e & (kD - 1));
             const float2 sz = __half22float2(as_h2(vm[(row << ng_sh) + (c >> gv_sh)]));
-            s_vd[w][lane] = h2f((uint16_t)(e >> 16)) - fmaf(small_int_f(tile_code<BITS>(vc, row, c)), sz.x, sz.y);
+            const uint32_t qc = tile_code<BITS>(vc, row, c);
+            s_vd[w][lane] = h2f((uint16_t)(e >> 16)) - fmaf(LV ? s_lvf[LV ? qc : 0] : small_int_f(qc), sz.x, sz.y);
           }
           const uint32_t peers = __match_any_sync(0xffffffffu, c);
           __syncwarp();
@@ -1011,8 +1061,13 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
           zacc[c4] = zacc[c4 - 1];   // same value group: the two sums stay equal
         }
         uint32_t x0[4], x1[4];
-        value_pair<BITS>(vc, lo, sl, 0, c4, x0);
-        value_pair<BITS>(vc, lo, sl, 1, c4, x1);
+        if constexpr (LV) {
+          value_pair_lv(vc, lo, sl, 0, c4, s_lut, 2 * (g & 1), x0);
+          value_pair_lv(vc, lo, sl, 1, c4, s_lut, 2 * (g & 1), x1);
+        } else {
+          value_pair<BITS>(vc, lo, sl, 0, c4, x0);
+          value_pair<BITS>(vc, lo, sl, 1, c4, x1);
+        }
 #pragma unroll
         for (int mi = 0; mi < 2; ++mi) {
           const uint4 av = make_uint4(x0[2 * mi], x0[2 * mi + 1], x1[2 * mi], x1[2 * mi + 1]);
@@ -1097,10 +1152,10 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
 
 }  // namespace tc
 
-template <int BITS, int G, int SL, bool OUTL, bool PAGED, bool PREC>
+template <int BITS, int G, int SL, bool OUTL, bool PAGED, int MODE>
 cudaError_t launch_tc(const DecodeArgs& a, const tc::StageLayout& L, const CUtensorMap& tk,
                       const CUtensorMap& tv, size_t smem, cudaStream_t st);
-template <int BITS, int G, int SL, bool OUTL, bool PAGED, bool PREC>
+template <int BITS, int G, int SL, bool OUTL, bool PAGED, int MODE>
 int tc_occupancy(size_t smem);
 
 }  // namespace kvq

@@ -8,10 +8,10 @@
 
 namespace kvq {
 
-template <int BITS, int G, int SL, bool OUTL, bool PAGED, bool PREC>
+template <int BITS, int G, int SL, bool OUTL, bool PAGED, int MODE>
 cudaError_t launch_tc(const DecodeArgs& a, const tc::StageLayout& L, const CUtensorMap& tk,
                       const CUtensorMap& tv, size_t smem, cudaStream_t st) {
-  auto kern = tc::decode_tc_kernel<BITS, G, SL, OUTL, PAGED, PREC>;
+  auto kern = tc::decode_tc_kernel<BITS, G, SL, OUTL, PAGED, MODE>;
   // largest dynamic shared memory requested so far, per device (a function attribute per device)
   static std::atomic<size_t> smem_set[kMaxDevices];
   int dev = 0;
@@ -28,9 +28,9 @@ cudaError_t launch_tc(const DecodeArgs& a, const tc::StageLayout& L, const CUten
   return cudaGetLastError();
 }
 
-template <int BITS, int G, int SL, bool OUTL, bool PAGED, bool PREC>
+template <int BITS, int G, int SL, bool OUTL, bool PAGED, int MODE>
 int tc_occupancy(size_t smem) {
-  auto kern = tc::decode_tc_kernel<BITS, G, SL, OUTL, PAGED, PREC>;
+  auto kern = tc::decode_tc_kernel<BITS, G, SL, OUTL, PAGED, MODE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return 1;
   int n = 0;
@@ -38,14 +38,25 @@ int tc_occupancy(size_t smem) {
   return n < 1 ? 1 : n;
 }
 
-#define KVQ_TC_ONE_P(BITS, G, SL, OUTL, PAGED, PREC)                                                         \
-  template cudaError_t launch_tc<BITS, G, SL, OUTL, PAGED, PREC>(const DecodeArgs&, const tc::StageLayout&,     \
+#define KVQ_TC_ONE_P(BITS, G, SL, OUTL, PAGED, MODE)                                                         \
+  template cudaError_t launch_tc<BITS, G, SL, OUTL, PAGED, MODE>(const DecodeArgs&, const tc::StageLayout&,     \
                                                                  const CUtensorMap&, const CUtensorMap&, size_t, \
                                                                  cudaStream_t);                                  \
-  template int tc_occupancy<BITS, G, SL, OUTL, PAGED, PREC>(size_t);
+  template int tc_occupancy<BITS, G, SL, OUTL, PAGED, MODE>(size_t);
+// modes 0 (fp16-operand scores) and 1 (precise scores)
 #define KVQ_TC_ONE(BITS, G, SL, OUTL, PAGED) \
-  KVQ_TC_ONE_P(BITS, G, SL, OUTL, PAGED, false) \
-  KVQ_TC_ONE_P(BITS, G, SL, OUTL, PAGED, true)
+  KVQ_TC_ONE_P(BITS, G, SL, OUTL, PAGED, 0) \
+  KVQ_TC_ONE_P(BITS, G, SL, OUTL, PAGED, 1)
+// mode 2 (level tables): 4-bit contiguous caches
+#define KVQ_INSTANTIATE_TC_LV(OUTL)      \
+  KVQ_TC_ONE_P(4, 1, 1, OUTL, false, 2)  \
+  KVQ_TC_ONE_P(4, 2, 1, OUTL, false, 2)  \
+  KVQ_TC_ONE_P(4, 4, 1, OUTL, false, 2)  \
+  KVQ_TC_ONE_P(4, 8, 1, OUTL, false, 2)  \
+  KVQ_TC_ONE_P(4, 1, 2, OUTL, false, 2)  \
+  KVQ_TC_ONE_P(4, 2, 2, OUTL, false, 2)  \
+  KVQ_TC_ONE_P(4, 4, 2, OUTL, false, 2)  \
+  KVQ_TC_ONE_P(4, 8, 2, OUTL, false, 2)
 #define KVQ_INSTANTIATE_TC(BITS, OUTL, PAGED) \
   KVQ_TC_ONE(BITS, 1, 1, OUTL, PAGED)         \
   KVQ_TC_ONE(BITS, 2, 1, OUTL, PAGED)         \

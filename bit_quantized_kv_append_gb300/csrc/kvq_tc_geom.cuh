@@ -60,6 +60,9 @@ __host__ __device__ constexpr int slot_byte(int s) { return (s >> 1) * 4 + (s & 
 // Byte offset of slot s inside an mma A quad {a0, a1, a2, a3}: slots 0, 1 in
 // a0 (row g, k = 2r, 2r+1), slots 2, 3 in a2 (row g, k = 2r+8, 2r+9).
 __host__ __device__ constexpr int aslot_byte(int s) { return (s >> 1) * 8 + (s & 1) * 2; }
+// The same inside a pair {a0, a2} (a1 = a3 = 0 left out): slots 0, 1 in a0,
+// slots 2, 3 in a2.
+__host__ __device__ constexpr int aslot2_byte(int s) { return (s >> 1) * 4 + (s & 1) * 2; }
 
 // In-block rotation table in fragment order, appended to the RoPE table for
 // D = 128: uint4 {cos s0|s1, cos s2|s3, sin s0|s1, sin s2|s3} (fp16) of token

@@ -27,6 +27,9 @@ CASES = {
     "d64_int3_bk128_two_outliers": (W("lv3", 1, 4, 2, 64, 256, 3, 128, 32, 0.04, 1e4, 52), 256, [256]),
     "mha_int8_norope": (W("lv8", 1, 2, 2, 128, 128, 8, 64, 64, 0.0, 0.0, 53), 128, [64, 64]),
     "g8_int2_gv128": (W("lv2", 1, 16, 2, 128, 192, 2, 64, 128, 0.01, 5e5, 54), 192, [192]),
+    # 4-bit codes at head_dim 128 run on the tensor-core kernel (level lookups)
+    "int4_bk128_mha_tc": (W("lv4b", 2, 4, 4, 128, 1024, 4, 128, 64, 0.0, 1e4, 56), 1024, [512, 512]),
+    "int4_g8_gv32_long_tc": (W("lv4g", 2, 16, 2, 128, 4096, 4, 64, 32, 0.01, 5e5, 57), 4096, [4096]),
 }
 
 
@@ -46,11 +49,17 @@ def _levels(w):
     return oc.fit_levels(u.ravel(), w.bits, 60)
 
 
+@pytest.mark.parametrize("precise", [False, True], ids=["default", "precise"])
 @pytest.mark.parametrize("name", list(CASES))
-def test_levels_parity(name):
+def test_levels_parity(name, precise):
+    """precise: KVQ_FLAG_PRECISE_SCORES, which keeps 4-bit head_dim-128 level
+    tables on the fp32 CUDA-core kernel (the default runs them on the
+    tensor-core kernel)."""
     w, T, pieces = CASES[name]
     lv = _levels(w)
-    cache = tl.make_cache(w, T + w.key_block)
+    cache = kvq.QuantizedKVCache(w.B, w.H_kv, w.D, T + w.key_block, w.bits, w.key_block, w.value_group,
+                                 w.outlier_frac, H_q=w.H_q, rope_theta=w.rope_theta, device="cuda",
+                                 precise=precise)
     K, V = ki.kv_torch(w, 0, 0, T, "cuda")
     t = 0
     for n in pieces:
