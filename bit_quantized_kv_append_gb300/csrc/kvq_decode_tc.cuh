@@ -21,8 +21,12 @@
 //    one LOP3 each (magic-number trick), dequantizes with one HFMA2 (s, z
 //    halved so the rotation cannot overflow fp16) and rotates with the
 //    in-block table R(j), j < 64, read through L1 in fragment order.
-//  * softmax: base 2, running (m, l) per warp and head. Key outliers add
-//    (x_out - x_dense) * <q, R(j) e_c> to their token's score.
+//  * softmax: base 2, running (m, l) per warp and head.
+//  * outliers, once per block in the preparation (one token per thread): a
+//    key outlier's score term (x_out - x_dense) * <q, R(t) e_c> for every
+//    head, in fp32, which the warps add to their scores; a value outlier's
+//    x_out - x_dense, written back into its list entry in the ring, which the
+//    warps scale by p and add into the shared sums with shared atomics.
 //  * P . V, transposed (rows = channels, columns = heads): A = value codes as
 //    exact fp16 subnormals (q * 2^-24, power-of-two rescale at the flush),
 //    B = p*s split into fp16 hi + lo; zero points as sum_t p*z per group.
@@ -140,15 +144,6 @@ __device__ __forceinline__ float ex2(float x) {   // 2^x, hardware approximation
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-// sin and cos of x in [0, 2^8): two-constant Cody-Waite reduction by 2 pi (the
-// high constant has 8 significant bits, so n * hi is exact for n < 2^16), then
-// the hardware approximations on [-pi, pi].
-__device__ __forceinline__ void sincos_small(float x, float& s, float& c) {
-  const float n = rintf(x * 0.15915494309189535f);
-  float r = fmaf(-n, 6.28125f, x);
-  r = fmaf(-n, 1.9353071795864769e-3f, r);
-  __sincosf(r, &s, &c);
 }
 // Small non-negative integer as float without a conversion instruction.
 __device__ __forceinline__ float small_int_f(uint32_t q) {
@@ -477,10 +472,12 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
   __shared__ __align__(16) uint2 s_ql[PREC ? 2 : 1][PREC ? SL : 1][PREC ? 8 : 1][PREC ? 32 : 1];
   __shared__ __align__(16) uint4 s_kz[2][4][4][2];            // key {s01, s23, z01, z23} / 2 [k-step][quarter][half]
   __shared__ __align__(16) float4 s_acc[kWarps][8][8][RQ];    // P.V sums in the frame m_frame, fragment order
-  __shared__ __align__(16) float4 s_tok[kWarps][16];          // key-outlier staging of one warp
-  __shared__ float s_p[kWarps][G][16];                        // p * 2^(m - m_frame) for value outliers
-  __shared__ float s_vd[kWarps][16];                          // value-outlier x_out - x_dense of the warp's tokens
-  __shared__ float s_w[OUTL ? HALF : 1];                      // RoPE frequency of every channel pair
+  __shared__ float s_p[OUTL ? kWarps : 1][G][16];            // p * 2^(m - m_frame) for value outliers
+  // key outliers: (x_out - x_dense) <q, R(t) e_c> / 2 of every token and head,
+  // [block parity][head][token], summed over the token's outliers (fp16 like
+  // the scores' operands; binary32 for precise scores)
+  using KcT = typename std::conditional<PREC, float, __half>::type;
+  __shared__ __align__(16) KcT s_kc[OUTL ? 2 : 1][OUTL ? G : 1][OUTL ? BK : 2];
   __shared__ float s_wm[kWarps][G], s_wl[kWarps][G], s_wf[kWarps][G];
   __shared__ float s_z[kWarps][G][4];                         // zero-point sums per 32-channel block
   __shared__ uint32_t s_lut[LV ? 256 : 1];                    // LV: {l[b & 15], l[b >> 4]} fp16 per code byte b
@@ -589,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
   // scale/zero (halved, fragment order).
   auto prep = [&](int u, int stage, float2 rr) {
     const int buf = (u - u0) & 1;
-    const uint8_t* st = ring + stage * L.stage_bytes;
+    uint8_t* st = ring + stage * L.stage_bytes;
     if (q_thread) {
 #pragma unroll
       for (int sl = 0; sl < SL; ++sl) {
@@ -618,12 +615,72 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
         }
       }
     }
-    if (u != n_full_b()) {
+    const bool tail = (u == n_full_b());
+    if (!tail) {
       const uint32_t m = reinterpret_cast<const uint32_t*>(st + L.km)[tid];
       const uint32_t mh = as_u32(__hmul2(as_h2(m), __float2half2_rn(0.5f)));
       uint8_t* kz = reinterpret_cast<uint8_t*>(&s_kz[buf][0][0][0]) + kz_off;
       *reinterpret_cast<uint16_t*>(kz) = (uint16_t)(mh & 0xFFFFu);
       *reinterpret_cast<uint16_t*>(kz + 8) = (uint16_t)(mh >> 16);
+    }
+    // Outliers of the block, one token per thread (keys, then values): a key
+    // outlier's score term (x_out - x_dense) <q, R(t) e_c> for every head, in
+    // fp32 from the unrotated queries and R(t) = R(BK u) R(j) of its channel
+    // pair; a value outlier's x_out - x_dense goes back into its list entry in
+    // the ring (binary32 with the channel in the 7 low mantissa bits).
+    if constexpr (OUTL) {
+      const int ntok_u = tail ? tail_len_b() : BK;
+      for (int e2 = tid; e2 < 2 * BK; e2 += kThreads) {
+        const bool val = e2 >= BK;
+        const int tok = val ? e2 - BK : e2;
+        if (!val) {
+          if (tail) continue;
+          const uint32_t* ko = reinterpret_cast<const uint32_t*>(st + L.ko);
+          const uint32_t* km = reinterpret_cast<const uint32_t*>(st + L.km);
+          const uint8_t* kc = st + L.kc;
+          float corr[G];
+#pragma unroll
+          for (int h = 0; h < G; ++h) corr[h] = 0.0f;
+          for (int oi = 0; oi < n_out; ++oi) {
+            const uint32_t e = ko[tok * n_out + oi];
+            const int c = (int)(e & (kD - 1)), i = c & (HALF - 1);
+            const uint32_t m = km[c];
+            const uint32_t qc = tile_code<BITS>(kc, tok, c);
+            const float xd = fmaf(LV ? s_lvf[LV ? qc : 0] : small_int_f(qc), h2f((uint16_t)(m & 0xFFFFu)),
+                                  h2f((uint16_t)(m >> 16)));
+            const float dl = 0.5f * (h2f((uint16_t)(e >> 16)) - xd);   // the scores carry q doubled
+            float2 R = make_float2(1.0f, 0.0f);
+            if (a.rope) {
+              const uint32_t ub = (uint32_t)u;
+              const float2 lo = __ldg(a.rope + (kLoOff + ((ub & (kRopeLo - 1)) << 6) + i));
+              const float2 hi = __ldg(a.rope + (kHiOff + ((ub / kRopeLo) << 6) + i));
+              R = rot_compose(rot_compose(hi, lo), __ldg(a.rope + (size_t)i * BK + tok));
+            }
+            // R(t) e_c: (cos, sin) on (i, i + D/2) for a first-half channel, (-sin, cos) for its partner
+            const bool first = c < HALF;
+            const float wy = first ? R.x : -R.y, wz = first ? R.y : R.x;
+#pragma unroll
+            for (int h = 0; h < G; ++h) corr[h] = fmaf(dl, fmaf(s_qp[h][i], wy, s_qp[h][i + HALF] * wz), corr[h]);
+          }
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            if constexpr (PREC) s_kc[OUTL ? buf : 0][OUTL ? h : 0][OUTL ? tok : 0] = corr[h];
+            else s_kc[OUTL ? buf : 0][OUTL ? h : 0][OUTL ? tok : 0] = __float2half_rn(corr[h]);
+          }
+        } else if (tok < ntok_u) {
+          uint32_t* vo = reinterpret_cast<uint32_t*>(st + L.vo);
+          const uint32_t* vm = reinterpret_cast<const uint32_t*>(st + L.vm);
+          const uint8_t* vc = st + L.vc;
+          for (int oi = 0; oi < n_out; ++oi) {
+            const uint32_t e = vo[tok * n_out + oi];
+            const int c = (int)(e & (kD - 1));
+            const float2 sz = __half22float2(as_h2(vm[(tok << ng_sh) + (c >> gv_sh)]));
+            const uint32_t qc = tile_code<BITS>(vc, tok, c);
+            const float dv = h2f((uint16_t)(e >> 16)) - fmaf(LV ? s_lvf[LV ? qc : 0] : small_int_f(qc), sz.x, sz.y);
+            vo[tok * n_out + oi] = (__float_as_uint(dv) & ~(uint32_t)(kD - 1)) | (uint32_t)c;
+          }
+        }
+      }
     }
   };
 
@@ -656,14 +713,6 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
     }
     s_qp[gg][i] = x * (2.0f * a.scale_log2);        // doubled: the keys are halved
     s_qp[gg][i + HALF] = y * (2.0f * a.scale_log2);
-  }
-  if (OUTL && tid < HALF) {
-    float wi = 0.0f;                                 // RoPE off: R(j) = identity
-    if (a.rope) {
-      const float2 r1 = rope_fine(a.rope, d, 1, tid);   // (cos w, sin w), 0 < w <= 1
-      wi = atan2f(r1.y, r1.x);
-    }
-    s_w[tid] = wi;
   }
   {
     uint32_t* z = reinterpret_cast<uint32_t*>(&s_qa[0][0][0][0]);
@@ -731,8 +780,6 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
     const uint8_t* st = ring + stage * L.stage_bytes;
     const uint8_t* kc = st + L.kc;
     const uint8_t* vc = st + L.vc;
-    const uint32_t* km = reinterpret_cast<const uint32_t*>(st + L.km);
-    const uint32_t* ko = reinterpret_cast<const uint32_t*>(st + L.ko);
     const uint32_t* vm = reinterpret_cast<const uint32_t*>(st + L.vm);
     const uint32_t* vo = reinterpret_cast<const uint32_t*>(st + L.vo);
 
@@ -877,46 +924,16 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
           sc[nt][1] += acc[nt][KVQ_TC_QK_CHAINS - 1][1];
         }
       }
-      // dense-and-sparse keys: (x_out - x_dense) * <q, R(j) e_c> per outlier
-      if (n_out > 0 && !is_tail) {
-        for (int oi = 0; oi < n_out; ++oi) {
-          if (lane < 16) {
-            const int nt_ = lane >> 3, n_ = lane & 7;
-            const int row = 64 * sl + 16 * w + 8 * nt_ + tperm(n_);
-            const uint32_t e = ko[row * n_out + oi];
-            const int c = (int)(e & (kD - 1));
-            const uint32_t m = km[c];
-            const uint32_t qc = tile_code<BITS>(kc, row, c);
-            const float xd = fmaf(LV ? s_lvf[LV ? qc : 0] : small_int_f(qc), h2f((uint16_t)(m & 0xFFFFu)),
-                                  h2f((uint16_t)(m >> 16)));
-            int rr, kq, s;
-            kslot<BITS>(c & (HALF - 1), rr, kq, s);
-            float sn, cs;                                // R(j) of the token's pair, j < 64 in the slice
-            sincos_small((float)(row & 63) * s_w[c & (HALF - 1)], sn, cs);
-            const bool first = c < HALF;
-            s_tok[w][lane] = make_float4(0.5f * (h2f((uint16_t)(e >> 16)) - xd), first ? cs : -sn, first ? sn : cs,
-                                         __int_as_float((kq * 32 + rr) * 8 + aslot2_byte(s)));
-          }
-          __syncwarp();
-          if (g < G) {
-            const uint8_t* qa = reinterpret_cast<const uint8_t*>(&s_qa[buf][sl][0][0]) + 32 * g;
-            const uint8_t* ql = reinterpret_cast<const uint8_t*>(&s_ql[PREC ? buf : 0][PREC ? sl : 0][0][0]) + 32 * g;
+      // dense-and-sparse keys: the outliers' score terms of this block
+      if (OUTL && n_out > 0 && !is_tail && g < G) {
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const float4 T = s_tok[w][8 * nt + 2 * r + e];
-                const int qa_off = __float_as_int(T.w);
-                float q0 = ld_h(qa + qa_off), q1 = ld_h(qa + qa_off + 1024);
-                if constexpr (PREC) {
-                  q0 += ld_h(ql + qa_off);
-                  q1 += ld_h(ql + qa_off + 1024);
-                }
-                const float wgt = fmaf(q0, T.y, q1 * T.z);
-                sc[nt][e] = fmaf(T.x, wgt, sc[nt][e]);
-              }
-          }
-          __syncwarp();
+        for (int nt = 0; nt < 2; ++nt) {
+          const KcT* kcp = &s_kc[OUTL ? buf : 0][OUTL ? g : 0][OUTL ? 64 * sl + 16 * w + 8 * nt + tperm(2 * r) : 0];
+          float2 t2;
+          if constexpr (PREC) t2 = *reinterpret_cast<const float2*>(kcp);
+          else t2 = __half22float2(*reinterpret_cast<const __half2*>(kcp));
+          sc[nt][0] += t2.x;
+          sc[nt][1] += t2.y;
         }
       }
       if (is_tail) {
@@ -983,48 +1000,31 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
       }
     }
 
-    // ---- value outliers: p * (x_out - x_dense) into the shared sums
-    if (n_out > 0) {
-      {
-        if (g < G) {
+    // ---- value outliers: p * (x_out - x_dense) into the shared sums (the
+    // prep left x_out - x_dense in the list entries); tokens of the slice that
+    // share a channel meet in the shared-memory atomics
+    if (OUTL && n_out > 0) {
+      if (g < G) {
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            s_p[w][g][8 * nt + 2 * r] = sc[nt][0] * fac;
-            s_p[w][g][8 * nt + 2 * r + 1] = sc[nt][1] * fac;
-          }
-        }
-        __syncwarp();
-        // token lanes 0..15; lanes whose outliers share a channel are summed by
-        // the lowest of them, so the shared sums take plain read-add-writes
-        const int row = 64 * sl + 16 * w + 8 * ((lane >> 3) & 1) + tperm(lane & 7);
-        float* accs = reinterpret_cast<float*>(&s_acc[0][0][0][0]);
-        for (int oi = 0; oi < n_out; ++oi) {
-          int c = -1 - lane;                             // never a channel: lanes 16..31, rows past the tail
-          if (lane < 16 && row < ntok) {
-            const uint32_t e = vo[row * n_out + oi];
-            c = (int)(e & (kD - 1));
-            const float2 sz = __half22float2(as_h2(vm[(row << ng_sh) + (c >> gv_sh)]));
-            const uint32_t qc = tile_code<BITS>(vc, row, c);
-            s_vd[w][lane] = h2f((uint16_t)(e >> 16)) - fmaf(LV ? s_lvf[LV ? qc : 0] : small_int_f(qc), sz.x, sz.y);
-          }
-          const uint32_t peers = __match_any_sync(0xffffffffu, c);
-          __syncwarp();
-          if (c >= 0 && (peers & ((1u << lane) - 1u)) == 0u) {
-            float sum[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) sum[h] = 0.0f;
-            for (uint32_t m = peers; m; m &= m - 1u) {
-              const int j = __ffs(m) - 1;
-              const float dj = s_vd[w][j];
-#pragma unroll
-              for (int h = 0; h < G; ++h) sum[h] = fmaf(s_p[w][h][j], dj, sum[h]);
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h) accs[acc_index<RQ>(w, c, h)] += sum[h];
-          }
-          __syncwarp();
+        for (int nt = 0; nt < 2; ++nt) {
+          s_p[OUTL ? w : 0][g][8 * nt + 2 * r] = sc[nt][0] * fac;
+          s_p[OUTL ? w : 0][g][8 * nt + 2 * r + 1] = sc[nt][1] * fac;
         }
       }
+      __syncwarp();
+      const int row = 64 * sl + 16 * w + 8 * ((lane >> 3) & 1) + tperm(lane & 7);
+      if (lane < 16 && row < ntok) {
+        float* accs = reinterpret_cast<float*>(&s_acc[0][0][0][0]);
+        for (int oi = 0; oi < n_out; ++oi) {
+          const uint32_t e = vo[row * n_out + oi];
+          const int c = (int)(e & (kD - 1));
+          const float dv = __uint_as_float(e & ~(uint32_t)(kD - 1));
+          const int base = acc_index<RQ>(w, c, 0);
+#pragma unroll
+          for (int h = 0; h < G; ++h) atomicAdd(accs + base + ((h >> 1) << 2) + (h & 1), s_p[OUTL ? w : 0][h][lane] * dv);
+        }
+      }
+      __syncwarp();
     }
 
     // ---- P . V: A = value codes (16 channels x 16 tokens), B = p * s (fp16 hi + lo)
@@ -1099,6 +1099,9 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
       return;
     }
     if (tid == 0 && u + NST < u1) {
+      // the stage took generic stores (value-outlier entries): order them
+      // before the copy engine refills it
+      if constexpr (OUTL) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       if constexpr (PAGED) {
         issue(u + NST, s_next_blk, stage);
         if (u + NST + 1 < u1) s_next_blk = unit_blk(u + NST + 1);
