@@ -14,22 +14,36 @@ template <int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restrict__ ws,
                                                            __half* __restrict__ out, int n_split,
                                                            int S) {
+  __shared__ float s_w[kMaxSplits];
+  __shared__ float s_red[D / 32];
   const int bhq = blockIdx.x;
   const float* p = ws + (size_t)bhq * S * (D + 2);
   const int c = threadIdx.x;
+  // the largest split maximum, the splits read in parallel
   float M = -INFINITY;
-  for (int s = 0; s < n_split; ++s) M = fmaxf(M, p[(size_t)s * (D + 2) + D]);
+  for (int s = c; s < n_split; s += D) M = fmaxf(M, p[(size_t)s * (D + 2) + D]);
+  M = warp_max(M);
+  if ((c & 31) == 0) s_red[c >> 5] = M;
+  __syncthreads();
+  M = s_red[0];
+#pragma unroll
+  for (int k = 1; k < D / 32; ++k) M = fmaxf(M, s_red[k]);
+  // split weights 2^(m_s - M): 0 for a split without tokens; the NaN partials
+  // of a split whose waits expired give NaN, which stays NaN below
+  for (int s = c; s < n_split; s += D) {
+    const float m = p[(size_t)s * (D + 2) + D];
+    s_w[s] = (m == -INFINITY) ? 0.0f : exp2f(m - M);
+  }
+  __syncthreads();
   float L = 0.0f, acc = 0.0f;
+#pragma unroll 8
   for (int s = 0; s < n_split; ++s) {
+    const float w = s_w[s];
     const float* ps = p + (size_t)s * (D + 2);
-    const float m = ps[D];
-    if (m == -INFINITY) continue;          // split without tokens
-    const float w = exp2f(m - M);
     L = fmaf(w, ps[D + 1], L);
     acc = fmaf(w, ps[c], acc);
   }
-  // a sequence without tokens: 0; partials of a split whose waits expired are
-  // NaN and stay NaN here
+  // a sequence without tokens: 0
   out[(size_t)bhq * D + c] = __float2half_rn(L == 0.0f ? 0.0f : acc / L);
 }
 
