@@ -626,7 +626,9 @@ def run_levels(args, w, rank, world, device):
     """Non-uniform codes: a level table fitted (kvq_fit_levels) to the
     normalized values of another layer's groups; the cache is filled with
     kvq_append_levels (whole key blocks) and each step times one
-    kvq_decode_attn_levels call over T tokens (the CUDA-core kernels)."""
+    kvq_decode_attn_levels call over T tokens (the tensor-core kernel in its
+    level-table mode for 4-bit codes at head_dim 128, the CUDA-core kernel
+    otherwise)."""
     import numpy as np
     import torch
     import torch.distributed as dist
@@ -687,7 +689,9 @@ def run_levels(args, w, rank, world, device):
         },
         "gpu_launches": 2 * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": peak_kind, "kernel": "decode_levels_kernel + combine (CUDA cores)",
+                     "peak_source": peak_kind,
+                     "kernel": ("decode_tc_kernel, level-table mode (+ decode_combine_kernel)" if w.D == 128 and w.bits == 4
+                                else "decode_levels_kernel + combine (CUDA cores)"),
                      "alg_bytes_per_launch": alg, "traffic": None},
         "clocks": clk,
     }

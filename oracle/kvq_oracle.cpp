@@ -15,8 +15,8 @@
 //                                         and the rest is quantized (dense).
 //   Same page, Quanto section, steps 1-2: block-wise quantization where each
 //     block keeps a scale and a zero_point used to restore the values.
-//   Readings where the page is silent or its formula image was lost (each one
-//   is listed in the design notes): unsigned codes q in [0, L], L = 2^b - 1;
+//   Readings taken where the page is silent or its formula image was lost:
+//   unsigned codes q in [0, L], L = 2^b - 1;
 //   zero z = the block minimum (fp16, exact); scale s = (max - min) / L in fp32,
 //   stored in fp16 rounded toward +infinity; q = clamp(rint((x - z) / s), 0, L)
 //   with fp32 round-to-nearest arithmetic and round-half-to-even; x_hat =
