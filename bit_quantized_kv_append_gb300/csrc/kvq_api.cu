@@ -493,13 +493,12 @@ int kvq_append_levels(const kvq_config* cfg, kvq_cache* cache, const void* k_new
   if (!make_levels(levels, d.bits, &t)) return KVQ_ERR_ARG;
   if (n_new == 0) return KVQ_OK;
   if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_ARG;
-  if (cache->T_cur % d.Bk || n_new % d.Bk) return KVQ_ERR_UNSUPPORTED;   // whole key blocks only
   if ((int64_t)cache->T_cur + n_new > d.T_max) return KVQ_ERR_CAPACITY;
   rc = device_ok();
   if (rc) return rc;
-  rc = cuda_status(launch_append_levels(d, *cache, static_cast<const __half*>(k_new),
-                                        static_cast<const __half*>(v_new), n_new, t,
-                                        static_cast<cudaStream_t>(stream)));
+  // the uniform append's kernel in its level-table mode (fp16 tail of an unfinished key block included)
+  rc = cuda_status(launch_append(d, *cache, static_cast<const __half*>(k_new), static_cast<const __half*>(v_new),
+                                 n_new, static_cast<cudaStream_t>(stream), nullptr, 0, nullptr, t.mid));
   if (rc == KVQ_OK) cache->T_cur += n_new;
   return rc;
 }
@@ -515,7 +514,6 @@ int kvq_decode_attn_levels(const kvq_config* cfg, const kvq_cache* cache, const 
   if (rc) return rc;
   LevelTable t;
   if (!make_levels(levels, d.bits, &t)) return KVQ_ERR_ARG;
-  if (cache->T_cur % d.Bk) return KVQ_ERR_UNSUPPORTED;                     // whole key blocks only
   rc = device_ok();
   if (rc) return rc;
   if (d.D == 128 && d.bits == 4 && !(d.flags & KVQ_FLAG_PRECISE_SCORES))   // the tensor-core kernel
@@ -527,6 +525,37 @@ int kvq_decode_attn_levels(const kvq_config* cfg, const kvq_cache* cache, const 
                                           static_cast<const float2*>(rope_tab), sm_scale,
                                           static_cast<__half*>(out), static_cast<float*>(workspace), t,
                                           static_cast<cudaStream_t>(stream)));
+}
+
+int kvq_decode_step_levels(const kvq_config* cfg, kvq_cache* cache, const void* k_new, const void* v_new,
+                           const void* q, int32_t H_q, const void* rope_tab, float sm_scale, void* out,
+                           void* workspace, size_t workspace_bytes, const float* levels, void* stream) {
+  Dims d;
+  int rc = make_dims(cfg, &d);
+  if (rc) return rc;
+  if (!cache || !cache_ptrs_ok(d, *cache)) return KVQ_ERR_ARG;
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_ARG;
+  LevelTable t;
+  if (!make_levels(levels, d.bits, &t)) return KVQ_ERR_ARG;
+  if (cache->T_cur + 1 > d.T_max) return KVQ_ERR_CAPACITY;
+  const int32_t pos = cache->T_cur;                  // the new token's position
+  rc = decode_checks(cfg, d, cache, pos + 1, q, H_q, pos, rope_tab, sm_scale, out, workspace,
+                     workspace_bytes);
+  if (rc) return rc;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  rc = device_ok();
+  if (rc) return rc;
+  rc = cuda_status(launch_append(d, *cache, static_cast<const __half*>(k_new), static_cast<const __half*>(v_new),
+                                 1, st, nullptr, 0, nullptr, t.mid));
+  if (rc) return rc;
+  cache->T_cur = pos + 1;
+  if (d.D == 128 && d.bits == 4 && !(d.flags & KVQ_FLAG_PRECISE_SCORES))   // the tensor-core kernel
+    return cuda_status(launch_decode(d, *cache, static_cast<const __half*>(q), H_q, pos,
+                                     static_cast<const float2*>(rope_tab), sm_scale, static_cast<__half*>(out),
+                                     static_cast<float*>(workspace), st, 0, nullptr, 0, t.lv));
+  return cuda_status(launch_decode_levels(d, *cache, static_cast<const __half*>(q), H_q, pos,
+                                          static_cast<const float2*>(rope_tab), sm_scale,
+                                          static_cast<__half*>(out), static_cast<float*>(workspace), t, st));
 }
 
 const char* kvq_status_string(int status) {

@@ -25,7 +25,14 @@
 //      Outlier positions are recomputed from their stored value.
 // All rounding follows the library's stated arithmetic: binary32 RN subtract
 // and divide, fp16 round-up for the scale, round-half-even codes.
+//
+// Level tables (KVQuant "Non-Uniform KV Cache Quantization", same page; LV):
+// the same kernel with r = fp16_round_up(fp32(max) - fp32(min)) in the scale's
+// slot and the code of x the nearest level of u = fp32(fp32(x - z) / r): the
+// number of binary32 midpoints of neighbouring levels below u (ties to the
+// lower level), found by a binary search over the midpoints in shared memory.
 #include <atomic>
+#include <type_traits>
 
 #include "kvq_common.cuh"
 
@@ -146,6 +153,42 @@ __device__ __forceinline__ uint32_t group_params(float mn, float mx, bool any, f
   return (uint32_t)hbits(sh) | ((uint32_t)hbits(zh) << 16);
 }
 
+// Level tables: range and zero of a group, {r (low half), z (high half)} as
+// fp16 bits; sz = (r, z) in binary32. No dense element: r = z = 0.
+__device__ __forceinline__ uint32_t range_zero(float mn, float mx, bool any, float2* sz) {
+  if (!any) {
+    *sz = make_float2(0.0f, 0.0f);
+    return 0u;
+  }
+  const __half rh = __float2half_ru(__fsub_rn(mx, mn));
+  const float z = (mn == 0.0f) ? 0.0f : mn;     // -0 stored as +0; mn is an fp16 value: exact
+  *sz = make_float2(__half2float(rh), z);
+  return (uint32_t)hbits(rh) | ((uint32_t)hbits(__float2half_rn(z)) << 16);
+}
+// The midpoints of a table of 2^BITS levels, in the launch's parameters.
+struct LvMid {
+  float mid[255];
+};
+struct NoLv {
+  int unused;
+};
+template <bool LV>
+using LvParam = typename std::conditional<LV, LvMid, NoLv>::type;
+// Number of midpoints below u (mid[0..2^BITS - 2], increasing); NaN: 0.
+template <int BITS>
+__device__ __forceinline__ uint32_t level_index(float u, const float* mid) {
+  uint32_t q = 0u;
+#pragma unroll
+  for (int st = 1 << (BITS - 1); st > 0; st >>= 1)
+    if (u > mid[q + st - 1]) q += st;
+  return q;
+}
+// Level code of x with d = fp32(x - z) already formed; 0 when r = 0.
+template <int BITS>
+__device__ __forceinline__ uint32_t level_code_d(float d, float r, const float* mid) {
+  return r > 0.0f ? level_index<BITS>(__fdiv_rn(d, r), mid) : 0u;
+}
+
 // Code-carrying bit patterns (float bits of y + kMagic: the code in bits 0-3,
 // zeros up to bit 21) -> packed LSB-first words.
 template <int BITS>
@@ -207,10 +250,11 @@ __device__ __forceinline__ int sw_off(int r, int D, int col) {
 // Step D for one 32-channel chunk of row r: codes from the packed fp32 path,
 // the exact rule for the elements near a rounding tie, and the outlier
 // positions' codes (computed in step C'); returns the packed words.
-template <int BITS, bool KEYS>
+template <int BITS, bool KEYS, bool LV>
 __device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv, const float4* sPk,
                                            const float* sS, const uint32_t* sO, const uint8_t* sQ, int D,
-                                           int Bk, int r, int ch, int grp, int n_out, uint32_t (&w)[BITS]) {
+                                           int Bk, int r, int ch, int grp, int n_out, const float* mid,
+                                           uint32_t (&w)[BITS]) {
   const float2 magic2 = make_float2(kMagic, kMagic), nmagic2 = make_float2(-kMagic, -kMagic);
   const float2 neg1 = make_float2(-1.0f, -1.0f);
   float4 vp = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -235,6 +279,13 @@ __device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv,
         r2 = make_float2(vp.y, vp.y);
       }
       const float2 d2 = make_float2(add_h_f((uint16_t)(hw[j] & 0xFFFFu), nz2.x), add_h_f((uint16_t)(hw[j] >> 16), nz2.y));
+      if constexpr (LV) {
+        // r2 holds the ranges: the exact quotient, then the midpoint search
+        // (NaN, an outlier position, gives 0 and is patched below)
+        mb[e] = level_code_d<BITS>(d2.x, r2.x, mid);
+        mb[e + 1] = level_code_d<BITS>(d2.y, r2.y, mid);
+        continue;
+      }
       const float2 y2 = __fmul2_rn(d2, r2);
       const float2 m2 = __fadd2_rn(y2, magic2);
       const float2 t2 = __ffma2_rn(__fadd2_rn(m2, nmagic2), neg1, y2);   // y - rint(y)
@@ -270,9 +321,13 @@ __device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv,
   }
 }
 
-template <int BITS, int D>
-__global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
+template <int BITS, int D, bool LV>
+__global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a, const LvParam<LV> lp) {
   extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ float s_mid[LV ? 256 : 1];   // LV: the table's midpoints
+  if constexpr (LV) {
+    for (int k = threadIdx.x; k < (1 << BITS) - 1; k += kThreads) s_mid[k] = lp.mid[k];
+  }
   const Dims d = a.d;
   const int Bk = d.Bk, n_out = d.n_out;
   const int tid = threadIdx.x;
@@ -480,9 +535,10 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
       const float mn = fminf(__low2float(mn2), __high2float(mn2));
       const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
       float2 sz;
-      const uint32_t packed = group_params(mn, mx, !isnan(mn), Lf, &sz);
+      const uint32_t packed = LV ? range_zero(mn, mx, !isnan(mn), &sz) : group_params(mn, mx, !isnan(mn), Lf, &sz);
       a.v_meta[(size_t)(row_base + t_row0 + r) * ng + g] = packed;
-      sPv[g * Bk + r] = make_float4(-sz.y, rcp_or_zero(sz.x), sz.x, 0.0f);
+      // {-z, 1/s (LV: r, the divisor), s (LV: r)}
+      sPv[g * Bk + r] = make_float4(-sz.y, LV ? sz.x : rcp_or_zero(sz.x), sz.x, 0.0f);
     }
   } else if (a.phase == 2) {
     // window keys: min and max of the dense elements of the last
@@ -537,11 +593,11 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
         a.k_bstat[kblk * D + c] = (uint32_t)lo | ((uint32_t)hi << 16);
       } else {
         float2 sz;
-        const uint32_t packed = group_params(mn, mx, !isnan(mn), Lf, &sz);
+        const uint32_t packed = LV ? range_zero(mn, mx, !isnan(mn), &sz) : group_params(mn, mx, !isnan(mn), Lf, &sz);
         a.k_meta[kblk * D + c] = packed;
         float* pk = reinterpret_cast<float*>(&sPk[cp]);
         pk[hc] = -sz.y;
-        pk[2 + hc] = rcp_or_zero(sz.x);
+        pk[2 + hc] = LV ? sz.x : rcp_or_zero(sz.x);
         sS[c] = sz.x;
       }
     }
@@ -568,7 +624,9 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
         rc = vp.y;
         sc = vp.z;
       }
-      sQ[o * Bk + r] = (uint8_t)exact_code<BITS>(__half2float(__ushort_as_half((uint16_t)(ev >> 16))), z, sc, rc);
+      const float xo = __half2float(__ushort_as_half((uint16_t)(ev >> 16)));
+      if constexpr (LV) sQ[o * Bk + r] = (uint8_t)level_code_d<BITS>(__fsub_rn(xo, z), sc, s_mid);
+      else sQ[o * Bk + r] = (uint8_t)exact_code<BITS>(xo, z, sc, rc);
     }
     __syncthreads();
   }
@@ -584,9 +642,9 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
       if (r >= rows) continue;
       uint32_t w[BITS];
       if (isK)
-        chunk_codes<BITS, true>(sX, sPv, sPk, sS, sO, sQ, D, Bk, r, ch, 0, n_out, w);
+        chunk_codes<BITS, true, LV>(sX, sPv, sPk, sS, sO, sQ, D, Bk, r, ch, 0, n_out, s_mid, w);
       else
-        chunk_codes<BITS, false>(sX, sPv, sPk, sS, sO, sQ, D, Bk, r, ch, (ch * 32) >> gv_sh, n_out, w);
+        chunk_codes<BITS, false, LV>(sX, sPv, sPk, sS, sO, sQ, D, Bk, r, ch, (ch * 32) >> gv_sh, n_out, s_mid, w);
       uint32_t* dst = reinterpret_cast<uint32_t*>(base + (size_t)(row_base + t_row0 + r) * d.cb) + ch * BITS;
       if constexpr (BITS == 8) {
         reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -631,24 +689,31 @@ size_t append_smem(const Dims& d) {
          (size_t)16 * (d.D / 2) * sizeof(__half2);
 }
 
-template <int BITS, int D>
-cudaError_t launch_bd(const AppendArgs& a, dim3 grid, size_t smem, cudaStream_t st) {
+template <int BITS, int D, bool LV>
+cudaError_t launch_bd(const AppendArgs& a, const LvParam<LV>& lp, dim3 grid, size_t smem, cudaStream_t st) {
   // the shared-memory limit is a per-device function attribute: set it once on each device
   static std::atomic<bool> attr_set[kMaxDevices];
   int dev = 0;
   if (current_device(&dev) != KVQ_OK) return cudaErrorInvalidDevice;   // the API checked it first
   if (!attr_set[dev].load(std::memory_order_acquire)) {
     const cudaError_t e =
-        cudaFuncSetAttribute(append_kernel<BITS, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+        cudaFuncSetAttribute(append_kernel<BITS, D, LV>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
     if (e != cudaSuccess) return e;
     attr_set[dev].store(true, std::memory_order_release);
   }
-  append_kernel<BITS, D><<<grid, kThreads, smem, st>>>(a);
+  append_kernel<BITS, D, LV><<<grid, kThreads, smem, st>>>(a, lp);
   return cudaGetLastError();
 }
+// lv_mid: the 2^BITS - 1 midpoints of a level table (host memory), or NULL
 template <int BITS>
-cudaError_t launch_bits(const AppendArgs& a, dim3 grid, size_t smem, cudaStream_t st) {
-  return a.d.D == 64 ? launch_bd<BITS, 64>(a, grid, smem, st) : launch_bd<BITS, 128>(a, grid, smem, st);
+cudaError_t launch_bits(const AppendArgs& a, dim3 grid, size_t smem, cudaStream_t st, const float* lv_mid) {
+  if (lv_mid) {
+    LvMid m;
+    for (int k = 0; k < 255; ++k) m.mid[k] = k < (1 << BITS) - 1 ? lv_mid[k] : 0.0f;
+    return a.d.D == 64 ? launch_bd<BITS, 64, true>(a, m, grid, smem, st) : launch_bd<BITS, 128, true>(a, m, grid, smem, st);
+  }
+  const NoLv n{0};
+  return a.d.D == 64 ? launch_bd<BITS, 64, false>(a, n, grid, smem, st) : launch_bd<BITS, 128, false>(a, n, grid, smem, st);
 }
 
 }  // namespace
@@ -663,7 +728,7 @@ __global__ void seq_len_advance_kernel(int32_t* seq_len, int B, int n_new, int T
 
 cudaError_t launch_append(const Dims& d, const kvq_cache& c, const __half* k_new,
                           const __half* v_new, int n_new, cudaStream_t st, const Paged* pg,
-                          int window_blocks, uint32_t* k_bstat) {
+                          int window_blocks, uint32_t* k_bstat, const float* lv_mid) {
   AppendArgs a;
   a.d = d;
   a.phase = window_blocks > 0 ? 1 : 0;
@@ -711,10 +776,10 @@ cudaError_t launch_append(const Dims& d, const kvq_cache& c, const __half* k_new
   const size_t smem = append_smem(d);
   cudaError_t e;
   switch (d.bits) {
-    case 2: e = launch_bits<2>(a, grid, smem, st); break;
-    case 3: e = launch_bits<3>(a, grid, smem, st); break;
-    case 8: e = launch_bits<8>(a, grid, smem, st); break;
-    default: e = launch_bits<4>(a, grid, smem, st); break;
+    case 2: e = launch_bits<2>(a, grid, smem, st, lv_mid); break;
+    case 3: e = launch_bits<3>(a, grid, smem, st, lv_mid); break;
+    case 8: e = launch_bits<8>(a, grid, smem, st, lv_mid); break;
+    default: e = launch_bits<4>(a, grid, smem, st, lv_mid); break;
   }
   if (e != cudaSuccess) return e;
   if (window_blocks > 0) {
@@ -722,10 +787,10 @@ cudaError_t launch_append(const Dims& d, const kvq_cache& c, const __half* k_new
     a.phase = 2;
     const dim3 grid2(blocks_x, d.B * d.H_kv, 1);
     switch (d.bits) {
-      case 2: e = launch_bits<2>(a, grid2, smem, st); break;
-      case 3: e = launch_bits<3>(a, grid2, smem, st); break;
-      case 8: e = launch_bits<8>(a, grid2, smem, st); break;
-      default: e = launch_bits<4>(a, grid2, smem, st); break;
+      case 2: e = launch_bits<2>(a, grid2, smem, st, nullptr); break;
+      case 3: e = launch_bits<3>(a, grid2, smem, st, nullptr); break;
+      case 8: e = launch_bits<8>(a, grid2, smem, st, nullptr); break;
+      default: e = launch_bits<4>(a, grid2, smem, st, nullptr); break;
     }
     if (e != cudaSuccess) return e;
   }

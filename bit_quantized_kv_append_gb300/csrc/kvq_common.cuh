@@ -107,10 +107,11 @@ cudaError_t launch_rope_init(const Dims& d, double theta, float2* tab, cudaStrea
 // pg: a paged cache (positions from pg->seq_len, advanced by n_new after the append).
 // window_blocks > 0: key statistics over the last window_blocks key blocks,
 // with every finished block's dense {min, max} per channel kept in k_bstat
-// (the size of K_META).
+// (the size of K_META). lv_mid: the 2^bits - 1 binary32 midpoints of a level
+// table (host memory; non-uniform codes), NULL for the uniform grid.
 cudaError_t launch_append(const Dims& d, const kvq_cache& c, const __half* k_new,
                           const __half* v_new, int n_new, cudaStream_t st, const Paged* pg = nullptr,
-                          int window_blocks = 0, uint32_t* k_bstat = nullptr);
+                          int window_blocks = 0, uint32_t* k_bstat = nullptr, const float* lv_mid = nullptr);
 // split_cap > 0 bounds the T splits (and the workspace stride) below max_splits().
 // pg: a paged cache (per-sequence lengths; q of sequence b at seq_len[b] - 1).
 // ws: the workspace, status word first (kWsHeaderBytes), partials after it.

@@ -13,8 +13,6 @@ struct LevelTable {
   int L;  // 2^bits - 1
 };
 
-cudaError_t launch_append_levels(const Dims& d, const kvq_cache& c, const __half* k_new, const __half* v_new,
-                                 int n_new, const LevelTable& t, cudaStream_t st);
 cudaError_t launch_decode_levels(const Dims& d, const kvq_cache& c, const __half* q, int H_q, int q_pos,
                                  const float2* rope, float sm_scale, __half* out, float* ws,
                                  const LevelTable& t, cudaStream_t st);

@@ -28,7 +28,7 @@ STATUS_TIMEOUT = 1          # bit of the device status word (first 4 bytes of a 
 WS_HEADER_BYTES = 256
 EXPORTS = ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_append_window", "kvq_decode_attn", "kvq_decode_step",
            "kvq_paged_layout", "kvq_paged_append", "kvq_paged_decode_attn",
-           "kvq_fit_levels", "kvq_append_levels", "kvq_decode_attn_levels",
+           "kvq_fit_levels", "kvq_append_levels", "kvq_decode_attn_levels", "kvq_decode_step_levels",
            "kvq_decode_attn_noalloc", "kvq_decode_attn_diag", "kvq_status_string", "kvq_version")
 
 
@@ -94,6 +94,8 @@ def lib():
         L.kvq_append_levels.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp, vp, i32, vp, vp]
         L.kvq_decode_attn_levels.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp, i32, i32, vp,
                                              ctypes.c_float, vp, vp, ctypes.c_size_t, vp, vp]
+        L.kvq_decode_step_levels.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp, vp, vp, i32,
+                                             vp, ctypes.c_float, vp, vp, ctypes.c_size_t, vp, vp]
         L.kvq_decode_attn_noalloc.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp,
                                               i32, i32, vp, ctypes.c_float, vp, vp]
         L.kvq_decode_attn_diag.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(CacheRef), vp, i32, i32, vp,
@@ -103,7 +105,7 @@ def lib():
         L.kvq_version.restype = ctypes.c_char_p
         for fn in ("kvq_layout", "kvq_rope_init", "kvq_append", "kvq_append_window", "kvq_decode_attn", "kvq_decode_step",
                    "kvq_paged_layout", "kvq_paged_append", "kvq_paged_decode_attn", "kvq_fit_levels",
-                   "kvq_append_levels", "kvq_decode_attn_levels", "kvq_decode_attn_noalloc",
+                   "kvq_append_levels", "kvq_decode_attn_levels", "kvq_decode_step_levels", "kvq_decode_attn_noalloc",
                    "kvq_decode_attn_diag"):
             getattr(L, fn).restype = ctypes.c_int
         _LIB = L
@@ -219,6 +221,17 @@ def decode_attn_levels(cfg: Config, ref: CacheRef, q: torch.Tensor, H_q: int, q_
                                         _ptr(rope), float(sm_scale), _ptr(out), _ptr(workspace),
                                         workspace.numel(), lv.ctypes.data_as(ctypes.c_void_p), _stream(stream)),
            "kvq_decode_attn_levels")
+
+
+def decode_step_levels(cfg: Config, ref: CacheRef, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor,
+                       H_q: int, rope: Optional[torch.Tensor], sm_scale: float, out: torch.Tensor,
+                       workspace: torch.Tensor, levels, stream=None):
+    """kvq_decode_step_levels: kvq_decode_step on a level-table cache."""
+    lv = _host_levels(levels, cfg.bits)
+    _check(lib().kvq_decode_step_levels(ctypes.byref(cfg), ctypes.byref(ref), _ptr(k_new), _ptr(v_new), _ptr(q),
+                                        int(H_q), _ptr(rope), float(sm_scale), _ptr(out), _ptr(workspace),
+                                        workspace.numel(), lv.ctypes.data_as(ctypes.c_void_p), _stream(stream)),
+           "kvq_decode_step_levels")
 
 
 def decode_attn_noalloc(cfg: Config, ref: CacheRef, q: torch.Tensor, H_q: int, q_pos: int,
@@ -342,7 +355,8 @@ class QuantizedKVCache:
 
     def append_levels(self, k_new: torch.Tensor, v_new: torch.Tensor, levels, stream=None):
         """Non-uniform codes against the level table ``levels`` (2^bits values,
-        0 first, 1 last, increasing); whole key blocks only."""
+        0 first, 1 last, increasing); any number of tokens (the keys of an
+        unfinished key block wait as fp16, as in append)."""
         c = self.cfg
         for t in (k_new, v_new):
             if t.dtype != torch.float16 or not t.is_contiguous() or t.device != self.device:
@@ -368,6 +382,29 @@ class QuantizedKVCache:
         sm_scale = 1.0 / math.sqrt(c.D) if sm_scale is None else sm_scale
         decode_attn_levels(self.cfg, self.ref(), q, self.H_q, q_pos, self.rope, sm_scale, out, self.workspace,
                            levels, stream)
+        return out
+
+    def decode_step_levels(self, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor, levels,
+                           sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                           stream=None) -> torch.Tensor:
+        """decode_step on a cache filled by append_levels, with the same table."""
+        c = self.cfg
+        for t in (k_new, v_new):
+            if t.dtype != torch.float16 or not t.is_contiguous() or t.device != self.device:
+                raise ValueError("k_new/v_new must be contiguous fp16 tensors on the cache device")
+            if tuple(t.shape) != (c.B, c.H_kv, 1, c.D):
+                raise ValueError(f"expected [B={c.B}, H_kv={c.H_kv}, 1, D={c.D}], got {tuple(t.shape)}")
+        if q.dtype != torch.float16 or not q.is_contiguous() or q.device != self.device:
+            raise ValueError("q must be a contiguous fp16 tensor on the cache device")
+        if tuple(q.shape) != (c.B, self.H_q, c.D):
+            raise ValueError(f"expected q [B={c.B}, H_q={self.H_q}, D={c.D}], got {tuple(q.shape)}")
+        if out is None:
+            out = torch.empty_like(q)
+        sm_scale = 1.0 / math.sqrt(c.D) if sm_scale is None else sm_scale
+        ref = self.ref()
+        decode_step_levels(self.cfg, ref, k_new, v_new, q, self.H_q, self.rope, sm_scale, out, self.workspace,
+                           levels, stream)
+        self.T_cur = ref.T_cur
         return out
 
     def decode_step(self, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor,

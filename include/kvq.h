@@ -387,24 +387,37 @@ KVQ_API int kvq_paged_decode_attn(const kvq_config* cfg, const kvq_paged_cache* 
 KVQ_API int kvq_fit_levels(const double* u, size_t n, int32_t bits, int32_t iters, float* levels);
 
 /* kvq_append with non-uniform codes (page 3, KVQuant "Non-Uniform KV Cache
- * Quantization"). levels: host pointer to the 2^bits
- * levels of the table (copied into the launch). T_cur and n_new must be
- * multiples of key_block. Errors: those of kvq_append; KVQ_ERR_ARG for a
- * table that does not start at 0, end at 1 and increase; KVQ_ERR_UNSUPPORTED
- * for a partial key block. */
+ * Quantization"). levels: host pointer to the 2^bits levels of the table
+ * (copied into the launch). Any T_cur and n_new, as kvq_append: the keys of an
+ * unfinished key block wait as fp16 in K_TAIL and are coded when the block
+ * completes; values are coded at once. Errors: those of kvq_append;
+ * KVQ_ERR_ARG for a table that does not start at 0, end at 1 and increase. */
 KVQ_API int kvq_append_levels(const kvq_config* cfg, kvq_cache* cache, const void* k_new, const void* v_new,
                               int32_t n_new, const float* levels, void* stream);
 
 /* kvq_decode_attn over a cache appended with kvq_append_levels and the same
  * table (page 3, KVQuant "Non-Uniform KV Cache Quantization": x_hat = z + r *
- * l_code on read; T_cur a multiple of key_block). 4-bit codes at head_dim 128
+ * l_code on read; any T_cur, the keys of an unfinished block from K_TAIL).
+ * 4-bit codes at head_dim 128
  * take the tensor-core kernel (levels as fp16 operands; the workspace then
  * carries the status word of kvq_decode_attn), other caches and
  * KVQ_FLAG_PRECISE_SCORES the fp32 CUDA-core kernel. Errors: those of
- * kvq_decode_attn; KVQ_ERR_ARG for a bad table; KVQ_ERR_UNSUPPORTED for a
- * partial key block. */
+ * kvq_decode_attn; KVQ_ERR_ARG for a bad table. */
 KVQ_API int kvq_decode_attn_levels(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t H_q,
                                    int32_t q_pos, const void* rope_tab, float sm_scale, void* out,
+                                   void* workspace, size_t workspace_bytes, const float* levels, void* stream);
+
+/* kvq_decode_step for a level-table cache (page 3, KVQuant "Non-Uniform KV
+ * Cache Quantization", in the serving workflow of mlqm.cn/news/1064729, §3.2
+ * and §4.2): kvq_append_levels of the new token (n_new = 1), then
+ * kvq_decode_attn_levels of q at its position T_cur, on one stream, with the
+ * same table (levels: host pointer to the 2^bits levels, copied into the
+ * launches). Arguments, results, ownership and the T_cur update are those of
+ * kvq_decode_step; the result and the cache are bit-identical to the two
+ * calls. Errors: those of kvq_decode_step, plus KVQ_ERR_ARG for a table that
+ * does not start at 0, end at 1 and increase (checked before any launch). */
+KVQ_API int kvq_decode_step_levels(const kvq_config* cfg, kvq_cache* cache, const void* k_new, const void* v_new,
+                                   const void* q, int32_t H_q, const void* rope_tab, float sm_scale, void* out,
                                    void* workspace, size_t workspace_bytes, const float* levels, void* stream);
 
 /* Static, human-readable name of a status code (a utility of this library;

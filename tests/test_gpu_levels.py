@@ -22,7 +22,7 @@ pytestmark = pytest.mark.gpu
 
 W = ki.Workload
 CASES = {
-    # name: (workload, T, append pieces (whole key blocks))
+    # name: (workload, T, append pieces)
     "gqa_int4_outliers_rope": (W("lv4", 2, 8, 2, 128, 256, 4, 64, 64, 0.01, 5e5, 51), 256, [128, 128]),
     "d64_int3_bk128_two_outliers": (W("lv3", 1, 4, 2, 64, 256, 3, 128, 32, 0.04, 1e4, 52), 256, [256]),
     "mha_int8_norope": (W("lv8", 1, 2, 2, 128, 128, 8, 64, 64, 0.0, 0.0, 53), 128, [64, 64]),
@@ -30,6 +30,11 @@ CASES = {
     # 4-bit codes at head_dim 128 run on the tensor-core kernel (level lookups)
     "int4_bk128_mha_tc": (W("lv4b", 2, 4, 4, 128, 1024, 4, 128, 64, 0.0, 1e4, 56), 1024, [512, 512]),
     "int4_g8_gv32_long_tc": (W("lv4g", 2, 16, 2, 128, 4096, 4, 64, 32, 0.01, 5e5, 57), 4096, [4096]),
+    # ragged appends ending in an unfinished key block (its keys stay fp16 in K_TAIL)
+    "int4_ragged_tc": (W("lv4r", 2, 8, 2, 128, 777, 4, 64, 64, 0.01, 5e5, 58), 777, [100, 1, 63, 300, 313]),
+    "int3_d64_ragged": (W("lv3r", 1, 4, 2, 64, 300, 3, 128, 32, 0.04, 1e4, 59), 300, [37, 91, 1, 171]),
+    "int8_ragged_norope": (W("lv8r", 1, 2, 2, 128, 200, 8, 64, 64, 0.01, 0.0, 60), 200, [65, 70, 65]),
+    "int2_g8_ragged": (W("lv2r", 1, 16, 2, 128, 250, 2, 64, 128, 0.01, 5e5, 61), 250, [1, 1, 1, 63, 184]),
 }
 
 
@@ -57,7 +62,8 @@ def test_levels_parity(name, precise):
     tensor-core kernel)."""
     w, T, pieces = CASES[name]
     lv = _levels(w)
-    cache = kvq.QuantizedKVCache(w.B, w.H_kv, w.D, T + w.key_block, w.bits, w.key_block, w.value_group,
+    T_max = (T // w.key_block + 1) * w.key_block
+    cache = kvq.QuantizedKVCache(w.B, w.H_kv, w.D, T_max, w.bits, w.key_block, w.value_group,
                                  w.outlier_frac, H_q=w.H_q, rope_theta=w.rope_theta, device="cuda",
                                  precise=precise)
     K, V = ki.kv_torch(w, 0, 0, T, "cuda")
@@ -80,10 +86,69 @@ def test_levels_parity(name, precise):
         tl.check_decode(tl.q_of_streams(out, w, streams), ref, f"{name} q_pos={q_pos}")
 
 
-def test_levels_reject_partial_blocks():
-    w = W("lvp", 1, 2, 2, 128, 64, 4, 64, 64, 0.0, 0.0, 55)
-    cache = tl.make_cache(w, 128)
-    K, V = ki.kv_torch(w, 0, 0, 32, "cuda")
-    with pytest.raises(kvq.KvqError) as e:
-        cache.append_levels(K, V, np.linspace(0, 1, 16, dtype=np.float32))
-    assert e.value.status == 2 and cache.T_cur == 0
+def test_levels_token_by_token_serving():
+    """The serving loop on a level-table cache: a prefill, then one token
+    appended and attended per step across key-block edges (tensor-core kernel
+    for these 4-bit codes; kvq_decode_step_levels on odd positions, the two
+    calls on even ones), against the oracle's encoding of the same prefix."""
+    w = W("lvtok", 1, 8, 2, 128, 200, 4, 64, 64, 0.01, 5e5, 62)
+    lv = _levels(w)
+    T0, T = 120, 200
+    cache = tl.make_cache(w, 256)
+    K, V = ki.kv_torch(w, 0, 0, T, "cuda")
+    cache.append_levels(K[:, :, :T0].contiguous(), V[:, :, :T0].contiguous(), lv)
+    streams = [(0, h) for h in range(w.H_kv)]
+    Kh, Vh = tl.host_streams(w, streams, T)
+    q = ki.queries_torch(w, 0, 0, "cuda")
+    qs = tl.q_of_streams(q.cpu().numpy(), w, streams)
+    for t in range(T0, T):
+        k1, v1 = K[:, :, t:t + 1].contiguous(), V[:, :, t:t + 1].contiguous()
+        if t % 2:                                        # the fused step on odd positions
+            out = cache.decode_step_levels(k1, v1, q, lv)
+        else:
+            cache.append_levels(k1, v1, lv)
+            out = cache.decode_levels(q, lv)
+        if t in (T0, 127, 128, 150, T - 1):
+            n = t + 1
+            out = out.cpu().numpy()
+            enc = oc.encode(Kh[:, :n], Vh[:, :n], w.bits, w.key_block, w.value_group, tl.n_out_of(w), levels=lv)
+            Kd, Vd = oc.dequant(enc, n, w.D, w.bits, w.key_block, w.value_group, tl.n_out_of(w), levels=lv)
+            ref = oc.attention(Kd, Vd, qs, n - 1, w.rope_theta, 1.0 / math.sqrt(w.D))
+            tl.check_decode(tl.q_of_streams(out, w, streams), ref, f"tokens={n}")
+    tl.sync()
+    enc = oc.encode(Kh, Vh, w.bits, w.key_block, w.value_group, tl.n_out_of(w), levels=lv)
+    tl.compare_streams(cache, streams, enc, T)
+
+
+def test_decode_step_levels_matches_the_two_calls():
+    """kvq_decode_step_levels is bit-identical to kvq_append_levels (one token)
+    followed by kvq_decode_attn_levels, on both level kernels."""
+    for w in (W("lvs4", 2, 8, 2, 128, 130, 4, 64, 64, 0.01, 5e5, 63),     # tensor-core kernel
+              W("lvs3", 1, 4, 2, 64, 130, 3, 64, 32, 0.04, 1e4, 64)):     # CUDA-core kernel
+        lv = _levels(w)
+        a, b = tl.make_cache(w, 192), tl.make_cache(w, 192)
+        K, V = ki.kv_torch(w, 0, 0, w.T + 3, "cuda")
+        for c in (a, b):
+            c.append_levels(K[:, :, :w.T].contiguous(), V[:, :, :w.T].contiguous(), lv)
+        q = ki.queries_torch(w, 0, 0, "cuda")
+        for t in range(w.T, w.T + 3):
+            k1, v1 = K[:, :, t:t + 1].contiguous(), V[:, :, t:t + 1].contiguous()
+            x = a.decode_step_levels(k1, v1, q, lv).clone()
+            b.append_levels(k1, v1, lv)
+            y = b.decode_levels(q, lv).clone()
+            assert torch.equal(x, y), t
+        tl.sync()
+        T, Bk = a.T_cur, w.key_block
+        nb = T // Bk
+        va, vb = a.views(), b.views()
+        for name in va:                                  # the rows written so far
+            x, y = va[name].cpu().numpy(), vb[name].cpu().numpy()
+            if name in ("k_codes", "k_outl"):
+                x, y = x[:, :, : nb * Bk], y[:, :, : nb * Bk]
+            elif name == "k_meta":
+                x, y = x[:, :, :nb], y[:, :, :nb]
+            elif name == "k_tail":
+                x, y = x[:, :, : T - nb * Bk], y[:, :, : T - nb * Bk]
+            else:
+                x, y = x[:, :, :T], y[:, :, :T]
+            assert np.array_equal(x.view(np.uint8), y.view(np.uint8)), name
