@@ -625,10 +625,9 @@ def run_paged(args, w, rank, world, device):
 def run_levels(args, w, rank, world, device):
     """Non-uniform codes: a level table fitted (kvq_fit_levels) to the
     normalized values of another layer's groups; the cache is filled with
-    kvq_append_levels (whole key blocks) and each step times one
-    kvq_decode_attn_levels call over T tokens (the tensor-core kernel in its
-    level-table mode for 4-bit codes at head_dim 128, the CUDA-core kernel
-    otherwise)."""
+    kvq_append_levels and each step times one kvq_decode_attn_levels call over
+    T tokens (the tensor-core kernel in its level-table mode at head_dim 128,
+    the CUDA-core kernel at head_dim 64)."""
     import numpy as np
     import torch
     import torch.distributed as dist
@@ -690,7 +689,7 @@ def run_levels(args, w, rank, world, device):
         "gpu_launches": 2 * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_kind,
-                     "kernel": ("decode_tc_kernel, level-table mode (+ decode_combine_kernel)" if w.D == 128 and w.bits == 4
+                     "kernel": ("decode_tc_kernel, level-table mode (+ decode_combine_kernel)" if w.D == 128
                                 else "decode_levels_kernel + combine (CUDA cores)"),
                      "alg_bytes_per_launch": alg, "traffic": None},
         "clocks": clk,

@@ -25,7 +25,7 @@ SOURCES = ["kvq_api.cu", "kvq_rope.cu", "kvq_append.cu", "kvq_decode.cu", "kvq_l
            "kvq_decode_tc_b2p.cu", "kvq_decode_tc_b3p.cu", "kvq_decode_tc_b4p.cu",
            "kvq_decode_tc_b2op.cu", "kvq_decode_tc_b3op.cu", "kvq_decode_tc_b4op.cu",
            "kvq_decode_tc_b8.cu", "kvq_decode_tc_b8o.cu", "kvq_decode_tc_b8p.cu", "kvq_decode_tc_b8op.cu",
-           "kvq_decode_tc_b4lv.cu"]
+           "kvq_decode_tc_b2lv.cu", "kvq_decode_tc_b3lv.cu", "kvq_decode_tc_b4lv.cu", "kvq_decode_tc_b8lv.cu"]
 
 
 def nvcc() -> str:

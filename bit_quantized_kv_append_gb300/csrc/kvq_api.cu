@@ -516,7 +516,7 @@ int kvq_decode_attn_levels(const kvq_config* cfg, const kvq_cache* cache, const 
   if (!make_levels(levels, d.bits, &t)) return KVQ_ERR_ARG;
   rc = device_ok();
   if (rc) return rc;
-  if (d.D == 128 && d.bits == 4 && !(d.flags & KVQ_FLAG_PRECISE_SCORES))   // the tensor-core kernel
+  if (d.D == 128 && !(d.flags & KVQ_FLAG_PRECISE_SCORES))   // the tensor-core kernel
     return cuda_status(launch_decode(d, *cache, static_cast<const __half*>(q), H_q, q_pos,
                                      static_cast<const float2*>(rope_tab), sm_scale, static_cast<__half*>(out),
                                      static_cast<float*>(workspace), static_cast<cudaStream_t>(stream), 0, nullptr,
@@ -549,7 +549,7 @@ int kvq_decode_step_levels(const kvq_config* cfg, kvq_cache* cache, const void* 
                                  1, st, nullptr, 0, nullptr, t.mid));
   if (rc) return rc;
   cache->T_cur = pos + 1;
-  if (d.D == 128 && d.bits == 4 && !(d.flags & KVQ_FLAG_PRECISE_SCORES))   // the tensor-core kernel
+  if (d.D == 128 && !(d.flags & KVQ_FLAG_PRECISE_SCORES))   // the tensor-core kernel
     return cuda_status(launch_decode(d, *cache, static_cast<const __half*>(q), H_q, pos,
                                      static_cast<const float2*>(rope_tab), sm_scale, static_cast<__half*>(out),
                                      static_cast<float*>(workspace), st, 0, nullptr, 0, t.lv));

@@ -182,14 +182,12 @@ void pick_tc_p(int Bk, int G, bool outl, TcLaunchFn* f, TcOccFn* o) {
   else
     outl ? pick_tc_g<BITS, 2, true, PAGED, MODE>(G, f, o) : pick_tc_g<BITS, 2, false, PAGED, MODE>(G, f, o);
 }
-// mode 0: fp16-operand scores, 1: precise scores, 2: level tables (4-bit, contiguous only)
+// mode 0: fp16-operand scores, 1: precise scores, 2: level tables (contiguous caches only)
 template <int BITS>
 void pick_tc(int Bk, int G, bool outl, bool paged, int mode, TcLaunchFn* f, TcOccFn* o) {
-  if constexpr (BITS == 4) {
-    if (mode == 2) {
-      pick_tc_p<4, false, 2>(Bk, G, outl, f, o);
-      return;
-    }
+  if (mode == 2) {
+    pick_tc_p<BITS, false, 2>(Bk, G, outl, f, o);
+    return;
   }
   if (mode == 1) paged ? pick_tc_p<BITS, true, 1>(Bk, G, outl, f, o) : pick_tc_p<BITS, false, 1>(Bk, G, outl, f, o);
   else paged ? pick_tc_p<BITS, true, 0>(Bk, G, outl, f, o) : pick_tc_p<BITS, false, 0>(Bk, G, outl, f, o);
@@ -231,7 +229,7 @@ cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, in
   a.ws = ws;
   a.status = reinterpret_cast<uint32_t*>(ws_all);
   a.tx_pad = tx_pad;
-  for (int k = 0; k < 16; ++k) a.lv[k] = levels ? levels[k] : 0.0f;
+  for (int k = 0; k < 256; ++k) a.lv[k] = (levels && k < (1 << d.bits)) ? levels[k] : 0.0f;
   // paged: the grid is sized for the longest sequence; each CTA reads its own length
   a.T = pg ? pg->max_len : c.T_cur;
   a.n_full = a.T / d.Bk;
@@ -263,7 +261,7 @@ cudaError_t launch_decode(const Dims& d, const kvq_cache& c, const __half* q, in
     TcOccFn occ_fn = nullptr;
     const bool paged = pg != nullptr;
     const int mode = levels ? 2 : (d.flags & KVQ_FLAG_PRECISE_SCORES) ? 1 : 0;
-    if (mode == 2 && (d.bits != 4 || paged)) return cudaErrorInvalidValue;   // the API only asks for 4-bit caches
+    if (mode == 2 && paged) return cudaErrorInvalidValue;   // the API asks for contiguous caches only
     switch (d.bits) {
       case 2: pick_tc<2>(d.Bk, G, d.n_out > 0, paged, mode, &fn, &occ_fn); break;
       case 3: pick_tc<3>(d.Bk, G, d.n_out > 0, paged, mode, &fn, &occ_fn); break;

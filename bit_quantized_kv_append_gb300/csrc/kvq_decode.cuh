@@ -47,7 +47,7 @@ struct DecodeArgs {
   int max_blocks, n_blocks;
   uint32_t* status;            // device status word: KVQ_STATUS_* bits are ORed in
   uint32_t tx_pad;             // diagnostics: bytes each ring stage expects beyond its copies (0)
-  float lv[16];                // level table of non-uniform 4-bit codes (tensor-core mode 2)
+  float lv[256];               // level table of non-uniform codes (tensor-core mode 2)
 };
 
 // Tokens, full key blocks, tail length and query position of sequence b.

@@ -367,19 +367,86 @@ __device__ __forceinline__ void value_pair(const uint8_t* vc, const LaneOff& o, 
     b[3] = x6 & 0x00380038u;
   }
 }
-// Level tables, 4-bit codes: the value A operands as fp16 levels. A byte of a
-// code row holds two channels; s_lut[byte] is {l[lo nibble], l[hi nibble]}.
-// b[0] = (l[channel 32 c4 + 4 g] at t, at t + 1), b[1] the next channel,
-// b[2], b[3] the following byte's two channels (the layout value_pair<4> gives).
-__device__ __forceinline__ void value_pair_lv(const uint8_t* vc, const LaneOff& o, int sl, int rp, int c4,
-                                              const uint32_t* s_lut, int bb, uint32_t (&b)[4]) {
-  const uint8_t* p = vc + (o.vb + ((c4 << 4) ^ o.vx)) + 4096 * sl + 512 * rp;
-  const uint32_t A = ld_s32(p), B = ld_s32(p + 64);
+// Level tables: the codes index fp16 levels instead of the uniform grid.
+// s_lut[i] = {l[i & (2^BITS - 1)], l[i >> BITS]} for a 2·BITS-bit index i (two
+// codes at once; 2, 3 and 4 bits), s_lvh[c] = l[c] (8 bits).
+__device__ __forceinline__ uint32_t lv_pair8(const __half* s_lvh, uint32_t lo, uint32_t hi) {
+  return as_u32(__halves2half2(s_lvh[lo & 0xFFu], s_lvh[hi & 0xFFu]));
+}
+// Key operands of k-step kq, slots (0, 1) -> x0 and (2, 3) -> x1, as the
+// uniform key_codes<BITS> pairs them, but as fp16 levels.
+template <int BITS>
+__device__ __forceinline__ void key_codes_lv(const uint32_t (&wd)[2], uint32_t ksh, int kq, const uint32_t* s_lut,
+                                             uint32_t& x0, uint32_t& x1) {
+  if constexpr (BITS == 4) {
+    // slots (0, 2) from byte kq & 1 of the word, (1, 3) from byte (kq & 1) + 2
+    const uint32_t W = wd[kq >> 1];
+    const int sh = 8 * (kq & 1);   // kq is unrolled: a constant shift
+    const uint32_t fa = s_lut[(W >> sh) & 0xFFu], fb = s_lut[(W >> (sh + 16)) & 0xFFu];
+    x0 = __byte_perm(fa, fb, 0x5410u);
+    x1 = __byte_perm(fa, fb, 0x7632u);
+  } else if constexpr (BITS == 2) {
+    // slots (0, 1): the codes at bits 2m and 16 + 2m of the word, m = 2 (kq & 1) (x0) and m + 1 (x1)
+    const uint32_t W = kq >= 2 ? wd[0] >> 8 : wd[0];
+    const int m = 2 * (kq & 1);
+    x0 = s_lut[((W >> (2 * m)) & 3u) | ((W >> (2 * m + 14)) & 0xCu)];
+    x1 = s_lut[((W >> (2 * m + 2)) & 3u) | ((W >> (2 * m + 16)) & 0xCu)];
+  } else {
+    // 3 bits: the 6-bit windows t0, t1 hold slots (0, 1) and (2, 3), low code first
+    const uint64_t X = (((uint64_t)wd[1] << 32) | wd[0]) >> ksh;
+    x0 = s_lut[(uint32_t)(X >> (12 * kq)) & 63u];
+    x1 = s_lut[(uint32_t)(X >> (12 * kq + 6)) & 63u];
+  }
+}
+// 8 bits: bytes (0, 1) -> x0, (2, 3) -> x1 as levels (the order of key_codes8).
+__device__ __forceinline__ void key_codes8_lv(uint32_t W, const __half* s_lvh, uint32_t& x0, uint32_t& x1) {
+  x0 = lv_pair8(s_lvh, W, W >> 8);
+  x1 = lv_pair8(s_lvh, W >> 16, W >> 24);
+}
+// The value A operands of value_pair<BITS> (token t in the low half, t + 1 in
+// the high half of b[e], channel 32 c4 + 4 g + e) as fp16 levels; the same
+// addresses as value_pair<BITS>.
+template <int BITS>
+__device__ __forceinline__ void value_pair_lv(const uint8_t* vc, const LaneOff& o, int sl, int rp, int c4, int g,
+                                              const uint32_t* s_lut, const __half* s_lvh, uint32_t (&b)[4]) {
+  if constexpr (BITS == 4) {
+    const int bb = 2 * (g & 1);
+    const uint8_t* p = vc + (o.vb + ((c4 << 4) ^ o.vx)) + 4096 * sl + 512 * rp;
+    const uint32_t A = ld_s32(p), B = ld_s32(p + 64);
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint32_t la = s_lut[(A >> (8 * (bb + h))) & 0xFFu], lb = s_lut[(B >> (8 * (bb + h))) & 0xFFu];
-    b[2 * h] = __byte_perm(la, lb, 0x5410u);
-    b[2 * h + 1] = __byte_perm(la, lb, 0x7632u);
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t la = s_lut[(A >> (8 * (bb + h))) & 0xFFu], lb = s_lut[(B >> (8 * (bb + h))) & 0xFFu];
+      b[2 * h] = __byte_perm(la, lb, 0x5410u);
+      b[2 * h + 1] = __byte_perm(la, lb, 0x7632u);
+    }
+  } else if constexpr (BITS == 8) {
+    const uint8_t* p = vc + o.vb + 8192 * sl + 1024 * rp;
+    const uint32_t ca = (((2 * c4 + o.vsh) << 4) ^ o.vx);
+    const uint32_t A = ld_s32(p + ca), B = ld_s32(p + 128 + (ca ^ 16u));
+#pragma unroll
+    for (int e = 0; e < 4; ++e) b[e] = lv_pair8(s_lvh, A >> (8 * e), B >> (8 * e));
+  } else if constexpr (BITS == 2) {
+    // x: token t's byte in bits 0-7, token t + 1's in bits 16-23 (as value_pair<2>)
+    const uint8_t* p = vc + (o.vb + (((c4 >> 1) << 4) ^ o.vx)) + 2048 * sl + 256 * rp + 8 * (c4 & 1);
+    const uint32_t x = __byte_perm(ld_s32(p), ld_s32(p + 32), o.sel0);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) b[e] = s_lut[((x >> (2 * e)) & 3u) | ((x >> (2 * e + 14)) & 0xCu)];
+  } else {
+    // 3 bits: x = token t's 12-bit window | token t + 1's << 16 (as value_pair<3>)
+    const uint8_t* p = vc + o.vb + 3072 * sl + 384 * rp + 12 * c4;
+    const uint32_t a0 = ld_s32(p), b0 = ld_s32(p + 48);
+    uint32_t a1 = 0u, b1 = 0u;
+    if (o.vsh + 12 > 32) {
+      a1 = ld_s32(p + 4);
+      b1 = ld_s32(p + 52);
+    }
+    const uint32_t tA = __funnelshift_r(a0, a1, o.vsh) & 0xFFFu, tB = __funnelshift_r(b0, b1, o.vsh) & 0xFFFu;
+    const uint32_t x = tA | (tB << 16);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t y = x >> (3 * e);
+      b[e] = s_lut[(y & 7u) | ((y >> 13) & 0x38u)];
+    }
   }
 }
 
@@ -455,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
                                                              const __grid_constant__ CUtensorMap tm_v) {
   constexpr bool PREC = MODE == 1;
   constexpr bool LV = MODE == 2;
-  static_assert(!LV || BITS == 4, "level tables run at 4 bits");
+  constexpr int LVN = (LV && BITS != 8) ? 1 << (2 * BITS) : 1;   // LV: entries of the pair table
   constexpr int HALF = kD / 2;
   constexpr int BK = 64 * SL;
   constexpr int NST = ring_stages(BK);
@@ -480,8 +547,9 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
   __shared__ __align__(16) KcT s_kc[OUTL ? 2 : 1][OUTL ? G : 1][OUTL ? BK : 2];
   __shared__ float s_wm[kWarps][G], s_wl[kWarps][G], s_wf[kWarps][G];
   __shared__ float s_z[kWarps][G][4];                         // zero-point sums per 32-channel block
-  __shared__ uint32_t s_lut[LV ? 256 : 1];                    // LV: {l[b & 15], l[b >> 4]} fp16 per code byte b
-  __shared__ float s_lvf[LV ? 16 : 1];                        // LV: the levels
+  __shared__ uint32_t s_lut[LVN];                             // LV: {l[i & M], l[i >> BITS]} fp16, two codes
+  __shared__ __half s_lvh[(LV && BITS == 8) ? 256 : 1];       // LV, 8 bits: the fp16 levels
+  __shared__ float s_lvf[LV ? 1 << BITS : 1];                 // LV: the levels
 
   const Dims d = a.d;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -720,9 +788,14 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
     uint32_t* zl = reinterpret_cast<uint32_t*>(&s_ql[0][0][0][0]);
     for (int e = tid; e < (int)(sizeof(s_ql) / 4); e += kThreads) zl[e] = 0u;
     if constexpr (LV) {
-      for (int e = tid; e < 256; e += kThreads)
-        s_lut[e] = as_u32(__floats2half2_rn(a.lv[e & 15], a.lv[e >> 4]));
-      if (tid < 16) s_lvf[tid] = a.lv[tid];
+      constexpr int NL = 1 << BITS;
+      if constexpr (BITS == 8) {
+        for (int e = tid; e < NL; e += kThreads) s_lvh[e] = __float2half_rn(a.lv[e]);
+      } else {
+        for (int e = tid; e < LVN; e += kThreads)
+          s_lut[e] = as_u32(__floats2half2_rn(a.lv[e & (NL - 1)], a.lv[e >> BITS]));
+      }
+      for (int e = tid; e < NL; e += kThreads) s_lvf[e] = a.lv[e];
     }
     float* f = reinterpret_cast<float*>(&s_acc[0][0][0][0]);
     for (int e = tid; e < (int)(sizeof(s_acc) / 4); e += kThreads) f[e] = 0.0f;
@@ -817,23 +890,19 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
             if constexpr (BITS == 8) {
               const uint32_t wf[4] = {k8f[nt].x, k8f[nt].y, k8f[nt].z, k8f[nt].w};
               const uint32_t wp[4] = {k8p[nt].x, k8p[nt].y, k8p[nt].z, k8p[nt].w};
-              key_codes8(wf[kq], f0, f1);
-              key_codes8(wp[kq], p0, p1);
-            } else {
               if constexpr (LV) {
-                // levels of slots (0, 2) from byte kq & 1 of the word, (1, 3) from byte (kq & 1) + 2
-                const uint32_t Wf = kw[nt].f[kq >> 1], Wp = kw[nt].p[kq >> 1];
-                const int sh = 8 * (kq & 1);   // kq is unrolled: a constant shift
-                const uint32_t fa = s_lut[(Wf >> sh) & 0xFFu], fb = s_lut[(Wf >> (sh + 16)) & 0xFFu];
-                const uint32_t pa = s_lut[(Wp >> sh) & 0xFFu], pb = s_lut[(Wp >> (sh + 16)) & 0xFFu];
-                f0 = __byte_perm(fa, fb, 0x5410u);
-                f1 = __byte_perm(fa, fb, 0x7632u);
-                p0 = __byte_perm(pa, pb, 0x5410u);
-                p1 = __byte_perm(pa, pb, 0x7632u);
+                key_codes8_lv(wf[kq], s_lvh, f0, f1);
+                key_codes8_lv(wp[kq], s_lvh, p0, p1);
               } else {
-                key_codes<BITS>(kw[nt].f, lo.ksh, kq, f0, f1);
-                key_codes<BITS>(kw[nt].p, lo.ksh, kq, p0, p1);
+                key_codes8(wf[kq], f0, f1);
+                key_codes8(wp[kq], p0, p1);
               }
+            } else if constexpr (LV) {
+              key_codes_lv<BITS>(kw[nt].f, lo.ksh, kq, s_lut, f0, f1);
+              key_codes_lv<BITS>(kw[nt].p, lo.ksh, kq, s_lut, p0, p1);
+            } else {
+              key_codes<BITS>(kw[nt].f, lo.ksh, kq, f0, f1);
+              key_codes<BITS>(kw[nt].p, lo.ksh, kq, p0, p1);
             }
             if constexpr (PREC) {
               const uint2 qfl2 = s_ql[PREC ? buf : 0][PREC ? sl : 0][PREC ? kq : 0][PREC ? lane : 0];
@@ -1062,8 +1131,8 @@ __global__ void __launch_bounds__(kThreads, KVQ_TC_MINB) decode_tc_kernel(const 
         }
         uint32_t x0[4], x1[4];
         if constexpr (LV) {
-          value_pair_lv(vc, lo, sl, 0, c4, s_lut, 2 * (g & 1), x0);
-          value_pair_lv(vc, lo, sl, 1, c4, s_lut, 2 * (g & 1), x1);
+          value_pair_lv<BITS>(vc, lo, sl, 0, c4, g, s_lut, s_lvh, x0);
+          value_pair_lv<BITS>(vc, lo, sl, 1, c4, g, s_lut, s_lvh, x1);
         } else {
           value_pair<BITS>(vc, lo, sl, 0, c4, x0);
           value_pair<BITS>(vc, lo, sl, 1, c4, x1);

@@ -1,0 +1,7 @@
+// Tensor-core decode kernels (head_dim 128) for 2-bit codes against a level table.
+#include "kvq_decode_tc_inst.cuh"
+
+namespace kvq {
+KVQ_INSTANTIATE_TC_LV(2, false)
+KVQ_INSTANTIATE_TC_LV(2, true)
+}  // namespace kvq

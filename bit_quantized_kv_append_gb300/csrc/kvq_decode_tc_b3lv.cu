@@ -1,0 +1,7 @@
+// Tensor-core decode kernels (head_dim 128) for 3-bit codes against a level table.
+#include "kvq_decode_tc_inst.cuh"
+
+namespace kvq {
+KVQ_INSTANTIATE_TC_LV(3, false)
+KVQ_INSTANTIATE_TC_LV(3, true)
+}  // namespace kvq

@@ -2,6 +2,6 @@
 #include "kvq_decode_tc_inst.cuh"
 
 namespace kvq {
-KVQ_INSTANTIATE_TC_LV(false)
-KVQ_INSTANTIATE_TC_LV(true)
+KVQ_INSTANTIATE_TC_LV(4, false)
+KVQ_INSTANTIATE_TC_LV(4, true)
 }  // namespace kvq

@@ -47,16 +47,16 @@ int tc_occupancy(size_t smem) {
 #define KVQ_TC_ONE(BITS, G, SL, OUTL, PAGED) \
   KVQ_TC_ONE_P(BITS, G, SL, OUTL, PAGED, 0) \
   KVQ_TC_ONE_P(BITS, G, SL, OUTL, PAGED, 1)
-// mode 2 (level tables): 4-bit contiguous caches
-#define KVQ_INSTANTIATE_TC_LV(OUTL)      \
-  KVQ_TC_ONE_P(4, 1, 1, OUTL, false, 2)  \
-  KVQ_TC_ONE_P(4, 2, 1, OUTL, false, 2)  \
-  KVQ_TC_ONE_P(4, 4, 1, OUTL, false, 2)  \
-  KVQ_TC_ONE_P(4, 8, 1, OUTL, false, 2)  \
-  KVQ_TC_ONE_P(4, 1, 2, OUTL, false, 2)  \
-  KVQ_TC_ONE_P(4, 2, 2, OUTL, false, 2)  \
-  KVQ_TC_ONE_P(4, 4, 2, OUTL, false, 2)  \
-  KVQ_TC_ONE_P(4, 8, 2, OUTL, false, 2)
+// mode 2 (level tables): contiguous caches
+#define KVQ_INSTANTIATE_TC_LV(BITS, OUTL)      \
+  KVQ_TC_ONE_P(BITS, 1, 1, OUTL, false, 2)     \
+  KVQ_TC_ONE_P(BITS, 2, 1, OUTL, false, 2)     \
+  KVQ_TC_ONE_P(BITS, 4, 1, OUTL, false, 2)     \
+  KVQ_TC_ONE_P(BITS, 8, 1, OUTL, false, 2)     \
+  KVQ_TC_ONE_P(BITS, 1, 2, OUTL, false, 2)     \
+  KVQ_TC_ONE_P(BITS, 2, 2, OUTL, false, 2)     \
+  KVQ_TC_ONE_P(BITS, 4, 2, OUTL, false, 2)     \
+  KVQ_TC_ONE_P(BITS, 8, 2, OUTL, false, 2)
 #define KVQ_INSTANTIATE_TC(BITS, OUTL, PAGED) \
   KVQ_TC_ONE(BITS, 1, 1, OUTL, PAGED)         \
   KVQ_TC_ONE(BITS, 2, 1, OUTL, PAGED)         \

@@ -9,8 +9,8 @@
 // those of the uniform cache.
 //
 // This file: the plain CUDA-core decode (split-T partials and their combine)
-// for the tables the tensor-core kernel's level mode does not take (bit widths
-// other than 4, head_dim 64, precise scores). The append is the uniform
+// for the calls the tensor-core kernel's level mode does not take (head_dim
+// 64, precise scores). The append is the uniform
 // append's kernel in its level-table mode (kvq_append.cu); the fp16 keys of an
 // unfinished key block come from K_TAIL here as in the uniform decode.
 #include "kvq_levels.cuh"

@@ -87,10 +87,10 @@ typedef enum kvq_status {
  * outputs' tolerance while the logits span a few nats but moves the weights
  * of attention whose competing logits are tens of nats apart from the rest.
  * The flag costs decode time (about 2.1-2.3x on GB300). head_dim 64 computes
- * in fp32 and ignores it; a level-table decode (kvq_decode_attn_levels) with
- * 4-bit codes at head_dim 128 runs on the tensor-core kernel with fp16
- * operands unless the flag is set, which sends it to the fp32 CUDA-core
- * kernel. Other bits: reserved (0). */
+ * in fp32 and ignores it; a level-table decode (kvq_decode_attn_levels) at
+ * head_dim 128 runs on the tensor-core kernel with fp16 operands unless the
+ * flag is set, which sends it to the fp32 CUDA-core kernel. Other bits:
+ * reserved (0). */
 #define KVQ_FLAG_PRECISE_SCORES 1
 
 /* One layer's cache shape. Supported: bits in {2, 3, 4, 8} (8: the 8-bit
@@ -398,9 +398,8 @@ KVQ_API int kvq_append_levels(const kvq_config* cfg, kvq_cache* cache, const voi
 /* kvq_decode_attn over a cache appended with kvq_append_levels and the same
  * table (page 3, KVQuant "Non-Uniform KV Cache Quantization": x_hat = z + r *
  * l_code on read; any T_cur, the keys of an unfinished block from K_TAIL).
- * 4-bit codes at head_dim 128
- * take the tensor-core kernel (levels as fp16 operands; the workspace then
- * carries the status word of kvq_decode_attn), other caches and
+ * head_dim 128 takes the tensor-core kernel (levels as fp16 operands; the
+ * workspace then carries the status word of kvq_decode_attn), head_dim 64 and
  * KVQ_FLAG_PRECISE_SCORES the fp32 CUDA-core kernel. Errors: those of
  * kvq_decode_attn; KVQ_ERR_ARG for a bad table. */
 KVQ_API int kvq_decode_attn_levels(const kvq_config* cfg, const kvq_cache* cache, const void* q, int32_t H_q,

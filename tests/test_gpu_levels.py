@@ -27,7 +27,7 @@ CASES = {
     "d64_int3_bk128_two_outliers": (W("lv3", 1, 4, 2, 64, 256, 3, 128, 32, 0.04, 1e4, 52), 256, [256]),
     "mha_int8_norope": (W("lv8", 1, 2, 2, 128, 128, 8, 64, 64, 0.0, 0.0, 53), 128, [64, 64]),
     "g8_int2_gv128": (W("lv2", 1, 16, 2, 128, 192, 2, 64, 128, 0.01, 5e5, 54), 192, [192]),
-    # 4-bit codes at head_dim 128 run on the tensor-core kernel (level lookups)
+    # head_dim 128 runs on the tensor-core kernel (level lookups), head_dim 64 on the CUDA-core one
     "int4_bk128_mha_tc": (W("lv4b", 2, 4, 4, 128, 1024, 4, 128, 64, 0.0, 1e4, 56), 1024, [512, 512]),
     "int4_g8_gv32_long_tc": (W("lv4g", 2, 16, 2, 128, 4096, 4, 64, 32, 0.01, 5e5, 57), 4096, [4096]),
     # ragged appends ending in an unfinished key block (its keys stay fp16 in K_TAIL)
@@ -35,6 +35,9 @@ CASES = {
     "int3_d64_ragged": (W("lv3r", 1, 4, 2, 64, 300, 3, 128, 32, 0.04, 1e4, 59), 300, [37, 91, 1, 171]),
     "int8_ragged_norope": (W("lv8r", 1, 2, 2, 128, 200, 8, 64, 64, 0.01, 0.0, 60), 200, [65, 70, 65]),
     "int2_g8_ragged": (W("lv2r", 1, 16, 2, 128, 250, 2, 64, 128, 0.01, 5e5, 61), 250, [1, 1, 1, 63, 184]),
+    # 3-bit codes at head_dim 128 (128- and 64-token key blocks)
+    "int3_bk128_gqa_tc": (W("lv3t", 2, 8, 2, 128, 700, 3, 128, 32, 0.01, 5e5, 65), 700, [300, 1, 399]),
+    "int3_bk64_mha_tc": (W("lv3s", 1, 4, 4, 128, 333, 3, 64, 64, 0.01, 1e4, 66), 333, [200, 133]),
 }
 
 
@@ -57,9 +60,9 @@ def _levels(w):
 @pytest.mark.parametrize("precise", [False, True], ids=["default", "precise"])
 @pytest.mark.parametrize("name", list(CASES))
 def test_levels_parity(name, precise):
-    """precise: KVQ_FLAG_PRECISE_SCORES, which keeps 4-bit head_dim-128 level
-    tables on the fp32 CUDA-core kernel (the default runs them on the
-    tensor-core kernel)."""
+    """precise: KVQ_FLAG_PRECISE_SCORES, which keeps head_dim-128 level tables
+    on the fp32 CUDA-core kernel (the default runs them on the tensor-core
+    kernel)."""
     w, T, pieces = CASES[name]
     lv = _levels(w)
     T_max = (T // w.key_block + 1) * w.key_block
