@@ -188,6 +188,19 @@ template <int BITS>
 __device__ __forceinline__ uint32_t level_code_d(float d, float r, const float* mid) {
   return r > 0.0f ? level_index<BITS>(__fdiv_rn(d, r), mid) : 0u;
 }
+// The same code from y = d * (1/r), 1/r within one ulp (rcp_or_zero): y is
+// within 2^-22 of fp32(d / r) for quotients up to 1, so a y further than
+// 2^-20 from both neighbouring midpoints has the code of the exact quotient;
+// otherwise the exact rule decides. NaN (an outlier position) gives 0.
+template <int BITS>
+__device__ __forceinline__ uint32_t level_code_fast(float y, float d, float r, const float* mid) {
+  constexpr uint32_t L = (1u << BITS) - 1u;
+  constexpr float kEps = 9.5367431640625e-07f;   // 2^-20
+  const uint32_t q = level_index<BITS>(y, mid);
+  const float lo = q > 0u ? mid[q - 1u] : -INFINITY, hi = q < L ? mid[q] : INFINITY;
+  if (!(y - lo <= kEps) && !(hi - y <= kEps)) return q;
+  return level_code_d<BITS>(d, r, mid);
+}
 
 // Code-carrying bit patterns (float bits of y + kMagic: the code in bits 0-3,
 // zeros up to bit 21) -> packed LSB-first words.
@@ -280,10 +293,13 @@ __device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv,
       }
       const float2 d2 = make_float2(add_h_f((uint16_t)(hw[j] & 0xFFFFu), nz2.x), add_h_f((uint16_t)(hw[j] >> 16), nz2.y));
       if constexpr (LV) {
-        // r2 holds the ranges: the exact quotient, then the midpoint search
-        // (NaN, an outlier position, gives 0 and is patched below)
-        mb[e] = level_code_d<BITS>(d2.x, r2.x, mid);
-        mb[e + 1] = level_code_d<BITS>(d2.y, r2.y, mid);
+        // r2 holds 1/r: the product, the midpoint search, the exact quotient
+        // only next to a midpoint (NaN, an outlier position, gives 0 and is
+        // patched below)
+        const float2 u2 = __fmul2_rn(d2, r2);
+        const float ra = KEYS ? sS[ch * 32 + e] : vp.z, rb = KEYS ? sS[ch * 32 + e + 1] : vp.z;
+        mb[e] = level_code_fast<BITS>(u2.x, d2.x, ra, mid);
+        mb[e + 1] = level_code_fast<BITS>(u2.y, d2.y, rb, mid);
         continue;
       }
       const float2 y2 = __fmul2_rn(d2, r2);
@@ -537,8 +553,8 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a, co
       float2 sz;
       const uint32_t packed = LV ? range_zero(mn, mx, !isnan(mn), &sz) : group_params(mn, mx, !isnan(mn), Lf, &sz);
       a.v_meta[(size_t)(row_base + t_row0 + r) * ng + g] = packed;
-      // {-z, 1/s (LV: r, the divisor), s (LV: r)}
-      sPv[g * Bk + r] = make_float4(-sz.y, LV ? sz.x : rcp_or_zero(sz.x), sz.x, 0.0f);
+      // {-z, 1/s, s} (LV: 1/r, r)
+      sPv[g * Bk + r] = make_float4(-sz.y, rcp_or_zero(sz.x), sz.x, 0.0f);
     }
   } else if (a.phase == 2) {
     // window keys: min and max of the dense elements of the last
@@ -597,7 +613,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a, co
         a.k_meta[kblk * D + c] = packed;
         float* pk = reinterpret_cast<float*>(&sPk[cp]);
         pk[hc] = -sz.y;
-        pk[2 + hc] = LV ? sz.x : rcp_or_zero(sz.x);
+        pk[2 + hc] = rcp_or_zero(sz.x);
         sS[c] = sz.x;
       }
     }
