@@ -155,3 +155,36 @@ def test_decode_step_levels_matches_the_two_calls():
             else:
                 x, y = x[:, :, :T], y[:, :, :T]
             assert np.array_equal(x.view(np.uint8), y.view(np.uint8)), name
+
+
+def test_levels_exact_midpoints():
+    """Quotients exactly on the midpoints (ties go to the lower level): a
+    table whose levels and midpoints are fp16 values, every value group and
+    key channel holding 0 and 1 (so z = 0, r = 1 and u = x), and elements
+    planted on every midpoint and next to them; codes bit-exact against the
+    oracle."""
+    w = W("lvmid", 1, 4, 2, 128, 192, 4, 64, 64, 0.0, 1e4, 67)
+    lv = np.array([k / 16 for k in range(15)] + [1.0], dtype=np.float32)
+    mids = (lv[:-1].astype(np.float64) + lv[1:]) / 2
+    pts = [0.0, 1.0]
+    for m in mids:
+        h = np.float16(m)
+        assert float(h) == m                                   # the midpoints are fp16 values
+        pts += [m, float(np.nextafter(h, np.float16(0))), float(np.nextafter(h, np.float16(1)))]
+    grid = np.array(pts, dtype=np.float16)
+    t = np.arange(w.T)[:, None]
+    c = np.arange(w.D)[None, :]
+    base = grid[(t + 3 * c) % len(grid)]                        # [T, D]: each token and channel meets 0 and 1
+    base[:, 0], base[:, 1] = 0.0, 1.0                           # every value group holds 0 and 1
+    base[0::64, :], base[1::64, :] = 0.0, 1.0                   # every key channel of a block holds 0 and 1
+    Kh = np.broadcast_to(base, (w.B * w.H_kv, w.T, w.D)).copy()
+    Vh = Kh[:, ::-1].copy()
+    cache = tl.make_cache(w, 256)
+    K = torch.from_numpy(Kh.reshape(w.B, w.H_kv, w.T, w.D)).cuda()
+    V = torch.from_numpy(Vh.reshape(w.B, w.H_kv, w.T, w.D)).cuda()
+    cache.append_levels(K[:, :, :100].contiguous(), V[:, :, :100].contiguous(), lv)
+    cache.append_levels(K[:, :, 100:].contiguous(), V[:, :, 100:].contiguous(), lv)
+    streams = [(0, h) for h in range(w.H_kv)]
+    enc = oc.encode(Kh, Vh, w.bits, w.key_block, w.value_group, 0, levels=lv)
+    tl.sync()
+    tl.compare_streams(cache, streams, enc, w.T)
