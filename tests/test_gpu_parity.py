@@ -216,7 +216,8 @@ FULL = ["mha7b", "gqa8b", "int3", "int2"]
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_sampled_streams(name):
     """Full workload on the device (prefill through one append call, then decode);
-    the oracle checks two sampled (b, h_kv) streams end to end."""
+    the oracle checks three sampled (b, h_kv) streams end to end: the first,
+    one from the middle of the batch and heads, and the last."""
     w = ki.WORKLOADS[name]
     T = w.T
     cache = tl.make_cache(w, T + w.key_block)
@@ -225,7 +226,7 @@ def test_full_size_sampled_streams(name):
     del K, V
     q = ki.queries_torch(w, 0, 0, "cuda")
     out = cache.decode(q).cpu().numpy()
-    streams = [(0, 0), (w.B - 1, w.H_kv - 1)]
+    streams = [(0, 0), (w.B // 2, w.H_kv // 2 + 1), (w.B - 1, w.H_kv - 1)]
     Kh, Vh = tl.host_streams(w, streams, T)
     enc = tl.oracle_encode(w, Kh, Vh)
     tl.compare_streams(cache, streams, enc, T)
