@@ -191,7 +191,7 @@ __device__ __forceinline__ uint32_t level_code_d(float d, float r, const float* 
 // The same code from y = d * (1/r), 1/r within one ulp (rcp_or_zero): y is
 // within 2^-22 of fp32(d / r) for quotients up to 1, so a y further than
 // 2^-20 from both neighbouring midpoints has the code of the exact quotient;
-// otherwise the exact rule decides. NaN (an outlier position) gives 0.
+// otherwise the exact rule decides. NaN gives 0.
 template <int BITS>
 __device__ __forceinline__ uint32_t level_code_fast(float y, float d, float r, const float* mid) {
   constexpr uint32_t L = (1u << BITS) - 1u;
@@ -202,11 +202,25 @@ __device__ __forceinline__ uint32_t level_code_fast(float y, float d, float r, c
   return level_code_d<BITS>(d, r, mid);
 }
 
-// Code-carrying bit patterns (float bits of y + kMagic: the code in bits 0-3,
-// zeros up to bit 21) -> packed LSB-first words.
+// Code-carrying bit patterns -> packed LSB-first words. A pattern is the
+// float bits of y + kMagic for a code y in [0, 2^22): kMagicBits plus the code
+// (every dense element is inside its group's range, and step C' sets the
+// outlier positions to the group's zero, so every pattern of finite inputs
+// has this form).
+constexpr uint32_t kMagicBits = 0x4B400000u;   // float bits of 1.5 * 2^23
+// 2 and 3 bits: a word is the sum of its patterns shifted into their fields
+// (one shift-add each, modulo 2^32) less the same shifts of kMagicBits, a
+// compile-time constant; a code that straddles two words adds its high bits
+// to the second from the bare code.
+template <int BITS>
+__host__ __device__ constexpr uint32_t pack_bias(int k) {
+  uint32_t c = 0u;
+  for (int e = 0; e < 32; ++e)
+    if ((e * BITS) >> 5 == k) c += kMagicBits << ((e * BITS) & 31);
+  return c;
+}
 template <int BITS>
 __device__ __forceinline__ void pack_bits(const uint32_t (&mb)[32], uint32_t (&w)[BITS]) {
-  constexpr uint32_t M = (1u << BITS) - 1u;
   if constexpr (BITS == 4) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -214,7 +228,7 @@ __device__ __forceinline__ void pack_bits(const uint32_t (&mb)[32], uint32_t (&w
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const uint32_t lo = mb[8 * k + 2 * j], hi = mb[8 * k + 2 * j + 1];
-        byte[j] = (lo & 0xFu) + (hi << 4);   // byte 0: two codes (a NaN-marked slot gives 0xF, patched later)
+        byte[j] = (lo & 0xFu) + (hi << 4);   // byte 0: two codes
       }
       w[k] = __byte_perm(__byte_perm(byte[0], byte[1], 0x0040u), __byte_perm(byte[2], byte[3], 0x0040u), 0x5410u);
     }
@@ -225,13 +239,12 @@ __device__ __forceinline__ void pack_bits(const uint32_t (&mb)[32], uint32_t (&w
                          __byte_perm(mb[4 * k + 2], mb[4 * k + 3], 0x0040u), 0x5410u);
   } else {
 #pragma unroll
-    for (int k = 0; k < BITS; ++k) w[k] = 0u;
+    for (int k = 0; k < BITS; ++k) w[k] = 0u - pack_bias<BITS>(k);
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
-      const int bit = e * BITS;
-      const uint32_t q = mb[e] & M;
-      w[bit >> 5] |= q << (bit & 31);
-      if ((bit & 31) + BITS > 32) w[(bit >> 5) + 1] |= q >> (32 - (bit & 31));
+      const int bit = e * BITS, sh = bit & 31;
+      w[bit >> 5] += mb[e] << sh;
+      if (sh + BITS > 32) w[(bit >> 5) + 1] += (mb[e] - kMagicBits) >> (32 - sh);
     }
   }
 }
@@ -294,18 +307,18 @@ __device__ __forceinline__ void chunk_codes(const __half* sX, const float4* sPv,
       const float2 d2 = make_float2(add_h_f((uint16_t)(hw[j] & 0xFFFFu), nz2.x), add_h_f((uint16_t)(hw[j] >> 16), nz2.y));
       if constexpr (LV) {
         // r2 holds 1/r: the product, the midpoint search, the exact quotient
-        // only next to a midpoint (NaN, an outlier position, gives 0 and is
-        // patched below)
+        // only next to a midpoint (outlier positions hold z: code 0, patched
+        // below)
         const float2 u2 = __fmul2_rn(d2, r2);
         const float ra = KEYS ? sS[ch * 32 + e] : vp.z, rb = KEYS ? sS[ch * 32 + e + 1] : vp.z;
-        mb[e] = level_code_fast<BITS>(u2.x, d2.x, ra, mid);
-        mb[e + 1] = level_code_fast<BITS>(u2.y, d2.y, rb, mid);
+        mb[e] = kMagicBits | level_code_fast<BITS>(u2.x, d2.x, ra, mid);
+        mb[e + 1] = kMagicBits | level_code_fast<BITS>(u2.y, d2.y, rb, mid);
         continue;
       }
       const float2 y2 = __fmul2_rn(d2, r2);
       const float2 m2 = __fadd2_rn(y2, magic2);
       const float2 t2 = __ffma2_rn(__fadd2_rn(m2, nmagic2), neg1, y2);   // y - rint(y)
-      // NaN (an outlier position) compares false
+      // NaN compares false
       near |= (fabsf(t2.x) > kNear ? 1u : 0u) << e;
       near |= (fabsf(t2.y) > kNear ? 1u : 0u) << (e + 1);
       mb[e] = __float_as_uint(m2.x);
@@ -643,6 +656,9 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a, co
       const float xo = __half2float(__ushort_as_half((uint16_t)(ev >> 16)));
       if constexpr (LV) sQ[o * Bk + r] = (uint8_t)level_code_d<BITS>(__fsub_rn(xo, z), sc, s_mid);
       else sQ[o * Bk + r] = (uint8_t)exact_code<BITS>(xo, z, sc, rc);
+      // the staged copy takes the group's zero (an fp16 value): step D then
+      // codes it 0, a clean pattern, before the stored code replaces it
+      sX[sw_off(r, D, c)] = __float2half_rn(z);
     }
     __syncthreads();
   }
