@@ -208,7 +208,7 @@ __device__ __forceinline__ uint32_t level_code_fast(float y, float d, float r, c
 // outlier positions to the group's zero, so every pattern of finite inputs
 // has this form).
 constexpr uint32_t kMagicBits = 0x4B400000u;   // float bits of 1.5 * 2^23
-// 2 and 3 bits: a word is the sum of its patterns shifted into their fields
+// 2, 3 and 4 bits: a word is the sum of its patterns shifted into their fields
 // (one shift-add each, modulo 2^32) less the same shifts of kMagicBits, a
 // compile-time constant; a code that straddles two words adds its high bits
 // to the second from the bare code.
@@ -221,18 +221,7 @@ __host__ __device__ constexpr uint32_t pack_bias(int k) {
 }
 template <int BITS>
 __device__ __forceinline__ void pack_bits(const uint32_t (&mb)[32], uint32_t (&w)[BITS]) {
-  if constexpr (BITS == 4) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint32_t byte[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t lo = mb[8 * k + 2 * j], hi = mb[8 * k + 2 * j + 1];
-        byte[j] = (lo & 0xFu) + (hi << 4);   // byte 0: two codes
-      }
-      w[k] = __byte_perm(__byte_perm(byte[0], byte[1], 0x0040u), __byte_perm(byte[2], byte[3], 0x0040u), 0x5410u);
-    }
-  } else if constexpr (BITS == 8) {
+  if constexpr (BITS == 8) {
 #pragma unroll
     for (int k = 0; k < 8; ++k)   // low byte of each pattern is the code
       w[k] = __byte_perm(__byte_perm(mb[4 * k], mb[4 * k + 1], 0x0040u),
