@@ -634,6 +634,8 @@ def run_levels(args, w, rank, world, device):
     import bit_quantized_kv_append_gb300 as kvq
 
     T = w.T
+    sha = source_sha(DECODE_SOURCES[128] + ["kvq_decode_tc_b2lv.cu", "kvq_decode_tc_b3lv.cu", "kvq_decode_tc_b4lv.cu",
+                                            "kvq_decode_tc_b8lv.cu"])
     Kc, Vc = ki.streams_np(w, [(0, 0)], 1024, layer=9)
     x = np.concatenate([Kc.reshape(-1, w.value_group), Vc.reshape(-1, w.value_group)]).astype(np.float64)
     span = x.max(axis=1, keepdims=True) - x.min(axis=1, keepdims=True)
@@ -691,7 +693,9 @@ def run_levels(args, w, rank, world, device):
                      "peak_source": peak_kind,
                      "kernel": ("decode_tc_kernel, level-table mode (+ decode_combine_kernel)" if w.D == 128
                                 else "decode_levels_kernel + combine (CUDA cores)"),
-                     "alg_bytes_per_launch": alg, "traffic": None},
+                     "alg_bytes_per_launch": alg,
+                     "traffic": profile_traffic(f"decode_tc_kernel_{w.name}_levels.txt", sha) if w.D == 128 else None,
+                     "source_sha": sha},
         "clocks": clk,
     }
 
